@@ -1,0 +1,547 @@
+#!/usr/bin/env python
+"""Benchmark of the paged KV-cache decode hot path on one GB300.
+
+One step = one decode layer-step of the whole hot path over a seeded synthetic
+batch: the new token of every sequence is written into its slot
+(reshape_and_cache), copy-on-write pairs are applied (copy_blocks, when the
+workload has any), and paged_attention_decode (+ its split merge) runs over
+every sequence's context.  The block tables and slot mappings come from the
+C++ block manager (set-up, host).
+
+Default workload: OPT-13B-shaped decode layer (64 sequences, 40 heads x 128,
+fp16 K/V, block size 16, lognormal context lengths with median 300 clipped to
+[1, 2048]); 40 per-layer pools are rotated so consecutive steps read cold K/V
+(each layer's K/V is larger than the 129 MB L2).
+
+Metric: achieved HBM GB/s of algorithmic bytes, where the bytes of a step are
+sum_s ctx_s * H * D * 2 (K and V) * 2 B + q and out (2 * S * H * D * 2 B) +
+the block-table entries read (sum_s ceil(ctx_s / B) * 4 B) + context_lens
+(4 S B) + the new-token write (2 * S * H * D * 2 B read and the same written).
+
+``--impl reference`` times the CPU fp64 oracle (the only reference there is)
+on the host cores over a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_cache_05_gb300 import workloads as W  # noqa: E402
+
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_NOTE = "fallback (MEASURED_PEAKS.json absent): one earlier GB300 copy measurement"
+
+
+# ------------------------------------------------------------------ helpers
+def read_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, copy burst)"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_NOTE
+
+
+def kernel_source_digest() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("decode_kernel.cuh", "decode_api.cu", "pkv_internal.h"):
+        with open(os.path.join(ROOT, "paged_kv_cache_05_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "paged_decode_main_%s.md" % workload)
+    if not os.path.exists(p):
+        return None
+    kv = {}
+    for line in open(p):
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            kv[k.strip()] = v.strip().strip("`")
+    if kv.get("kernel_source_sha256_16") != kernel_source_digest():
+        return None
+    try:
+        return float(kv["dram_bytes_per_launch_full_size"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle-reason sampling while the GPU is busy."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ workload
+class Workload:
+    """Device-resident inputs of one workload plus the algorithmic byte counts."""
+
+    def __init__(self, name: str, device, partition=None, block_size=None, layers=None):
+        import torch
+        import paged_kv_cache_05_gb300 as pkv
+        self.pkv = pkv
+        spec = W.SPECS[name]
+        self.spec = spec
+        self.name = name
+        B = block_size or spec.block_size
+        self.B = B
+        S, H, D = spec.num_seqs, spec.num_heads, spec.head_dim
+        self.S, self.H, self.D = S, H, D
+        self.partition = spec.partition_size if partition is None else partition
+        ctx = W.context_lens(spec)
+        self.ctx_host = ctx
+        nb = W.pool_blocks(spec, ctx, B)
+        self.nb = nb
+        dt = W.torch_dtype(spec.dtype)
+        self.dtype = spec.dtype
+        # block manager: every sequence holds ctx-1 tokens, then one decode
+        # step reserves the slot of its new token (position ctx-1)
+        bm = pkv.BlockManager(nb, B, spec.seed)
+        ids = list(range(S))
+        pairs = np.zeros((0, 2), np.int32)
+        if name == "shared_prefix":
+            p_len, s_len = W.prompt_and_suffix_lens(spec)
+            g = spec.extra["per_group"]
+            for gi in range(len(p_len)):
+                bm.add_sequence(gi * g, int(p_len[gi]))
+                for c in range(1, g):
+                    bm.fork(gi * g, gi * g + c)
+            # all but the last suffix token of each sequence, round-robin; the
+            # copy-on-write pairs this emits (first suffix token of the first
+            # five samples of a group whose prompt ends mid-block) are applied
+            # by copy_blocks in every timed step
+            got = []
+            for t in range(int(s_len.max()) - 1):
+                act = [s for s in ids if t < s_len[s] - 1]
+                sl, pr = bm.append_slots(act)
+                got.append(pr)
+            slots, pr = bm.append_slots(ids)
+            got.append(pr)
+            pairs = np.concatenate(got).astype(np.int32).reshape(-1, 2)
+        else:
+            for s in ids:
+                bm.add_sequence(s, int(ctx[s]) - 1)
+            slots, pairs = bm.append_slots(ids)
+        self.max_blocks = max(1, max(-(-int(c) // B) for c in ctx))
+        tables, ctx2 = bm.export(ids, self.max_blocks)
+        assert np.array_equal(ctx2, ctx)
+        self.tables_host = tables
+        self.slots_host = slots
+        self.pairs_host = pairs
+        self.bm = bm
+        dev = device
+        self.layers = layers or spec.layers
+        self.kc, self.vc = [], []
+        if name == "long":
+            # an 80 GB pool, uninitialised except the blocks the batch uses
+            kc = torch.empty((nb, H, B, D), dtype=dt, device=dev)
+            vc = torch.empty((nb, H, B, D), dtype=dt, device=dev)
+            used = torch.from_numpy(np.unique(np.concatenate(
+                [tables[s, :-(-int(ctx[s]) // B)] for s in ids]))).long().to(dev)
+            for pool, seed in ((kc, spec.seed + 1), (vc, spec.seed + 2)):
+                vals = W.device_normal((used.numel(), H, B, D), spec.dtype, seed, dev)
+                pool.index_copy_(0, used, vals)
+                del vals
+            self.kc.append(kc)
+            self.vc.append(vc)
+        else:
+            for layer in range(self.layers):
+                self.kc.append(W.device_normal((nb, H, B, D), spec.dtype,
+                                               spec.seed * 1000 + 2 * layer, dev))
+                self.vc.append(W.device_normal((nb, H, B, D), spec.dtype,
+                                               spec.seed * 1000 + 2 * layer + 1, dev))
+        self.q = W.device_normal((S, H, D), spec.dtype, spec.seed * 1000 + 900, dev)
+        self.k_new = W.device_normal((S, H, D), spec.dtype, spec.seed * 1000 + 901, dev)
+        self.v_new = W.device_normal((S, H, D), spec.dtype, spec.seed * 1000 + 902, dev)
+        self.out = torch.empty_like(self.q)
+        self.tables = torch.from_numpy(tables).to(dev)
+        self.ctx = torch.from_numpy(ctx).to(dev)
+        self.slots = torch.from_numpy(slots).to(dev)
+        self.pairs = torch.from_numpy(pairs).to(dev)
+        self.ws = pkv.alloc_workspace(S, H, D, B, self.max_blocks, self.partition, dev)
+        self.scale = spec.scale
+        e = 2
+        self.attn_bytes = (int(ctx.astype(np.int64).sum()) * H * D * 2 * e + 2 * S * H * D * e
+                           + sum(-(-int(c) // B) for c in ctx) * 4 + 4 * S)
+        self.reshape_bytes = 2 * (2 * S * H * D * e)
+        self.copy_bytes = len(pairs) * 2 * 2 * H * B * D * e
+        self.step_bytes = self.attn_bytes + self.reshape_bytes + self.copy_bytes
+        self.launches_per_step = 3 + (1 if len(pairs) else 0)
+        self.unique_kv_bytes = None
+        if name == "shared_prefix":
+            blocks = set()
+            for s in ids:
+                blocks.update(tables[s, :-(-int(ctx[s]) // B)].tolist())
+            self.unique_kv_bytes = len(blocks) * H * B * D * 2 * e
+
+    def step(self, i: int, ev=None):
+        pkv = self.pkv
+        layer = i % self.layers
+        kc, vc = self.kc[layer], self.vc[layer]
+        if len(self.pairs_host):
+            pkv.copy_blocks(kc, vc, self.pairs)
+        pkv.reshape_and_cache(self.k_new, self.v_new, kc, vc, self.slots)
+        if ev is not None:
+            ev[0].record()
+        pkv.paged_attention_decode(self.out, self.q, kc, vc, self.tables, self.ctx, self.scale,
+                                   self.partition, self.ws)
+        if ev is not None:
+            ev[1].record()
+
+    def describe(self) -> str:
+        sp = self.spec
+        c = self.ctx_host
+        return ("%s: %d seqs x %d heads x %d, %s K/V, B=%d, ctx %d..%d (sum %d), pool %d blocks"
+                " x %d layer pool(s), split %s" % (
+                    self.name, self.S, self.H, self.D, sp.dtype, self.B, int(c.min()),
+                    int(c.max()), int(c.sum()), self.nb, self.layers,
+                    "balanced" if self.partition == 0 else "%d tokens" % self.partition))
+
+
+# ------------------------------------------------------------------ oracle leg
+def oracle_sample(wl: Workload, max_seconds: float = 20.0):
+    """Host copies of a bounded sample of the workload, for the CPU oracle."""
+    import torch
+    order = np.argsort(wl.ctx_host)          # a spread of lengths: every k-th sequence
+    S = wl.S
+    pick = sorted(order[::max(1, S // 8)].tolist())
+    heads = list(range(wl.H))
+    B = wl.B
+    used = sorted(set(int(b) for s in pick for b in wl.tables_host[s, :-(-int(wl.ctx_host[s]) // B)]))
+    remap = {b: i for i, b in enumerate(used)}
+    idx = torch.tensor(used, dtype=torch.long, device=wl.kc[0].device)
+    kc = W.torch_to_words(wl.kc[0].index_select(0, idx))
+    vc = W.torch_to_words(wl.vc[0].index_select(0, idx))
+    q = W.torch_to_words(wl.q[torch.tensor(pick, device=wl.q.device)])
+    mb = max(1, max(-(-int(wl.ctx_host[s]) // B) for s in pick))
+    bt = np.full((len(pick), mb), -1, np.int32)
+    for i, s in enumerate(pick):
+        n = -(-int(wl.ctx_host[s]) // B)
+        bt[i, :n] = [remap[int(b)] for b in wl.tables_host[s, :n]]
+    cl = wl.ctx_host[pick].astype(np.int32)
+    H, D, e = wl.H, wl.D, 2
+    nbytes = (int(cl.astype(np.int64).sum()) * H * D * 2 * e + 2 * len(pick) * H * D * e
+              + sum(-(-int(c) // B) for c in cl) * 4 + 4 * len(pick))
+    return dict(q=q, kc=kc, vc=vc, bt=bt, cl=cl, bytes=nbytes, seqs=len(pick), heads=len(heads))
+
+
+def run_oracle(sample, scale, dtype, threads):
+    import oracle
+    dt = oracle.F16 if dtype == "f16" else oracle.BF16
+    t0 = time.perf_counter()
+    oracle.paged_attention_decode_threaded(sample["q"], sample["kc"], sample["vc"], sample["bt"],
+                                           sample["cl"], float(np.float32(scale)), dt,
+                                           threads=threads)
+    return time.perf_counter() - t0
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------ main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="opt13b", choices=sorted(W.SPECS))
+    ap.add_argument("--partition", type=int, default=None,
+                    help="split length in tokens (0 = balanced); default: the workload's")
+    ap.add_argument("--block-size", type=int, default=None)
+    ap.add_argument("--layers", type=int, default=None)
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+
+    if args.impl == "reference":
+        return reference_arm(args, world, rank, dist)
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    from paged_kv_cache_05_gb300 import build
+    build.build()
+    wl = Workload(args.workload, device, args.partition, args.block_size, args.layers)
+    stream = torch.cuda.current_stream()
+
+    for i in range(args.warmup):
+        wl.step(i)
+    torch.cuda.synchronize()
+    if wl.pkv.get_device_error() != 0:
+        raise SystemExit("bench.py: device error bits after warm-up")
+
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(device.index if device.index is not None else 0)
+    sampler.start()
+    time.sleep(0.3)                       # let the sampler start before the timed region
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for i in range(K):
+        wl.step(args.warmup + i, evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clocks = sampler.stop()
+    ms_total = t_start.elapsed_time(t_end)
+    attn_ms = [a.elapsed_time(b) for a, b in evs]
+    if dist is not None:
+        t = torch.tensor([ms_total], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / K
+    attn_avg = statistics.mean(attn_ms)
+    attn_med = statistics.median(attn_ms)
+    value = world * wl.step_bytes / (ms_step * 1e-3) / 1e9
+
+    # ---- end to end: host (pinned) inputs -> C ABI -> host output, every step
+    e2e = None
+    if args.e2e_steps > 0:
+        e2e = measure_e2e(wl, args.e2e_steps, device, dist)
+        if dist is not None:
+            t = torch.tensor([e2e["seconds"]], dtype=torch.float64, device=device)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e["seconds"] = float(t.item())
+
+    if wl.pkv.get_device_error() != 0:
+        raise SystemExit("bench.py: device error bits after the timed region")
+
+    peak, peak_note = read_peaks()
+    achieved = wl.attn_bytes / (attn_avg * 1e-3) / 1e9
+    traffic = profiled_traffic(args.workload)
+    line = {
+        "metric": "paged-attn decode: achieved HBM GB/s (% of GB300 peak), us/layer-step at OPT-13B",
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "us_per_layer_step": round(ms_step * 1e3, 2),
+        "attention_us_per_call": round(attn_avg * 1e3, 2),
+        "attention_us_median": round(attn_med * 1e3, 2),
+        "pct_of_peak": round(100 * value / world / peak, 1),
+        "seq_heads_per_s": round(world * wl.S * wl.H / (ms_step * 1e-3), 1),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded; N(0,1) K/V/q, lognormal/uniform context lengths)",
+        "config": {
+            "workload": wl.describe(),
+            "storage": wl.dtype,
+            "num_seqs": wl.S, "num_heads": wl.H, "head_dim": wl.D, "block_size": wl.B,
+            "partition_size": wl.partition,
+            "algorithmic_bytes_per_step": wl.step_bytes,
+            "attention_bytes_per_call": wl.attn_bytes,
+            "l2": "inputs larger than L2: %.0f MB of K/V per layer, %d layer pools rotated" % (
+                wl.attn_bytes / 1e6, wl.layers),
+            "parallelism": "replicas" if world > 1 else "1 GPU",
+        },
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "paged_attention_decode (paged_decode_main + paged_decode_merge)",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": traffic,
+            "peak_source": peak_note,
+        },
+        "gpu_launches": K * wl.launches_per_step,
+        "clocks": clocks,
+    }
+    if wl.unique_kv_bytes is not None:
+        line["config"]["unique_kv_bytes"] = wl.unique_kv_bytes
+    if e2e is not None:
+        line["e2e"] = {"value": round(world * wl.step_bytes / (e2e["seconds"] / e2e["steps"]) / 1e9, 1),
+                       "unit": "GB/s", "h2d_bytes_per_step": e2e["h2d"],
+                       "d2h_bytes_per_step": e2e["d2h"], "steps": e2e["steps"],
+                       "us_per_step": round(1e6 * e2e["seconds"] / e2e["steps"], 2)}
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def measure_e2e(wl: Workload, steps: int, device, dist):
+    """Per step: pinned host inputs -> device (q, new K/V, slots, tables,
+    context lengths), the step's kernels through the C ABI, the output back to
+    pinned host memory, stream synchronised."""
+    import torch
+    host = {n: t.detach().cpu().pin_memory() for n, t in (
+        ("q", wl.q), ("k_new", wl.k_new), ("v_new", wl.v_new), ("slots", wl.slots),
+        ("tables", wl.tables), ("ctx", wl.ctx), ("pairs", wl.pairs))}
+    dev = {n: torch.empty_like(t, device=device) for n, t in host.items()}
+    out_host = torch.empty(wl.out.shape, dtype=wl.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+    pkv = wl.pkv
+
+    def one(i):
+        layer = i % wl.layers
+        for n in host:
+            if host[n].numel():
+                dev[n].copy_(host[n], non_blocking=True)
+        kc, vc = wl.kc[layer], wl.vc[layer]
+        if len(wl.pairs_host):
+            pkv.copy_blocks(kc, vc, dev["pairs"])
+        pkv.reshape_and_cache(dev["k_new"], dev["v_new"], kc, vc, dev["slots"])
+        pkv.paged_attention_decode(wl.out, dev["q"], kc, vc, dev["tables"], dev["ctx"], wl.scale,
+                                   wl.partition, wl.ws)
+        out_host.copy_(wl.out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for i in range(3):
+        one(i)
+    if dist is not None:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for i in range(steps):
+        one(i)
+    sec = time.perf_counter() - t0
+    return {"seconds": sec, "steps": steps, "h2d": h2d, "d2h": d2h}
+
+
+def cpu_baseline(wl: Workload) -> dict:
+    sample = oracle_sample(wl)
+    threads = host_cores()
+    sec = run_oracle(sample, wl.scale, wl.dtype, threads)
+    return {"value": round(sample["bytes"] / sec / 1e9, 4), "unit": "GB/s", "cores": threads,
+            "kind": "oracle",
+            "sample": "%d of %d sequences (every %d-th by length), all %d heads, layer 0; %.2f s" % (
+                sample["seqs"], wl.S, max(1, wl.S // 8), wl.H, sec)}
+
+
+def reference_arm(args, world, rank, dist):
+    """The CPU fp64 oracle as the reference arm, on the host cores."""
+    import torch
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    device = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
+    if device.type == "cuda":
+        from paged_kv_cache_05_gb300 import build
+        build.build()
+        wl = Workload(args.workload, device, args.partition, args.block_size, layers=1)
+        sample = oracle_sample(wl)
+    else:
+        raise SystemExit("bench.py --impl reference: needs the device workload generator")
+    threads = host_cores()
+    for _ in range(min(args.warmup, 1)):
+        run_oracle(sample, wl.scale, wl.dtype, threads)
+    times = [run_oracle(sample, wl.scale, wl.dtype, threads) for _ in range(max(1, min(args.steps, 3)))]
+    sec = statistics.mean(times)
+    v = sample["bytes"] / sec / 1e9
+    line = {
+        "impl": "reference",
+        "metric": "paged-attn decode: achieved HBM GB/s (% of GB300 peak), us/layer-step at OPT-13B",
+        "value": round(v, 4), "unit": "GB/s", "n_gpus": world, "steps": len(times),
+        "warmup": min(args.warmup, 1), "ms_per_step": round(sec * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": wl.describe(), "sample_seqs": sample["seqs"]},
+        "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": "%d of %d sequences, all heads, layer 0" % (sample["seqs"], wl.S)},
+        "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,244 @@
+/*
+ * pagedkv.h -- C ABI of libpagedkv.so: the decode-phase hot path of paged KV
+ * caching (PagedAttention), for NVIDIA GB300 (sm_103a).
+ *
+ * The operations, and where they are defined:
+ *   - pkv_paged_attention_decode: exact single-query attention of every
+ *     sequence over its K/V, which sit in fixed-size blocks scattered through
+ *     a preallocated pool and are reached through a per-sequence block table.
+ *     "Efficient Memory Management for Large Language Model Serving with
+ *     PagedAttention" (wywy.jp notes), glossary entries "PagedAttention" and
+ *     "Block table"; zhaifeiyue.github.io detail page, the block-indexed
+ *     attention formula (paper section 4.1) and its equivalence to standard
+ *     attention; ricepunchb garden "KV Cache Optimization", section 3.3 (each
+ *     block's scores at kernel level, a final reduction completes the softmax).
+ *   - pkv_reshape_and_cache: the write of each new token's K and V into the
+ *     slot the block manager assigned (wywy.jp notes, autoregressive
+ *     generation phase: only the new token's K/V is produced per iteration;
+ *     garden section 3.2: slot = table[pos / B] * B + pos mod B).
+ *   - pkv_copy_blocks: the block engine's block-granular copy used by
+ *     copy-on-write (wywy.jp notes, parallel sampling walkthrough; detail
+ *     page, Memory Management table, "Copy-on-Write: one block").
+ *   - pkv_bm_*: the host KV block manager -- free list, reference counts,
+ *     on-demand allocation, fork and copy-on-write of the last shared block
+ *     (wywy.jp notes, "KV cache manager", "Reference count", "Copy-on-write";
+ *     detail page, Memory Management table: Allocate / Free / Copy-on-Write).
+ *
+ * Memory layout (all 16-bit element types; the pages leave layout open):
+ *   k_cache, v_cache  [num_blocks][num_heads][block_size][head_dim]   one pool each;
+ *                     one physical block id addresses both pools (the paper
+ *                     keeps K and V in separate blocks with their own tables;
+ *                     two identical tables are read as one).
+ *   q, out            [num_seqs][num_heads][head_dim]
+ *   k, v (new tokens) [num_tokens][num_heads][head_dim]
+ *   block_tables      int32 [num_seqs][max_blocks_per_seq]; row s lists the
+ *                     physical blocks of sequence s in logical order; entries
+ *                     past ceil(context_lens[s] / block_size) are never read.
+ *   context_lens      int32 [num_seqs]: tokens sequence s attends (its newest
+ *                     token, the query's own, included).
+ *   slot_mapping      int64 [num_tokens]: physical block * block_size + offset,
+ *                     or a negative value for "do not write".
+ *   pairs             int32 [num_pairs][2] = (src, dst) physical block ids.
+ *
+ * Supported shapes: head_dim 64 or 128; block_size 8, 16, 32 or 64; fp16 or
+ * bf16 storage; fp32 arithmetic; K/V heads == query heads.
+ *
+ * Ownership and execution: every pointer passed to a kernel entry point is a
+ * device pointer owned by the caller and must stay valid until the work on
+ * `stream` completes; calls are asynchronous on `stream`.  The library never
+ * allocates device memory: the decode entry point takes a caller-provided
+ * workspace (size from pkv_decode_workspace_size).  q/out/k/v/caches must be
+ * 16-byte aligned, the workspace 256-byte aligned.
+ *
+ * Errors: argument problems found on the host return PKV_ERR_INVALID and
+ * launch nothing; a failed launch returns PKV_ERR_CUDA; in both cases
+ * pkv_last_error() (thread-local) describes it.  Kernels validate every block
+ * id, slot and context length they use: a bad value is skipped or clamped
+ * (never dereferenced) and sets a bit in the library's device error word,
+ * which pkv_get_device_error reads.  Kernels never wait without a bound: a
+ * wait that runs out sets PKV_DEVERR_TIMEOUT and the kernel returns.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PKV_OK = 0,
+    PKV_ERR_INVALID = 1,   /* bad argument, nothing launched / state unchanged */
+    PKV_ERR_CUDA = 2,      /* a CUDA runtime call or launch failed */
+    PKV_ERR_OOM = 3,       /* block manager: not enough free physical blocks */
+    PKV_ERR_DEVICE = 4     /* pkv_get_device_error found device-side error bits */
+} pkv_status;
+
+typedef enum { PKV_F16 = 0, PKV_BF16 = 1 } pkv_dtype;
+
+/* bits of the device error word */
+#define PKV_DEVERR_BAD_BLOCK   1  /* a block id outside [0, num_blocks) was read */
+#define PKV_DEVERR_BAD_SLOT    2  /* a slot >= num_blocks * block_size was given */
+#define PKV_DEVERR_BAD_CONTEXT 4  /* context_lens[s] < 0 or > max_blocks_per_seq * block_size */
+#define PKV_DEVERR_TIMEOUT     8  /* a bounded wait inside a kernel ran out */
+#define PKV_DEVERR_WORKSPACE  16  /* the workspace was too small for the launch */
+
+/* Largest grid the decode kernel uses (CTAs); bounds the workspace. */
+#define PKV_MAX_GRID 4096
+/* Largest batch of sequences per decode call. */
+#define PKV_MAX_SEQS 16384
+
+/* ------------------------------------------------------------------------ */
+/* Decode attention                                                          */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Bytes of workspace pkv_paged_attention_decode needs for these sizes.
+ * partition_size: split length in tokens of the split-K pass, or 0 for the
+ * balanced split (each CTA of a persistent grid takes an equal share of the
+ * batch's K/V).  A nonzero value must be a positive multiple of the kernel's
+ * step (16 tokens for head_dim 128, 32 for head_dim 64, or block_size if
+ * smaller).  Host only; never touches the GPU.
+ */
+pkv_status pkv_decode_workspace_size(int num_seqs, int num_heads, int head_dim,
+                                     int block_size, int max_blocks_per_seq,
+                                     int partition_size, size_t* bytes);
+
+/*
+ * out[s][h][:] = sum_t softmax_t(scale * q[s][h] . K_s[t][h]) V_s[t][h] over
+ * t < context_lens[s], where K_s[t] = k_cache[block_tables[s][t / B]][h][t % B].
+ * Exact attention (not an approximation); fp32 accumulation, output rounded
+ * to nearest in the storage dtype.  context_lens[s] == 0 gives a zero row.
+ *
+ * Work split: a persistent grid; each CTA streams a contiguous share of the
+ * batch's (sequence, head, K/V step) space, keeps an online-softmax state per
+ * warp, and writes either the final row (when it saw the whole sequence/head)
+ * or a partial (max, sum, unnormalised output) that a second kernel merges
+ * with the log-sum-exp rule.  Two launches on `stream`.
+ *
+ * workspace: device, >= pkv_decode_workspace_size(...) bytes, 256-B aligned;
+ * its contents need no initialisation and are scratch between calls; two
+ * calls in flight at once must not share it.
+ */
+pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* k_cache,
+                                      const void* v_cache, const int32_t* block_tables,
+                                      const int32_t* context_lens, float scale,
+                                      int num_seqs, int num_heads, int head_dim,
+                                      int block_size, int max_blocks_per_seq,
+                                      int64_t num_blocks, pkv_dtype dtype,
+                                      int partition_size, void* workspace,
+                                      size_t workspace_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Cache maintenance                                                         */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * For each token t with slot_mapping[t] >= 0 and each head h:
+ *   k_cache[slot / B][h][slot % B][:] = k[t][h][:]   (same for v)
+ * A bit copy.  Slots within one call must be distinct (else the result for
+ * the duplicated slot is one of the writers').  A slot beyond the pool is
+ * skipped and sets PKV_DEVERR_BAD_SLOT.  num_tokens == 0 launches nothing.
+ */
+pkv_status pkv_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,
+                                 const int64_t* slot_mapping, int num_tokens, int num_heads,
+                                 int head_dim, int block_size, int64_t num_blocks,
+                                 pkv_dtype dtype, cudaStream_t stream);
+
+/*
+ * For each pair p: k_cache[dst] = k_cache[src] and v_cache[dst] = v_cache[src],
+ * whole blocks (all heads).  Destinations must be distinct and must not be the
+ * source of any pair in the same call (copy-on-write always copies into a
+ * freshly allocated block, so this holds for pairs the block manager emits).
+ * A bad id skips the pair and sets PKV_DEVERR_BAD_BLOCK.
+ * num_pairs == 0 launches nothing.
+ */
+pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_pairs,
+                           int num_heads, int head_dim, int block_size, int64_t num_blocks,
+                           pkv_dtype dtype, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Errors                                                                    */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Synchronises `stream`, then reads the device error word of the current
+ * device into *bits (PKV_DEVERR_* bits, 0 = none) and, if clear != 0, resets
+ * it.  Returns PKV_ERR_DEVICE when bits != 0, PKV_OK otherwise.
+ */
+pkv_status pkv_get_device_error(int32_t* bits, int clear, cudaStream_t stream);
+
+/* Thread-local description of the last non-OK status of this thread. */
+const char* pkv_last_error(void);
+
+/* Library version string. */
+const char* pkv_version(void);
+
+/* ------------------------------------------------------------------------ */
+/* Host block manager (host memory only; not thread-safe per handle)          */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Policy: the free list starts as a seeded permutation of [0, num_blocks)
+ * (Fisher-Yates driven by SplitMix64(seed), j = next() mod (i + 1) for
+ * i = n-1 .. 1); allocation pops its front; a block whose count drops to zero
+ * is pushed to its back (in block-table order).  A new block is allocated
+ * only when the sequence's last block is full; writing into a partially
+ * filled last block whose reference count is above one allocates a new block,
+ * emits the (old, new) copy pair and decrements the old block's count.
+ * Every failing call leaves the manager unchanged.
+ */
+typedef struct pkv_bm pkv_bm;
+
+pkv_status pkv_bm_create(int64_t num_blocks, int block_size, uint64_t seed, pkv_bm** out);
+void pkv_bm_destroy(pkv_bm* bm);
+
+/* New sequence holding prompt_len tokens: allocates ceil(prompt_len / B)
+ * blocks; writes the prompt tokens' slots to slots_out[prompt_len] (may be
+ * NULL).  PKV_ERR_INVALID if seq_id exists; PKV_ERR_OOM if blocks run out. */
+pkv_status pkv_bm_add_sequence(pkv_bm* bm, int64_t seq_id, int32_t prompt_len,
+                               int64_t* slots_out);
+
+/* child shares every block of parent (each block's count + 1). */
+pkv_status pkv_bm_fork(pkv_bm* bm, int64_t parent, int64_t child);
+
+/* Reserve the slot of the sequence's next token.  *cow_src / *cow_dst are the
+ * copy pair the caller must apply (pkv_copy_blocks) before writing, or -1. */
+pkv_status pkv_bm_append_slot(pkv_bm* bm, int64_t seq_id, int64_t* slot, int32_t* cow_src,
+                              int32_t* cow_dst);
+
+/* One decode step for n sequences, in order: slots[n]; copy pairs into
+ * pairs[n][2] (at most one per sequence), their number in *num_pairs.
+ * All-or-nothing: on failure the manager is unchanged. */
+pkv_status pkv_bm_append_slots(pkv_bm* bm, const int64_t* seq_ids, int n, int64_t* slots,
+                               int32_t* pairs, int32_t* num_pairs);
+
+/* Release every block of the sequence (count - 1; zero -> free list). */
+pkv_status pkv_bm_free_sequence(pkv_bm* bm, int64_t seq_id);
+
+/* Copy the sequence's block table into out[cap]; *n = its length.
+ * PKV_ERR_INVALID if cap is too small (nothing written). */
+pkv_status pkv_bm_block_table(const pkv_bm* bm, int64_t seq_id, int32_t* out, int32_t cap,
+                              int32_t* n);
+
+/* Tokens held by the sequence. */
+pkv_status pkv_bm_context_len(const pkv_bm* bm, int64_t seq_id, int32_t* n);
+
+/* Decode-call inputs for n sequences: tables[n][max_blocks] (unused entries
+ * set to -1) and context_lens[n].  PKV_ERR_INVALID if a table is longer than
+ * max_blocks or a sequence is unknown. */
+pkv_status pkv_bm_export(const pkv_bm* bm, const int64_t* seq_ids, int n, int32_t* tables,
+                         int32_t max_blocks, int32_t* context_lens);
+
+/* Reference count of a block (-1 if out of range); number of free blocks. */
+int32_t pkv_bm_refcount(const pkv_bm* bm, int32_t block);
+int64_t pkv_bm_num_free(const pkv_bm* bm);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

@@ -1,0 +1,13 @@
+"""GB300-native paged KV-cache decode path (PagedAttention) behind a C ABI.
+
+The compute lives in libpagedkv.so (CUDA kernels for sm_103a plus the C++
+block manager); ``pagedkv`` is its thin ctypes binding and ``workloads`` the
+seeded synthetic inputs.  Build with ``python -m paged_kv_cache_05_gb300.build``.
+"""
+from .pagedkv import (BlockManager, OutOfBlocks, PagedKVError, alloc_workspace, copy_blocks,
+                      decode_workspace_size, get_device_error, lib, paged_attention_decode,
+                      reshape_and_cache, version)
+
+__all__ = ["BlockManager", "OutOfBlocks", "PagedKVError", "alloc_workspace", "copy_blocks",
+           "decode_workspace_size", "get_device_error", "lib", "paged_attention_decode",
+           "reshape_and_cache", "version"]

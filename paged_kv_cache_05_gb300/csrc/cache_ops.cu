@@ -1,0 +1,176 @@
+// Cache maintenance kernels: the new-token write (reshape_and_cache) and the
+// block-granular copy used by copy-on-write (copy_blocks).
+//
+// Both are pure bit copies bound by HBM bandwidth: 16-byte vector loads and
+// stores, consecutive threads on consecutive 16-byte pieces of a row.
+#include <cuda_runtime.h>
+
+#include "pkv_internal.h"
+
+namespace {
+
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+// One thread per (token, head, 16-byte piece): copies that piece of K and of V.
+// Destination: slot / B is the physical block, slot % B the offset inside it
+// (ricepunchb garden, section 3.2).
+__global__ void __launch_bounds__(256) reshape_and_cache_kernel(
+    const uint4* __restrict__ k, const uint4* __restrict__ v, uint4* __restrict__ k_cache,
+    uint4* __restrict__ v_cache, const int64_t* __restrict__ slots, int T, int H, int vecs_per_row,
+    int B, int64_t num_slots, int32_t* err) {
+    const int64_t total = (int64_t)T * H * vecs_per_row;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t row = i / vecs_per_row;          // token * H + head
+        const int piece = (int)(i - row * vecs_per_row);
+        const int t = (int)(row / H);
+        const int h = (int)(row - (int64_t)t * H);
+        const int64_t slot = slots[t];
+        if (slot < 0) continue;
+        if (slot >= num_slots) {
+            if (h == 0 && piece == 0) atomicOr(err, PKV_DEVERR_BAD_SLOT);
+            continue;
+        }
+        const int64_t blk = slot / B, off = slot - blk * B;
+        const int64_t dst = ((blk * H + h) * B + off) * vecs_per_row + piece;
+        const uint4 kv = ld_nc_v4(k + i);
+        const uint4 vv = ld_nc_v4(v + i);
+        k_cache[dst] = kv;
+        v_cache[dst] = vv;
+    }
+}
+
+// grid = (pieces, pairs, 2): blockIdx.z picks the K or the V pool; each thread
+// moves kUnroll 16-byte vectors of the whole-block copy src -> dst.
+constexpr int kCopyThreads = 256;
+constexpr int kCopyUnroll = 4;
+
+__global__ void __launch_bounds__(kCopyThreads) copy_blocks_kernel(
+    uint4* __restrict__ k_cache, uint4* __restrict__ v_cache, const int32_t* __restrict__ pairs,
+    int64_t vecs_per_block, int64_t num_blocks, int32_t* err) {
+    const int p = blockIdx.y;
+    const int64_t src = pairs[2 * p], dst = pairs[2 * p + 1];
+    if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+        if (blockIdx.x == 0 && blockIdx.z == 0 && threadIdx.x == 0)
+            atomicOr(err, PKV_DEVERR_BAD_BLOCK);
+        return;
+    }
+    uint4* pool = blockIdx.z == 0 ? k_cache : v_cache;
+    const uint4* s = pool + src * vecs_per_block;
+    uint4* d = pool + dst * vecs_per_block;
+    const int64_t base = (int64_t)blockIdx.x * kCopyThreads * kCopyUnroll + threadIdx.x;
+    uint4 buf[kCopyUnroll];
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+        const int64_t i = base + (int64_t)u * kCopyThreads;
+        if (i < vecs_per_block) buf[u] = ld_nc_v4(s + i);
+    }
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+        const int64_t i = base + (int64_t)u * kCopyThreads;
+        if (i < vecs_per_block) d[i] = buf[u];
+    }
+}
+
+}  // namespace
+
+namespace pkv {
+
+cudaError_t launch_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,
+                                     const int64_t* slots, int T, int H, int D, int B,
+                                     int64_t num_blocks, int32_t* err, cudaStream_t stream) {
+    const int vecs = D / 8;
+    const int64_t total = (int64_t)T * H * vecs;
+    int64_t blocks = (total + 255) / 256;
+    if (blocks > 65535LL * 16) blocks = 65535LL * 16;
+    reshape_and_cache_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
+        static_cast<const uint4*>(k), static_cast<const uint4*>(v), static_cast<uint4*>(k_cache),
+        static_cast<uint4*>(v_cache), slots, T, H, vecs, B, num_blocks * B, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int P, int H,
+                               int D, int B, int64_t num_blocks, int32_t* err,
+                               cudaStream_t stream) {
+    const int64_t vecs = (int64_t)H * B * D / 8;
+    const int64_t per_cta = kCopyThreads * kCopyUnroll;
+    dim3 grid((unsigned)((vecs + per_cta - 1) / per_cta), (unsigned)P, 2);
+    copy_blocks_kernel<<<grid, kCopyThreads, 0, stream>>>(static_cast<uint4*>(k_cache),
+                                                         static_cast<uint4*>(v_cache), pairs,
+                                                         vecs, num_blocks, err);
+    return cudaGetLastError();
+}
+
+}  // namespace pkv
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+pkv_status check_common(int H, int D, int B, int64_t num_blocks, pkv_dtype dtype,
+                        const char* fn) {
+    if (H < 1) return pkv::fail(PKV_ERR_INVALID, "%s: num_heads must be >= 1", fn);
+    if (D != 64 && D != 128) return pkv::fail(PKV_ERR_INVALID, "%s: head_dim must be 64 or 128", fn);
+    if (B != 8 && B != 16 && B != 32 && B != 64)
+        return pkv::fail(PKV_ERR_INVALID, "%s: block_size must be 8, 16, 32 or 64", fn);
+    if (num_blocks < 1) return pkv::fail(PKV_ERR_INVALID, "%s: num_blocks must be >= 1", fn);
+    if (dtype != PKV_F16 && dtype != PKV_BF16)
+        return pkv::fail(PKV_ERR_INVALID, "%s: unknown dtype", fn);
+    return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,
+                                 const int64_t* slot_mapping, int num_tokens, int num_heads,
+                                 int head_dim, int block_size, int64_t num_blocks,
+                                 pkv_dtype dtype, cudaStream_t stream) {
+    const char* fn = "pkv_reshape_and_cache";
+    pkv_status st = check_common(num_heads, head_dim, block_size, num_blocks, dtype, fn);
+    if (st != PKV_OK) return st;
+    if (num_tokens < 0) return pkv::fail(PKV_ERR_INVALID, "%s: num_tokens < 0", fn);
+    if (num_tokens == 0) return PKV_OK;
+    if (!k || !v || !k_cache || !v_cache || !slot_mapping)
+        return pkv::fail(PKV_ERR_INVALID, "%s: NULL pointer", fn);
+    if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache))
+        return pkv::fail(PKV_ERR_INVALID, "%s: k, v and the caches must be 16-byte aligned", fn);
+    if ((reinterpret_cast<uintptr_t>(slot_mapping) & 7) != 0)
+        return pkv::fail(PKV_ERR_INVALID, "%s: slot_mapping must be 8-byte aligned", fn);
+    int32_t* err = pkv::device_error_word();
+    if (!err) return pkv::fail(PKV_ERR_CUDA, "%s: no CUDA device", fn);
+    cudaError_t e = pkv::launch_reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, num_tokens,
+                                                  num_heads, head_dim, block_size, num_blocks, err,
+                                                  stream);
+    if (e != cudaSuccess) return pkv::cuda_fail(e, fn);
+    return PKV_OK;
+}
+
+pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_pairs,
+                           int num_heads, int head_dim, int block_size, int64_t num_blocks,
+                           pkv_dtype dtype, cudaStream_t stream) {
+    const char* fn = "pkv_copy_blocks";
+    pkv_status st = check_common(num_heads, head_dim, block_size, num_blocks, dtype, fn);
+    if (st != PKV_OK) return st;
+    if (num_pairs < 0 || num_pairs > 65535)
+        return pkv::fail(PKV_ERR_INVALID, "%s: num_pairs must be in [0, 65535]", fn);
+    if (num_pairs == 0) return PKV_OK;
+    if (!k_cache || !v_cache || !pairs) return pkv::fail(PKV_ERR_INVALID, "%s: NULL pointer", fn);
+    if (!aligned16(k_cache) || !aligned16(v_cache))
+        return pkv::fail(PKV_ERR_INVALID, "%s: the caches must be 16-byte aligned", fn);
+    int32_t* err = pkv::device_error_word();
+    if (!err) return pkv::fail(PKV_ERR_CUDA, "%s: no CUDA device", fn);
+    cudaError_t e = pkv::launch_copy_blocks(k_cache, v_cache, pairs, num_pairs, num_heads,
+                                            head_dim, block_size, num_blocks, err, stream);
+    if (e != cudaSuccess) return pkv::cuda_fail(e, fn);
+    return PKV_OK;
+}
+
+}  // extern "C"

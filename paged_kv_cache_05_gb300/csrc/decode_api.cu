@@ -1,0 +1,164 @@
+// C ABI of the decode attention: argument checks, workspace sizing, grid choice.
+#include <cmath>
+#include <mutex>
+
+#include "pkv_internal.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+// Lower bound of a balanced chunk, in steps: keeps tiny batches from being cut
+// into one-step pieces that would all need the merge pass.
+constexpr int kMinChunkSteps = 8;
+
+struct OccEntry {
+    const pkv::DecodeKernel* k;
+    size_t smem;
+    int ctas;
+};
+
+std::mutex g_mu;
+OccEntry g_occ[kMaxDevices][8] = {};
+
+// CTAs per SM for kernel k with `smem` bytes, cached per device (it also sets
+// the kernel's dynamic shared memory limit on first use on a device).
+cudaError_t ctas_per_sm(const pkv::DecodeKernel* k, int dev, size_t smem, int* out) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    OccEntry* row = g_occ[dev];
+    for (int i = 0; i < 8; ++i)
+        if (row[i].k == k && row[i].smem == smem) {
+            *out = row[i].ctas;
+            return cudaSuccess;
+        }
+    int n = 0;
+    cudaError_t e = k->occupancy(&n, smem);
+    if (e != cudaSuccess) return e;
+    for (int i = 7; i > 0; --i) row[i] = row[i - 1];
+    row[0] = {k, smem, n};
+    *out = n;
+    return cudaSuccess;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Host-only checks shared by the workspace query and the launch.
+pkv_status check_shape(int S, int H, int D, int B, int max_blocks, int partition_size,
+                       const char* fn) {
+    if (S < 0 || S > PKV_MAX_SEQS)
+        return pkv::fail(PKV_ERR_INVALID, "%s: num_seqs must be in [0, %d]", fn, PKV_MAX_SEQS);
+    if (H < 1) return pkv::fail(PKV_ERR_INVALID, "%s: num_heads must be >= 1", fn);
+    if (D != 64 && D != 128) return pkv::fail(PKV_ERR_INVALID, "%s: head_dim must be 64 or 128", fn);
+    if (B != 8 && B != 16 && B != 32 && B != 64)
+        return pkv::fail(PKV_ERR_INVALID, "%s: block_size must be 8, 16, 32 or 64", fn);
+    if (max_blocks < 1) return pkv::fail(PKV_ERR_INVALID, "%s: max_blocks_per_seq must be >= 1", fn);
+    const int sub = pkv::step_tokens(D, B);
+    const int64_t steps = (int64_t)S * max_blocks * (B / sub);
+    if (steps >= (1LL << 31) || steps * H >= (1LL << 62))
+        return pkv::fail(PKV_ERR_INVALID, "%s: batch too large (step count overflows)", fn);
+    if (partition_size < 0 || (partition_size > 0 && partition_size % sub != 0))
+        return pkv::fail(PKV_ERR_INVALID,
+                         "%s: partition_size must be 0 or a positive multiple of %d tokens", fn,
+                         sub);
+    return PKV_OK;
+}
+
+int64_t max_chunks(int S, int H, int D, int B, int max_blocks, int partition_size) {
+    if (partition_size == 0) return PKV_MAX_GRID;
+    const int sub = pkv::step_tokens(D, B);
+    const int64_t L = partition_size / sub;
+    const int64_t steps = (int64_t)S * H * max_blocks * (B / sub);
+    return (steps + L - 1) / L;
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_decode_workspace_size(int num_seqs, int num_heads, int head_dim, int block_size,
+                                     int max_blocks_per_seq, int partition_size, size_t* bytes) {
+    const char* fn = "pkv_decode_workspace_size";
+    if (!bytes) return pkv::fail(PKV_ERR_INVALID, "%s: bytes is NULL", fn);
+    pkv_status st = check_shape(num_seqs, num_heads, head_dim, block_size, max_blocks_per_seq,
+                                partition_size, fn);
+    if (st != PKV_OK) return st;
+    const int64_t mc = max_chunks(num_seqs, num_heads, head_dim, block_size, max_blocks_per_seq,
+                                  partition_size);
+    *bytes = pkv::ws_layout(num_seqs, num_heads, head_dim, mc).total;
+    return PKV_OK;
+}
+
+pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* k_cache,
+                                      const void* v_cache, const int32_t* block_tables,
+                                      const int32_t* context_lens, float scale, int num_seqs,
+                                      int num_heads, int head_dim, int block_size,
+                                      int max_blocks_per_seq, int64_t num_blocks,
+                                      pkv_dtype dtype, int partition_size, void* workspace,
+                                      size_t workspace_bytes, cudaStream_t stream) {
+    const char* fn = "pkv_paged_attention_decode";
+    pkv_status st = check_shape(num_seqs, num_heads, head_dim, block_size, max_blocks_per_seq,
+                                partition_size, fn);
+    if (st != PKV_OK) return st;
+    if (num_blocks < 1) return pkv::fail(PKV_ERR_INVALID, "%s: num_blocks must be >= 1", fn);
+    if (dtype != PKV_F16 && dtype != PKV_BF16)
+        return pkv::fail(PKV_ERR_INVALID, "%s: unknown dtype", fn);
+    if (!std::isfinite(scale)) return pkv::fail(PKV_ERR_INVALID, "%s: scale is not finite", fn);
+    if (num_seqs == 0) return PKV_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !workspace)
+        return pkv::fail(PKV_ERR_INVALID, "%s: NULL pointer", fn);
+    if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+        return pkv::fail(PKV_ERR_INVALID, "%s: out, q and the caches must be 16-byte aligned", fn);
+    if (!aligned(block_tables, 4) || !aligned(context_lens, 4))
+        return pkv::fail(PKV_ERR_INVALID, "%s: int32 arrays must be 4-byte aligned", fn);
+    if (!aligned(workspace, 256))
+        return pkv::fail(PKV_ERR_INVALID, "%s: workspace must be 256-byte aligned", fn);
+    const int64_t mc = max_chunks(num_seqs, num_heads, head_dim, block_size, max_blocks_per_seq,
+                                  partition_size);
+    const pkv::WsLayout wl = pkv::ws_layout(num_seqs, num_heads, head_dim, mc);
+    if (workspace_bytes < wl.total)
+        return pkv::fail(PKV_ERR_INVALID, "%s: workspace too small (%zu < %zu bytes)", fn,
+                         workspace_bytes, wl.total);
+
+    const pkv::DecodeKernel* k = dtype == PKV_F16 ? pkv::decode_kernel_f16(head_dim, block_size)
+                                                  : pkv::decode_kernel_bf16(head_dim, block_size);
+    if (!k) return pkv::fail(PKV_ERR_INVALID, "%s: unsupported head_dim/block_size", fn);
+
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return pkv::cuda_fail(e, fn);
+    if (dev < 0 || dev >= kMaxDevices) return pkv::fail(PKV_ERR_INVALID, "%s: device id", fn);
+    const size_t smem = k->smem_bytes(num_seqs);
+    int per_sm = 0;
+    e = ctas_per_sm(k, dev, smem, &per_sm);
+    if (e != cudaSuccess) return pkv::cuda_fail(e, "pkv_paged_attention_decode: occupancy");
+    if (per_sm < 1)
+        return pkv::fail(PKV_ERR_INVALID, "%s: %d sequences need %zu bytes of shared memory", fn,
+                         num_seqs, smem);
+    int grid = pkv::sm_count(dev) * per_sm;
+    if (grid < 1) return pkv::fail(PKV_ERR_CUDA, "%s: no multiprocessors", fn);
+    if (grid > PKV_MAX_GRID) grid = PKV_MAX_GRID;
+    int32_t* err = pkv::device_error_word();
+    if (!err) return pkv::fail(PKV_ERR_CUDA, "%s: no device error word", fn);
+
+    pkv::DecodeArgs a;
+    a.out = out;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.S = num_seqs;
+    a.H = num_heads;
+    a.max_blocks = max_blocks_per_seq;
+    a.num_blocks = num_blocks;
+    a.L_steps = partition_size > 0 ? partition_size / pkv::step_tokens(head_dim, block_size) : 0;
+    a.min_chunk_steps = kMinChunkSteps;
+    a.ws = static_cast<char*>(workspace);
+    a.ws_l = wl;
+    a.err = err;
+    e = k->launch(a, grid, stream);
+    if (e != cudaSuccess) return pkv::cuda_fail(e, fn);
+    return PKV_OK;
+}
+
+}  // extern "C"

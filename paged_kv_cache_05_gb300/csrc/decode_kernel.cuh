@@ -1,0 +1,680 @@
+// Paged decode attention for sm_103a.
+//
+// What it computes (the block-indexed attention of the PagedAttention paper,
+// section 4.1, as printed on the zhaifeiyue.github.io detail page, and the
+// ricepunchb garden's section 3.3: per-block scores at kernel level, then a
+// reduction that completes the softmax):
+//
+//   out[s][h] = sum_t softmax_t(scale * q[s][h] . K[t]) V[t],  t < ctx[s],
+//   K[t] = k_cache[table[s][t / B]][h][t % B]  (V likewise).
+//
+// Design (GB300-first; the pages' A100 kernel notes are prior art only):
+//   * The batch's work is the ordered space of steps (s, h, j): step j of
+//     (sequence s, head h) covers SUB consecutive tokens of one physical
+//     block (SUB = 16 for head_dim 128), i.e. one contiguous K chunk and one
+//     contiguous V chunk of at most 4 KiB each in the [block][head][B][D]
+//     pools.  A persistent grid (a few CTAs per SM) splits that space into
+//     equal contiguous ranges, so every CTA moves the same number of bytes
+//     whatever the mix of context lengths (split-K with balanced splits), or
+//     into fixed-length chunks when a split length is requested.
+//   * Per CTA: one producer warp walks its range, reads block-table entries
+//     32 at a time (and prefetches the next 32), and issues 1-D TMA bulk
+//     copies (cp.async.bulk) of each step's K and V chunk into a ring of
+//     shared-memory stages guarded by mbarriers (full: transaction bytes;
+//     empty: released by the consuming warp).  No multicast: every CTA
+//     fetches its own blocks.
+//   * Four consumer warps take the steps round-robin.  Per step a warp reads
+//     the K chunk from shared memory with conflict-free 16-byte loads (lane l
+//     reads bytes [16 l, 16 l + 16) of every 512-byte row), forms q . k
+//     partial dot products in fp32, and finishes them with a reduce-scatter
+//     butterfly (8 shuffles for 16 tokens) that leaves each lane holding one
+//     token's score.  An online softmax (running max m, running sum l, both
+//     in log2 units) rescales the fp32 accumulator, and the V chunk is
+//     accumulated with the per-token weights.  Masked positions (>= ctx) are
+//     excluded by selection, never by multiplying, so unwritten pool memory
+//     (any bit pattern) cannot leak into the result.
+//   * At the end of each piece (a (s, h) run inside one chunk) the warps'
+//     states are merged through shared memory.  A piece that covers its whole
+//     (s, h) writes the normalised output; otherwise it writes (m, l, acc) to
+//     workspace slot s*H + h + chunk, and the merge kernel combines the
+//     slots of each split (s, h) with the log-sum-exp rule.
+//   * CUDA cores, not tensor cores: decode attention is a matrix-vector
+//     product, about 0.5 flop per byte of K/V, bound by HBM bandwidth.
+//   * Every wait is bounded (1 s); a wait that runs out sets a device error
+//     bit and the CTA winds down (after draining its copies in flight).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace dec {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
+constexpr uint32_t kWaitLimitIters = 1u << 26;
+
+// ---------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// 1-D bulk copy global -> this CTA's shared memory, completion counted in
+// bytes on `bar`.  Both addresses 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+// Wait for the phase of `bar` with the given parity to complete.  Gives up
+// (returns false) after kWaitLimitNs, after kWaitLimitIters polls, or, when
+// `abort` is given, once *abort becomes nonzero.
+static __device__ __noinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t it = 1; it < kWaitLimitIters; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 31) == 0) {
+            if (abort && *abort) return false;
+            if (global_ns() - t0 > kWaitLimitNs) return false;
+        }
+    }
+    return false;
+}
+
+// ------------------------------------------------------------ element types
+template <typename T>
+struct Elem;
+
+template <>
+struct Elem<__half> {
+    static __device__ __forceinline__ void to_f32x8(const uint4& u, float (&f)[8]) {
+        const __half2* h = reinterpret_cast<const __half2*>(&u);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 t = __half22float2(h[i]);
+            f[2 * i] = t.x;
+            f[2 * i + 1] = t.y;
+        }
+    }
+    static __device__ __forceinline__ __half from_f32(float x) { return __float2half_rn(x); }
+    static __device__ __forceinline__ __half zero() { return __float2half_rn(0.f); }
+};
+
+template <>
+struct Elem<__nv_bfloat16> {
+    static __device__ __forceinline__ void to_f32x8(const uint4& u, float (&f)[8]) {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+    static __device__ __forceinline__ __nv_bfloat16 from_f32(float x) {
+        return __float2bfloat16_rn(x);
+    }
+    static __device__ __forceinline__ __nv_bfloat16 zero() { return __float2bfloat16_rn(0.f); }
+};
+
+constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
+
+// ------------------------------------------------------------ configuration
+template <int D, int B>
+struct Cfg {
+    static constexpr int NW = 4;                        // consumer warps
+    static constexpr int THREADS = (NW + 1) * 32;       // + one producer warp
+    static constexpr int SUB = step_tokens(D, B);       // tokens per step
+    static constexpr int SPB = B / SUB;                 // steps per block
+    static constexpr int CHUNK = SUB * D * 2;           // bytes of K (or V) per step
+    static constexpr int STAGE = 2 * CHUNK;
+    static constexpr int NSTAGE = 98304 / STAGE;        // ~96 KiB ring
+    static constexpr int NL = CHUNK / 512;              // 16-B loads per lane per chunk
+    static constexpr int TPL = 256 / D;                 // tokens per 512-B row
+    static constexpr int LPT = D / 8;                   // lanes per token row
+    static constexpr int LOG_LPT = ilog2(LPT);
+    static constexpr int LOG_NL = ilog2(NL);
+    static constexpr int RS = LOG_LPT - LOG_NL;
+    static constexpr int MROW = D + 4;                  // merge row: acc[D], m, l, pad
+    static constexpr size_t RING = (size_t)NSTAGE * STAGE;
+    static constexpr size_t BAR_OFF = RING;
+    static constexpr size_t MERGE_OFF = BAR_OFF + 16 * (size_t)NSTAGE;
+    static constexpr size_t MISC_OFF = MERGE_OFF + 4 * (size_t)(2 * NW * MROW);
+    static constexpr size_t CTX_OFF = MISC_OFF + 64;
+    static_assert(NL >= 1 && NL <= LPT, "step layout");
+    static_assert(TPL * NL == SUB, "tokens per step");
+    static_assert(B % SUB == 0, "steps per block");
+    static_assert(NW * 32 >= D, "merge: one thread per output element");
+    static __host__ __device__ size_t smem(int S) {
+        return CTX_OFF + 4 * (size_t)S + 4 * (size_t)(S + 1);
+    }
+};
+
+// ------------------------------------------------------------ warp reductions
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+    return v;
+}
+
+// NL partial dot products, one per 16-B load, each spread over the LPT lanes
+// of a token row.  Halving exchanges on lane bits LOG_LPT-1, LOG_LPT-2, ...
+// leave lane (dl = lane mod LPT) with the full dot product of load
+// dl >> (LOG_LPT - LOG_NL); plain butterflies on the remaining low bits make
+// the 2^RS lanes that share a load agree bit for bit.
+template <int NL, int LOG_LPT>
+__device__ __forceinline__ float reduce_scatter(float (&v)[NL], int dl) {
+    constexpr int LOG_NL = ilog2(NL);
+#pragma unroll
+    for (int step = 0; step < LOG_NL; ++step) {
+        const int bit = LOG_LPT - 1 - step;
+        const int half = (NL >> step) >> 1;
+        const bool upper = (dl >> bit) & 1;
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+            const float keep = upper ? v[half + i] : v[i];
+            const float give = upper ? v[i] : v[half + i];
+            v[i] = keep + __shfl_xor_sync(kFull, give, 1 << bit);
+        }
+    }
+    float z = v[0];
+#pragma unroll
+    for (int bit = LOG_LPT - LOG_NL - 1; bit >= 0; --bit) z += __shfl_xor_sync(kFull, z, 1 << bit);
+    return z;
+}
+
+// ------------------------------------------------------------ the step space
+struct Pos {
+    int s, h, j;
+};
+
+// Largest s with H * base[s] <= x; requires x < H * base[S] (so that
+// sequence s has at least one step).
+__device__ __forceinline__ Pos locate(int64_t x, const int* base, int S, int H) {
+    int lo = 0, hi = S - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((int64_t)H * base[mid] <= x) lo = mid;
+        else hi = mid - 1;
+    }
+    const int ns = base[lo + 1] - base[lo];
+    const int64_t r = x - (int64_t)H * base[lo];
+    Pos p;
+    p.s = lo;
+    p.h = (int)(r / ns);
+    p.j = (int)(r - (int64_t)p.h * ns);
+    return p;
+}
+
+__device__ __forceinline__ void next_segment(Pos& p, const int* base, int S, int H) {
+    p.j = 0;
+    if (++p.h == H) {
+        p.h = 0;
+        do {
+            ++p.s;
+        } while (p.s < S && base[p.s + 1] == base[p.s]);
+    }
+}
+
+// Exclusive prefix of steps per sequence: base[s] = sum_{s' < s} ceil(ctx[s'] / SUB).
+template <int SUB>
+__device__ void scan_steps(const int* ctx, int* base, int S, int* scratch) {
+    const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, w = tid >> 5;
+    const int per = (S + nt - 1) / nt;
+    const int b = min(tid * per, S), e = min(b + per, S);
+    int local = 0;
+    for (int i = b; i < e; ++i) local += (ctx[i] + SUB - 1) / SUB;
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) scratch[w] = incl;
+    __syncthreads();
+    int run = incl - local;
+    for (int i = 0; i < w; ++i) run += scratch[i];
+    for (int i = b; i < e; ++i) {
+        base[i] = run;
+        run += (ctx[i] + SUB - 1) / SUB;
+    }
+    if (tid == nt - 1) base[S] = run;
+    __syncthreads();
+}
+
+// ------------------------------------------------------------ the main kernel
+template <typename T, int D, int B>
+__global__ void __launch_bounds__(Cfg<D, B>::THREADS) paged_decode_main(const DecodeArgs a) {
+    using C = Cfg<D, B>;
+    extern __shared__ __align__(1024) unsigned char smem[];
+    unsigned char* ring = smem;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+    uint64_t* empty = full + C::NSTAGE;
+    float* merge = reinterpret_cast<float*>(smem + C::MERGE_OFF);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF);
+    int* scratch = reinterpret_cast<int*>(smem + C::MISC_OFF) + 4;   // 8 ints
+    int* s_ctx = reinterpret_cast<int*>(smem + C::CTX_OFF);
+    int* s_base = s_ctx + a.S;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int S = a.S, H = a.H;
+
+    // 1. context lengths (validated and clamped) and the step prefix
+    const int cap = a.max_blocks * B;
+    for (int s = tid; s < S; s += C::THREADS) {
+        int c = a.context_lens[s];
+        if (c < 0 || c > cap) {
+            atomicOr(a.err, PKV_DEVERR_BAD_CONTEXT);
+            c = c < 0 ? 0 : cap;
+        }
+        s_ctx[s] = c;
+    }
+    if (tid == 0) {
+        for (int i = 0; i < C::NSTAGE; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        fence_mbar_init();
+        *abort_flag = 0;
+    }
+    __syncthreads();
+    scan_steps<C::SUB>(s_ctx, s_base, S, scratch);
+
+    // 2. this CTA's range of the step space
+    const int64_t total = (int64_t)H * s_base[S];
+    int64_t L = a.L_steps;
+    if (L <= 0) {
+        L = (total + gridDim.x - 1) / gridDim.x;
+        if (L < a.min_chunk_steps) L = a.min_chunk_steps;
+    }
+    const int64_t K = (total + L - 1) / L;
+    const bool ws_ok = (int64_t)S * H + K <= a.ws_l.cap;
+    if (blockIdx.x == 0) {
+        int64_t* hdr = reinterpret_cast<int64_t*>(a.ws);
+        int* wbase = reinterpret_cast<int*>(a.ws + a.ws_l.base_off);
+        for (int i = tid; i <= S; i += C::THREADS) wbase[i] = s_base[i];
+        if (tid == 0) {
+            hdr[0] = ws_ok ? L : 0;
+            hdr[1] = total;
+            if (!ws_ok) atomicOr(a.err, PKV_DEVERR_WORKSPACE);
+        }
+    }
+    if (!ws_ok || total == 0) return;
+    const int64_t kb = (int64_t)blockIdx.x * K / gridDim.x;
+    const int64_t ke = (int64_t)(blockIdx.x + 1) * K / gridDim.x;
+    const int64_t xb = kb * L;
+    const int64_t xe = ke * L < total ? ke * L : total;
+    if (xb >= xe) return;
+
+    if (warp == C::NW) {
+        // ================================================= producer warp
+        const char* kpool = static_cast<const char*>(a.k_cache);
+        const char* vpool = static_cast<const char*>(a.v_cache);
+        Pos p = locate(xb, s_base, S, H);
+        int stage = 0;
+        uint32_t phase = 0;
+        int issued = 0;
+        int tc_s = -1, tc_win = 0, tc_val = 0, tn_val = 0;
+        bool tn_ok = false;
+        bool stop = false;
+        for (int64_t x = xb; x < xe && !stop;) {
+            const int ns = s_base[p.s + 1] - s_base[p.s];
+            const int64_t left = xe - x;
+            const int run = (int64_t)(ns - p.j) < left ? ns - p.j : (int)left;
+            const int nblk = (s_ctx[p.s] + B - 1) / B;
+            const int32_t* row = a.block_tables + (int64_t)p.s * a.max_blocks;
+            for (int i = 0; i < run; ++i) {
+                const int j = p.j + i;
+                const int jb = j / C::SPB;
+                const int sub = j - jb * C::SPB;
+                const int win = jb & ~31;
+                if (p.s != tc_s || win != tc_win) {
+                    if (p.s == tc_s && win == tc_win + 32 && tn_ok) {
+                        tc_val = tn_val;
+                    } else {
+                        tc_val = (win + lane < nblk) ? __ldg(row + win + lane) : 0;
+                    }
+                    tc_s = p.s;
+                    tc_win = win;
+                    tn_ok = win + 32 < nblk;
+                    if (tn_ok) tn_val = (win + 32 + lane < nblk) ? __ldg(row + win + 32 + lane) : 0;
+                }
+                const int phys_raw = __shfl_sync(kFull, tc_val, jb - win);
+                int ok = 1;
+                if (lane == 0) {
+                    ok = wait_bounded(&empty[stage], phase ^ 1u, abort_flag) ? 1 : 0;
+                    if (ok) {
+                        int64_t phys = phys_raw;
+                        if (phys < 0 || phys >= a.num_blocks) {
+                            atomicOr(a.err, PKV_DEVERR_BAD_BLOCK);
+                            phys = 0;
+                        }
+                        const int64_t off =
+                            ((phys * H + p.h) * B + (int64_t)sub * C::SUB) * (int64_t)D * 2;
+                        unsigned char* dst = ring + (size_t)stage * C::STAGE;
+                        mbar_arrive_expect_tx(&full[stage], C::STAGE);
+                        bulk_g2s(dst, kpool + off, C::CHUNK, &full[stage]);
+                        bulk_g2s(dst + C::CHUNK, vpool + off, C::CHUNK, &full[stage]);
+                    }
+                }
+                ok = __shfl_sync(kFull, ok, 0);
+                if (!ok) {
+                    if (lane == 0) {
+                        if (!*abort_flag) atomicOr(a.err, PKV_DEVERR_TIMEOUT);
+                        *abort_flag = 1;
+                    }
+                    stop = true;
+                    break;
+                }
+                ++issued;
+                if (++stage == C::NSTAGE) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (stop) break;
+            x += run;
+            p.j += run;
+            if (p.j == ns && x < xe) next_segment(p, s_base, S, H);
+        }
+        __syncwarp();
+        if (*abort_flag && lane == 0) {
+            // wind down: let the copies still in flight land before exiting
+            const int n = issued < C::NSTAGE ? issued : C::NSTAGE;
+            int st = stage;
+            uint32_t ph = phase;
+            for (int i = 0; i < n; ++i) {
+                if (--st < 0) {
+                    st = C::NSTAGE - 1;
+                    ph ^= 1u;
+                }
+                wait_bounded(&full[st], ph, nullptr);
+            }
+        }
+        return;
+    }
+
+    // ===================================================== consumer warps
+    const int hi = lane >> C::LOG_LPT;          // token within a 512-B row
+    const int dl = lane & (C::LPT - 1);         // 8-element slice of head_dim
+    const int own = dl >> C::RS;                // load whose score this lane ends up with
+    const bool leader = (dl & ((1 << C::RS) - 1)) == 0;
+    const T* qptr = static_cast<const T*>(a.q);
+    T* optr = static_cast<T*>(a.out);
+    float2* ws_ml = reinterpret_cast<float2*>(a.ws + a.ws_l.ml_off);
+    float* ws_acc = reinterpret_cast<float*>(a.ws + a.ws_l.acc_off);
+
+    Pos p = locate(xb, s_base, S, H);
+    int64_t x = xb;
+    uint32_t g0 = 0;
+    int pbuf = 0;
+    while (x < xe) {
+        const int ns = s_base[p.s + 1] - s_base[p.s];
+        const int64_t chunk = x / L;
+        int64_t len64 = ns - p.j;
+        if (L - (x - chunk * L) < len64) len64 = L - (x - chunk * L);
+        if (xe - x < len64) len64 = xe - x;
+        const int len = (int)len64;
+        const bool whole = (p.j == 0 && len == ns);
+        const int ctx = s_ctx[p.s];
+        const int64_t row = (int64_t)p.s * H + p.h;
+
+        float qf[8];
+        {
+            const uint4 raw = ld_nc_v4(qptr + row * D + dl * 8);
+            Elem<T>::to_f32x8(raw, qf);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) qf[e] *= a.scale_log2;
+        }
+        float m = -INFINITY, l = 0.f;
+        float acc[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+
+        const int first = (int)((uint32_t)(warp + C::NW - (int)(g0 % C::NW)) % C::NW);
+        for (int i = first; i < len; i += C::NW) {
+            const uint32_t g = g0 + (uint32_t)i;
+            const int stage = (int)(g % C::NSTAGE);
+            const uint32_t par = (g / C::NSTAGE) & 1u;
+            if (!*abort_flag) {
+                if (!wait_bounded(&full[stage], par, abort_flag)) {
+                    if (lane == 0) {
+                        if (!*abort_flag) atomicOr(a.err, PKV_DEVERR_TIMEOUT);
+                        *abort_flag = 1;
+                    }
+                }
+            }
+            __syncwarp();
+            const uint4* Ks = reinterpret_cast<const uint4*>(ring + (size_t)stage * C::STAGE);
+            const uint4* Vs = Ks + C::CHUNK / 16;
+            const int nvalid = ctx - (p.j + i) * C::SUB;   // >= 1
+
+            float part[C::NL];
+#pragma unroll
+            for (int t = 0; t < C::NL; ++t) {
+                const uint4 kv = Ks[t * 32 + lane];
+                float kf[8];
+                Elem<T>::to_f32x8(kv, kf);
+                float d = 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) d = fmaf(qf[e], kf[e], d);
+                part[t] = d;
+            }
+            float z = reduce_scatter<C::NL, C::LOG_LPT>(part, dl);
+            if (own * C::TPL + hi >= nvalid) z = -INFINITY;
+            const float m_new = fmaxf(m, warp_max(z));
+            const float alpha = exp2f(m - m_new);
+            const float pz = exp2f(z - m_new);
+            l = fmaf(l, alpha, leader ? pz : 0.f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] *= alpha;
+#pragma unroll
+            for (int t = 0; t < C::NL; ++t) {
+                const float pt = __shfl_sync(kFull, pz, (hi << C::LOG_LPT) | (t << C::RS));
+                if (t * C::TPL + hi < nvalid) {
+                    const uint4 vv = Vs[t * 32 + lane];
+                    float vf[8];
+                    Elem<T>::to_f32x8(vv, vf);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc[e] = fmaf(pt, vf[e], acc[e]);
+                }
+            }
+            m = m_new;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[stage]);
+        }
+
+        // fold the token groups of the warp, then merge the warps
+#pragma unroll
+        for (int o = C::LPT; o < 32; o <<= 1)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] += __shfl_xor_sync(kFull, acc[e], o);
+        l = warp_sum(l);
+        float* mrow = merge + (pbuf * C::NW + warp) * C::MROW;
+        if (lane < C::LPT) {
+            float4* d4 = reinterpret_cast<float4*>(mrow + dl * 8);
+            d4[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            d4[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+        }
+        if (lane == 0) {
+            mrow[D] = m;
+            mrow[D + 1] = l;
+        }
+        named_bar_sync(1, C::NW * 32);
+        if (tid < D && !*abort_flag) {
+            const float* mb = merge + pbuf * C::NW * C::MROW;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < C::NW; ++w) M = fmaxf(M, mb[w * C::MROW + D]);
+            float ls = 0.f, av = 0.f;
+#pragma unroll
+            for (int w = 0; w < C::NW; ++w) {
+                const float sc = exp2f(mb[w * C::MROW + D] - M);
+                ls = fmaf(sc, mb[w * C::MROW + D + 1], ls);
+                av = fmaf(sc, mb[w * C::MROW + tid], av);
+            }
+            if (whole) {
+                optr[row * D + tid] = Elem<T>::from_f32(av / ls);
+            } else {
+                const int64_t slot = row + chunk;
+                ws_acc[slot * D + tid] = av;
+                if (tid == 0) ws_ml[slot] = make_float2(M, ls);
+            }
+        }
+        pbuf ^= 1;
+        x += len;
+        g0 += (uint32_t)len;
+        p.j += len;
+        if (p.j == ns && x < xe) next_segment(p, s_base, S, H);
+    }
+}
+
+// ------------------------------------------------------------ the merge kernel
+// One warp per (sequence, head).  Rows whose (s, h) fell inside one chunk were
+// written by the main kernel; a zero-length sequence gets a zero row; the rest
+// combine their partials: M = max_k m_k, out = sum_k 2^(m_k - M) acc_k /
+// sum_k 2^(m_k - M) l_k.
+template <typename T, int D>
+__global__ void __launch_bounds__(128) paged_decode_merge(const DecodeArgs a) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t sh = (int64_t)blockIdx.x * 4 + warp;
+    if (sh >= (int64_t)a.S * a.H) return;
+    const int64_t L = reinterpret_cast<const int64_t*>(a.ws)[0];
+    if (L <= 0) return;
+    const int* base = reinterpret_cast<const int*>(a.ws + a.ws_l.base_off);
+    const int s = (int)(sh / a.H), h = (int)(sh - (int64_t)s * a.H);
+    const int ns = base[s + 1] - base[s];
+    constexpr int PER = D / 32;
+    T* o = static_cast<T*>(a.out) + sh * D + lane * PER;
+    if (ns == 0) {
+#pragma unroll
+        for (int e = 0; e < PER; ++e) o[e] = Elem<T>::zero();
+        return;
+    }
+    const int64_t x0 = (int64_t)a.H * base[s] + (int64_t)h * ns;
+    const int64_t kf = x0 / L, kl = (x0 + ns - 1) / L;
+    if (kf == kl) return;
+    const float2* ml = reinterpret_cast<const float2*>(a.ws + a.ws_l.ml_off);
+    const float* accw = reinterpret_cast<const float*>(a.ws + a.ws_l.acc_off);
+    float M = -INFINITY;
+    for (int64_t k = kf + lane; k <= kl; k += 32) M = fmaxf(M, ml[sh + k].x);
+    M = warp_max(M);
+    float ls = 0.f, acc[PER];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+#pragma unroll 4
+    for (int64_t k = kf; k <= kl; ++k) {
+        const float2 v = ml[sh + k];
+        const float sc = exp2f(v.x - M);
+        ls = fmaf(sc, v.y, ls);
+        const float* r = accw + (sh + k) * D + lane * PER;
+        if constexpr (PER == 4) {
+            const float4 f = *reinterpret_cast<const float4*>(r);
+            acc[0] = fmaf(sc, f.x, acc[0]);
+            acc[1] = fmaf(sc, f.y, acc[1]);
+            acc[2] = fmaf(sc, f.z, acc[2]);
+            acc[3] = fmaf(sc, f.w, acc[3]);
+        } else {
+            const float2 f = *reinterpret_cast<const float2*>(r);
+            acc[0] = fmaf(sc, f.x, acc[0]);
+            acc[1] = fmaf(sc, f.y, acc[1]);
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < PER; ++e) o[e] = Elem<T>::from_f32(acc[e] / ls);
+}
+
+// ------------------------------------------------------------ host glue
+template <typename T, int D, int B>
+struct Launcher {
+    using C = Cfg<D, B>;
+    static size_t smem_bytes(int S) { return C::smem(S); }
+    static cudaError_t occupancy(int* ctas, size_t smem) {
+        cudaError_t e = cudaFuncSetAttribute(paged_decode_main<T, D, B>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+        if (e != cudaSuccess) return e;
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, paged_decode_main<T, D, B>,
+                                                             C::THREADS, smem);
+    }
+    static cudaError_t launch(const DecodeArgs& a, int grid, cudaStream_t stream) {
+        const size_t smem = C::smem(a.S);
+        paged_decode_main<T, D, B><<<grid, C::THREADS, smem, stream>>>(a);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        const int64_t warps = (int64_t)a.S * a.H;
+        paged_decode_merge<T, D><<<(unsigned)((warps + 3) / 4), 128, 0, stream>>>(a);
+        return cudaGetLastError();
+    }
+    static const DecodeKernel* get() {
+        static const DecodeKernel k = {&launch, &smem_bytes, &occupancy, C::THREADS};
+        return &k;
+    }
+};
+
+}  // namespace dec
+}  // namespace pkv

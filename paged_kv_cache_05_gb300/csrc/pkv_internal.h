@@ -1,0 +1,94 @@
+// Internal declarations shared by the library's translation units (host side,
+// plus the workspace layout that host and device code must agree on).
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#include "pagedkv.h"
+
+namespace pkv {
+
+// ---- status / last error ---------------------------------------------------
+pkv_status fail(pkv_status st, const char* fmt, ...);
+pkv_status cuda_fail(cudaError_t e, const char* what);
+void clear_last_error();
+
+// ---- device error word (one per device, lives in errors.cu) -----------------
+// Returns the device address of the error word of the current device.
+int32_t* device_error_word();
+
+// ---- device facts, cached per device ---------------------------------------
+int sm_count(int device);
+
+// ---- decode workspace layout -------------------------------------------------
+// [0, 64)                  header: int64 L (chunk length in steps), int64 total steps
+// [64, 64 + 4 (S + 1))     int32 step prefix per sequence (written by CTA 0)
+// then, 256-aligned:       float2 ml[cap]   (running max in log2 units, sum)
+// then, 256-aligned:       float  acc[cap][D] (unnormalised output)
+// cap = S * H + (max number of chunks)
+struct WsLayout {
+    size_t base_off, ml_off, acc_off, total;
+    int64_t cap;
+};
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+__host__ __device__ inline WsLayout ws_layout(int S, int H, int D, int64_t max_chunks) {
+    WsLayout w;
+    w.cap = (int64_t)S * H + max_chunks;
+    w.base_off = 64;
+    w.ml_off = align_up(w.base_off + 4 * (size_t)(S + 1), 256);
+    w.acc_off = align_up(w.ml_off + 8 * (size_t)w.cap, 256);
+    w.total = align_up(w.acc_off + 4 * (size_t)w.cap * D, 256);
+    return w;
+}
+
+// Tokens per pipeline step: a step moves SUB tokens of one (block, head) for K
+// and for V, at most 4 KiB each.
+__host__ __device__ constexpr int step_tokens(int D, int B) {
+    return B < 2048 / D ? B : 2048 / D;
+}
+
+// ---- decode kernel dispatch ---------------------------------------------------
+struct DecodeArgs {
+    void* out;
+    const void* q;
+    const void* k_cache;
+    const void* v_cache;
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    float scale_log2;        // softmax scale * log2(e)
+    int S, H, max_blocks;
+    int64_t num_blocks;
+    int64_t L_steps;         // fixed chunk length in steps, 0 = balanced
+    int min_chunk_steps;     // balanced mode: lower bound of the chunk length
+    char* ws;
+    WsLayout ws_l;
+    int32_t* err;
+};
+
+struct DecodeKernel {
+    // launch main + merge on `stream`; grid = number of persistent CTAs
+    cudaError_t (*launch)(const DecodeArgs& a, int grid, cudaStream_t stream);
+    // dynamic shared memory of the main kernel for S sequences
+    size_t (*smem_bytes)(int S);
+    // CTAs per SM the main kernel can keep resident with that shared memory
+    cudaError_t (*occupancy)(int* ctas_per_sm, size_t smem);
+    int threads;
+};
+
+const DecodeKernel* decode_kernel_f16(int D, int B);
+const DecodeKernel* decode_kernel_bf16(int D, int B);
+
+// ---- cache kernels -----------------------------------------------------------
+cudaError_t launch_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,
+                                     const int64_t* slots, int T, int H, int D, int B,
+                                     int64_t num_blocks, int32_t* err, cudaStream_t stream);
+cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int P,
+                               int H, int D, int B, int64_t num_blocks, int32_t* err,
+                               cudaStream_t stream);
+
+}  // namespace pkv

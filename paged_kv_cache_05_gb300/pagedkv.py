@@ -1,0 +1,308 @@
+"""Thin ctypes binding of libpagedkv.so (include/pagedkv.h).
+
+Argument marshalling only: tensors become device pointers, the current torch
+stream becomes the cudaStream_t, and a non-OK status becomes an exception.
+Every step of the computation runs in the library's CUDA kernels (or, for the
+block manager, its C++ code).  There is no fallback: if the library is not
+built, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpagedkv.so")
+
+PKV_OK, PKV_ERR_INVALID, PKV_ERR_CUDA, PKV_ERR_OOM, PKV_ERR_DEVICE = range(5)
+STATUS_NAMES = {0: "PKV_OK", 1: "PKV_ERR_INVALID", 2: "PKV_ERR_CUDA", 3: "PKV_ERR_OOM",
+                4: "PKV_ERR_DEVICE"}
+PKV_F16, PKV_BF16 = 0, 1
+DEVERR_BAD_BLOCK, DEVERR_BAD_SLOT, DEVERR_BAD_CONTEXT, DEVERR_TIMEOUT, DEVERR_WORKSPACE = (
+    1, 2, 4, 8, 16)
+MAX_GRID = 4096
+MAX_SEQS = 16384
+
+_lib = None
+_lock = threading.Lock()
+
+
+class PagedKVError(RuntimeError):
+    def __init__(self, fn, status, message):
+        super().__init__("%s: %s: %s" % (fn, STATUS_NAMES.get(status, status), message))
+        self.status = status
+
+
+class OutOfBlocks(PagedKVError):
+    pass
+
+
+def lib():
+    """Load libpagedkv.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libpagedkv.so is not built (%s); run "
+                               "`python -m paged_kv_cache_05_gb300.build`" % LIB_PATH)
+        L = ctypes.CDLL(LIB_PATH)
+        P, i32, i64, u64, f32 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint64,
+                                 ctypes.c_float)
+        sz = ctypes.c_size_t
+        sig = {
+            "pkv_decode_workspace_size": ([i32, i32, i32, i32, i32, i32, ctypes.POINTER(sz)], i32),
+            "pkv_paged_attention_decode": ([P, P, P, P, P, P, f32, i32, i32, i32, i32, i32, i64,
+                                            i32, i32, P, sz, P], i32),
+            "pkv_reshape_and_cache": ([P, P, P, P, P, i32, i32, i32, i32, i64, i32, P], i32),
+            "pkv_copy_blocks": ([P, P, P, i32, i32, i32, i32, i64, i32, P], i32),
+            "pkv_get_device_error": ([ctypes.POINTER(ctypes.c_int32), i32, P], i32),
+            "pkv_last_error": ([], ctypes.c_char_p),
+            "pkv_version": ([], ctypes.c_char_p),
+            "pkv_bm_create": ([i64, i32, u64, ctypes.POINTER(P)], i32),
+            "pkv_bm_destroy": ([P], None),
+            "pkv_bm_add_sequence": ([P, i64, ctypes.c_int32, P], i32),
+            "pkv_bm_fork": ([P, i64, i64], i32),
+            "pkv_bm_append_slot": ([P, i64, ctypes.POINTER(ctypes.c_int64),
+                                    ctypes.POINTER(ctypes.c_int32),
+                                    ctypes.POINTER(ctypes.c_int32)], i32),
+            "pkv_bm_append_slots": ([P, P, i32, P, P, ctypes.POINTER(ctypes.c_int32)], i32),
+            "pkv_bm_free_sequence": ([P, i64], i32),
+            "pkv_bm_block_table": ([P, i64, P, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)],
+                                   i32),
+            "pkv_bm_context_len": ([P, i64, ctypes.POINTER(ctypes.c_int32)], i32),
+            "pkv_bm_export": ([P, P, i32, P, ctypes.c_int32, P], i32),
+            "pkv_bm_refcount": ([P, ctypes.c_int32], ctypes.c_int32),
+            "pkv_bm_num_free": ([P], i64),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = L
+        return L
+
+
+def last_error() -> str:
+    return lib().pkv_last_error().decode()
+
+
+def version() -> str:
+    return lib().pkv_version().decode()
+
+
+def _check(fn: str, status: int):
+    if status != PKV_OK:
+        cls = OutOfBlocks if status == PKV_ERR_OOM else PagedKVError
+        raise cls(fn, status, last_error())
+
+
+# ----------------------------------------------------------------- torch side
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t == torch.float16:
+        return PKV_F16
+    if t == torch.bfloat16:
+        return PKV_BF16
+    raise TypeError("fp16 or bf16 storage expected, got %s" % t)
+
+
+def _stream(stream) -> int:
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _dev(t, name, dtype=None, ndim=None):
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError("%s must have %d dimensions" % (name, ndim))
+    return t.data_ptr()
+
+
+def decode_workspace_size(num_seqs, num_heads, head_dim, block_size, max_blocks_per_seq,
+                          partition_size=0) -> int:
+    out = ctypes.c_size_t(0)
+    _check("pkv_decode_workspace_size",
+           lib().pkv_decode_workspace_size(num_seqs, num_heads, head_dim, block_size,
+                                           max_blocks_per_seq, partition_size,
+                                           ctypes.byref(out)))
+    return out.value
+
+
+def alloc_workspace(num_seqs, num_heads, head_dim, block_size, max_blocks_per_seq,
+                    partition_size=0, device="cuda"):
+    """A device buffer (torch uint8, 256-B aligned by torch's allocator) of the needed size."""
+    torch = _torch()
+    n = decode_workspace_size(num_seqs, num_heads, head_dim, block_size, max_blocks_per_seq,
+                              partition_size)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+
+
+def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale,
+                           partition_size=0, workspace=None, stream=None):
+    """out[s,h] = softmax(scale q[s,h] . K_s) V_s over the sequence's paged K/V."""
+    torch = _torch()
+    S, H, D = q.shape
+    nb, H2, B, D2 = k_cache.shape
+    if (H2, D2) != (H, D) or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("q / cache shape mismatch")
+    if tuple(out.shape) != (S, H, D) or out.dtype != q.dtype or k_cache.dtype != q.dtype:
+        raise ValueError("out/q/cache dtype or shape mismatch")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S:
+        raise ValueError("block_tables must be [num_seqs, max_blocks]")
+    if workspace is None:
+        workspace = alloc_workspace(S, H, D, B, block_tables.shape[1], partition_size,
+                                    q.device)
+    ptrs = [_dev(out, "out"), _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+            _dev(block_tables, "block_tables", torch.int32),
+            _dev(context_lens, "context_lens", torch.int32, 1)]
+    wsp = _dev(workspace, "workspace")
+    _check("pkv_paged_attention_decode",
+           lib().pkv_paged_attention_decode(*ptrs, float(scale), S, H, D, B,
+                                            block_tables.shape[1], nb, _dtype_code(q.dtype),
+                                            int(partition_size), wsp,
+                                            workspace.numel() * workspace.element_size(),
+                                            _stream(stream)))
+    return out
+
+
+def reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, stream=None):
+    """k_cache[slot // B, h, slot % B] = k[t, h] (and v) for slot_mapping[t] >= 0."""
+    torch = _torch()
+    T, H, D = k.shape
+    nb, H2, B, D2 = k_cache.shape
+    if (H2, D2) != (H, D) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("k/v/cache shape mismatch")
+    if k.dtype != k_cache.dtype or v.dtype != k.dtype or v_cache.dtype != k.dtype:
+        raise TypeError("k, v and the caches must share a dtype")
+    _check("pkv_reshape_and_cache",
+           lib().pkv_reshape_and_cache(_dev(k, "k"), _dev(v, "v"), _dev(k_cache, "k_cache"),
+                                       _dev(v_cache, "v_cache"),
+                                       _dev(slot_mapping, "slot_mapping", torch.int64, 1),
+                                       T, H, D, B, nb, _dtype_code(k.dtype), _stream(stream)))
+
+
+def copy_blocks(k_cache, v_cache, pairs, stream=None):
+    """For each (src, dst) row of pairs: whole-block copy in both pools."""
+    torch = _torch()
+    nb, H, B, D = k_cache.shape
+    P = pairs.shape[0] if pairs.numel() else 0
+    if P == 0:
+        return
+    if pairs.dim() != 2 or pairs.shape[1] != 2:
+        raise ValueError("pairs must be [num_pairs, 2]")
+    _check("pkv_copy_blocks",
+           lib().pkv_copy_blocks(_dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+                                 _dev(pairs, "pairs", torch.int32), P, H, D, B, nb,
+                                 _dtype_code(k_cache.dtype), _stream(stream)))
+
+
+def get_device_error(clear=True, stream=None) -> int:
+    """Device error bits (PKV_DEVERR_*) of the current device; syncs the stream."""
+    bits = ctypes.c_int32(0)
+    st = lib().pkv_get_device_error(ctypes.byref(bits), int(bool(clear)), _stream(stream))
+    if st not in (PKV_OK, PKV_ERR_DEVICE):
+        _check("pkv_get_device_error", st)
+    return bits.value
+
+
+# ------------------------------------------------------------- block manager
+class BlockManager:
+    """Host KV block manager (C++ in libpagedkv.so)."""
+
+    def __init__(self, num_blocks: int, block_size: int, seed: int):
+        h = ctypes.c_void_p()
+        _check("pkv_bm_create", lib().pkv_bm_create(int(num_blocks), int(block_size),
+                                                    int(seed) & ((1 << 64) - 1),
+                                                    ctypes.byref(h)))
+        self._h = h
+        self.num_blocks = num_blocks
+        self.block_size = block_size
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value and _lib is not None:
+            _lib.pkv_bm_destroy(h)
+            self._h = None
+
+    def add_sequence(self, seq_id: int, prompt_len: int) -> np.ndarray:
+        slots = np.empty(max(prompt_len, 1), dtype=np.int64)
+        _check("pkv_bm_add_sequence",
+               lib().pkv_bm_add_sequence(self._h, int(seq_id), int(prompt_len),
+                                         slots.ctypes.data_as(ctypes.c_void_p)))
+        return slots[:prompt_len]
+
+    def fork(self, parent: int, child: int) -> None:
+        _check("pkv_bm_fork", lib().pkv_bm_fork(self._h, int(parent), int(child)))
+
+    def append_slot(self, seq_id: int):
+        slot, src, dst = ctypes.c_int64(), ctypes.c_int32(), ctypes.c_int32()
+        _check("pkv_bm_append_slot",
+               lib().pkv_bm_append_slot(self._h, int(seq_id), ctypes.byref(slot),
+                                        ctypes.byref(src), ctypes.byref(dst)))
+        return slot.value, src.value, dst.value
+
+    def append_slots(self, seq_ids):
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        n = ids.shape[0]
+        slots = np.empty(max(n, 1), dtype=np.int64)
+        pairs = np.empty((max(n, 1), 2), dtype=np.int32)
+        npairs = ctypes.c_int32(0)
+        _check("pkv_bm_append_slots",
+               lib().pkv_bm_append_slots(self._h, ids.ctypes.data_as(ctypes.c_void_p), n,
+                                         slots.ctypes.data_as(ctypes.c_void_p),
+                                         pairs.ctypes.data_as(ctypes.c_void_p),
+                                         ctypes.byref(npairs)))
+        return slots[:n], pairs[:npairs.value]
+
+    def free_sequence(self, seq_id: int) -> None:
+        _check("pkv_bm_free_sequence", lib().pkv_bm_free_sequence(self._h, int(seq_id)))
+
+    def block_table(self, seq_id: int) -> list:
+        n = ctypes.c_int32(0)
+        st = lib().pkv_bm_block_table(self._h, int(seq_id), None, 0, ctypes.byref(n))
+        if st != PKV_OK and n.value == 0:
+            _check("pkv_bm_block_table", st)
+        buf = np.empty(max(n.value, 1), dtype=np.int32)
+        _check("pkv_bm_block_table",
+               lib().pkv_bm_block_table(self._h, int(seq_id), buf.ctypes.data_as(ctypes.c_void_p),
+                                        n.value, ctypes.byref(n)))
+        return buf[:n.value].tolist()
+
+    def context_len(self, seq_id: int) -> int:
+        n = ctypes.c_int32(0)
+        _check("pkv_bm_context_len", lib().pkv_bm_context_len(self._h, int(seq_id),
+                                                              ctypes.byref(n)))
+        return n.value
+
+    def export(self, seq_ids, max_blocks: int):
+        """(block_tables int32 [n, max_blocks] with -1 padding, context_lens int32 [n])."""
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        n = ids.shape[0]
+        tables = np.empty((max(n, 1), max_blocks), dtype=np.int32)
+        ctx = np.empty(max(n, 1), dtype=np.int32)
+        _check("pkv_bm_export",
+               lib().pkv_bm_export(self._h, ids.ctypes.data_as(ctypes.c_void_p), n,
+                                   tables.ctypes.data_as(ctypes.c_void_p), int(max_blocks),
+                                   ctx.ctypes.data_as(ctypes.c_void_p)))
+        return tables[:n], ctx[:n]
+
+    def refcount(self, block: int) -> int:
+        return lib().pkv_bm_refcount(self._h, int(block))
+
+    def num_free(self) -> int:
+        return lib().pkv_bm_num_free(self._h)

@@ -1,0 +1,186 @@
+"""The C ABI without a GPU: exports, host-side argument checks, the C++ block
+manager against the oracle's independent model (bit-exact)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle.block_manager import BlockManagerModel, OutOfBlocks as ModelOOM
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    from paged_kv_cache_05_gb300 import build
+    build.build()
+    import paged_kv_cache_05_gb300 as m
+    return m
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "pagedkv.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_\w+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(pkv):
+    names = declared_functions()
+    assert len(names) >= 19
+    L = ctypes.CDLL(pkv.pagedkv.LIB_PATH)
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_workspace_size_checks(pkv):
+    assert pkv.decode_workspace_size(64, 40, 128, 16, 128, 0) > 0
+    assert pkv.decode_workspace_size(8, 32, 128, 16, 2048, 512) > \
+        pkv.decode_workspace_size(8, 32, 128, 16, 2048, 0) // 2
+    for bad in [(64, 40, 96, 16, 128, 0),      # head_dim
+                (64, 40, 128, 12, 128, 0),     # block_size
+                (64, 40, 128, 16, 0, 0),       # max_blocks
+                (-1, 40, 128, 16, 8, 0),       # num_seqs
+                (64, 40, 128, 16, 8, 24),      # partition not a multiple of the step
+                (64, 0, 128, 16, 8, 0)]:       # heads
+        with pytest.raises(pkv.PagedKVError) as e:
+            pkv.decode_workspace_size(*bad)
+        assert e.value.status == 1
+
+
+def test_decode_rejects_bad_arguments_before_touching_a_gpu(pkv):
+    L = pkv.lib()
+    ws = ctypes.c_size_t(0)
+    assert L.pkv_decode_workspace_size(4, 8, 64, 16, 4, 0, ctypes.byref(ws)) == 0
+    fake = 1 << 20   # never dereferenced: validation fails first
+    base = [fake, fake, fake, fake, fake, fake, 0.125, 4, 8, 64, 16, 4, 64, 0, 0, fake * 256,
+            ws.value, None]
+
+    def call(**kw):
+        args = list(base)
+        names = ["out", "q", "k", "v", "bt", "cl", "scale", "S", "H", "D", "B", "maxb", "nb",
+                 "dtype", "part", "ws", "wsb", "stream"]
+        for k, v in kw.items():
+            args[names.index(k)] = v
+        return L.pkv_paged_attention_decode(*args)
+
+    assert call(D=80) == 1
+    assert call(B=4) == 1
+    assert call(nb=0) == 1
+    assert call(dtype=7) == 1
+    assert call(scale=float("nan")) == 1
+    assert call(out=0) == 1
+    assert call(q=fake + 8) == 1            # misaligned
+    assert call(ws=fake * 256 + 64) == 1    # workspace misaligned
+    assert call(wsb=ws.value - 1) == 1      # workspace too small
+    assert call(part=20) == 1
+    assert "workspace" in pkv.pagedkv.last_error() or "partition" in pkv.pagedkv.last_error()
+    assert call(S=0) == 0                   # empty batch: nothing to do
+
+
+def test_cache_ops_reject_bad_arguments(pkv):
+    L = pkv.lib()
+    f = 1 << 20
+    assert L.pkv_reshape_and_cache(f, f, f, f, f, 4, 8, 100, 16, 64, 0, None) == 1
+    assert L.pkv_reshape_and_cache(f, f, f, f, f, -1, 8, 64, 16, 64, 0, None) == 1
+    assert L.pkv_reshape_and_cache(f + 4, f, f, f, f, 4, 8, 64, 16, 64, 0, None) == 1
+    assert L.pkv_reshape_and_cache(f, f, f, f, f, 0, 8, 64, 16, 64, 0, None) == 0
+    assert L.pkv_copy_blocks(f, f, f, 2, 8, 64, 24, 64, 0, None) == 1
+    assert L.pkv_copy_blocks(f, f, f, 70000, 8, 64, 16, 64, 0, None) == 1
+    assert L.pkv_copy_blocks(f, f, f, 0, 8, 64, 16, 64, 0, None) == 0
+
+
+# ---------------------------------------------------------------- block manager
+def same_state(bm, model, seq_ids):
+    for s in seq_ids:
+        assert bm.block_table(s) == model.block_table(s)
+        assert bm.context_len(s) == model.context_len(s)
+    assert bm.num_free() == model.num_free()
+    for b in range(model.num_blocks):
+        assert bm.refcount(b) == model.refcount(b)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 1001, 2**63 + 5])
+def test_manager_matches_model_on_random_churn(pkv, seed):
+    rs = np.random.default_rng(seed % 1000)
+    nb, B = 150, 16
+    bm = pkv.BlockManager(nb, B, seed)
+    model = BlockManagerModel(nb, B, seed)
+    live, nxt = [], 0
+    for step in range(1500):
+        op = int(rs.integers(0, 10))
+        if op < 2 or not live:
+            n = int(rs.integers(0, 70))
+            try:
+                ref = model.add_sequence(nxt, n)
+            except ModelOOM:
+                with pytest.raises(pkv.OutOfBlocks):
+                    bm.add_sequence(nxt, n)
+                continue
+            assert bm.add_sequence(nxt, n).tolist() == ref
+            live.append(nxt)
+            nxt += 1
+        elif op < 3:
+            parent = live[int(rs.integers(len(live)))]
+            model.fork(parent, nxt)
+            bm.fork(parent, nxt)
+            live.append(nxt)
+            nxt += 1
+        elif op < 4:
+            sid = live.pop(int(rs.integers(len(live))))
+            model.free_sequence(sid)
+            bm.free_sequence(sid)
+        else:
+            sid = live[int(rs.integers(len(live)))]
+            try:
+                ref = model.append_slot(sid)
+            except ModelOOM:
+                with pytest.raises(pkv.OutOfBlocks):
+                    bm.append_slot(sid)
+                continue
+            assert bm.append_slot(sid) == ref
+        if step % 50 == 0:
+            same_state(bm, model, live)
+    same_state(bm, model, live)
+
+
+def test_batched_append_matches_sequential_model(pkv):
+    B = 16
+    bm = pkv.BlockManager(400, B, 77)
+    model = BlockManagerModel(400, B, 77)
+    for g in range(4):                       # 4 prompts, each forked into 6 samples
+        p = 100 + 37 * g
+        bm.add_sequence(g * 10, p)
+        model.add_sequence(g * 10, p)
+        for c in range(1, 6):
+            bm.fork(g * 10, g * 10 + c)
+            model.fork(g * 10, g * 10 + c)
+    ids = [g * 10 + c for g in range(4) for c in range(6)]
+    for _ in range(40):
+        slots, pairs = bm.append_slots(ids)
+        ref = [model.append_slot(s) for s in ids]
+        assert slots.tolist() == [r[0] for r in ref]
+        assert pairs.tolist() == [[r[1], r[2]] for r in ref if r[1] >= 0]
+    same_state(bm, model, ids)
+    tables, ctx = bm.export(ids, 64)
+    for i, s in enumerate(ids):
+        t = model.block_table(s)
+        assert tables[i, :len(t)].tolist() == t and (tables[i, len(t):] == -1).all()
+        assert ctx[i] == model.context_len(s)
+
+
+def test_batched_append_is_all_or_nothing(pkv):
+    bm = pkv.BlockManager(6, 4, 3)
+    bm.add_sequence(1, 4)
+    bm.add_sequence(2, 4)
+    bm.add_sequence(3, 13)                   # 4 blocks: 6 used, none free
+    before = (bm.block_table(1), bm.block_table(2), bm.num_free())
+    with pytest.raises(pkv.OutOfBlocks):
+        bm.append_slots([1, 2])
+    assert (bm.block_table(1), bm.block_table(2), bm.num_free()) == before
+    with pytest.raises(pkv.PagedKVError):
+        bm.append_slots([1, 1])              # repeated sequence
+    with pytest.raises(pkv.PagedKVError):
+        bm.append_slots([9])                 # unknown sequence
+    assert bm.context_len(1) == 4
