@@ -23,7 +23,10 @@
 //     shared-memory stages guarded by mbarriers (full: transaction bytes;
 //     empty: released by the consuming warp).  No multicast: every CTA
 //     fetches its own blocks.
-//   * Four consumer warps take the steps round-robin.  Per step a warp reads
+//   * Two consumer warps take the steps round-robin (small CTAs: 96 threads
+//     and a 32 KiB ring, five resident per SM, measured best for short and
+//     mixed context lengths; the count and ring size are compile-time knobs).
+//     Per step a warp reads
 //     the K chunk from shared memory with conflict-free 16-byte loads (lane l
 //     reads bytes [16 l, 16 l + 16) of every 512-byte row), forms q . k
 //     partial dot products in fp32, and finishes them with a reduce-scatter
@@ -140,6 +143,22 @@ static __device__ __noinline__ bool wait_bounded(uint64_t* bar, uint32_t parity,
     return false;
 }
 
+// Common case inline (the phase has already completed); the bounded loop only
+// when it has not.
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_bounded(bar, parity, abort);
+}
+
+// Programmatic dependent launch: wait for the preceding kernel in the stream
+// (no-op when launched without the dependency), or let the next one start.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------ element types
 template <typename T>
 struct Elem;
@@ -178,15 +197,30 @@ struct Elem<__nv_bfloat16> {
 constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
 
 // ------------------------------------------------------------ configuration
+#ifndef PKV_DECODE_WARPS
+#define PKV_DECODE_WARPS 2          // consumer warps per CTA
+#endif
+#ifndef PKV_DECODE_RING_BYTES
+#define PKV_DECODE_RING_BYTES 32768 // shared-memory ring per CTA (4 stages of 8 KiB at D=128)
+#endif
+#ifndef PKV_DECODE_MIN_CTAS
+#define PKV_DECODE_MIN_CTAS 1       // launch-bounds hint: resident CTAs per SM
+#endif
+
 template <int D, int B>
 struct Cfg {
-    static constexpr int NW = 4;                        // consumer warps
+    static constexpr int NW = PKV_DECODE_WARPS;         // consumer warps
     static constexpr int THREADS = (NW + 1) * 32;       // + one producer warp
     static constexpr int SUB = step_tokens(D, B);       // tokens per step
     static constexpr int SPB = B / SUB;                 // steps per block
     static constexpr int CHUNK = SUB * D * 2;           // bytes of K (or V) per step
     static constexpr int STAGE = 2 * CHUNK;
-    static constexpr int NSTAGE = 98304 / STAGE;        // ~96 KiB ring
+    // Step g uses stage g % NSTAGE and is consumed by warp g % NW.  NSTAGE must
+    // be a multiple of NW: then the previous use of a stage (step g - NSTAGE)
+    // belongs to the same warp, which has already waited for it, so a warp
+    // never polls a full barrier whose previous phase is still pending (the
+    // parity test would report that previous phase as complete).
+    static constexpr int NSTAGE = (PKV_DECODE_RING_BYTES / STAGE) / NW * NW;
     static constexpr int NL = CHUNK / 512;              // 16-B loads per lane per chunk
     static constexpr int TPL = 256 / D;                 // tokens per 512-B row
     static constexpr int LPT = D / 8;                   // lanes per token row
@@ -198,11 +232,13 @@ struct Cfg {
     static constexpr size_t BAR_OFF = RING;
     static constexpr size_t MERGE_OFF = BAR_OFF + 16 * (size_t)NSTAGE;
     static constexpr size_t MISC_OFF = MERGE_OFF + 4 * (size_t)(2 * NW * MROW);
-    static constexpr size_t CTX_OFF = MISC_OFF + 64;
+    // misc: the abort flag (16 B), then one scan partial per warp
+    static constexpr size_t MISC_BYTES = (16 + 4 * (NW + 1) + 15) / 16 * 16;
+    static constexpr size_t CTX_OFF = MISC_OFF + MISC_BYTES;
     static_assert(NL >= 1 && NL <= LPT, "step layout");
+    static_assert(NSTAGE >= NW && NSTAGE % NW == 0, "ring depth: a multiple of the warps");
     static_assert(TPL * NL == SUB, "tokens per step");
     static_assert(B % SUB == 0, "steps per block");
-    static_assert(NW * 32 >= D, "merge: one thread per output element");
     static __host__ __device__ size_t smem(int S) {
         return CTX_OFF + 4 * (size_t)S + 4 * (size_t)(S + 1);
     }
@@ -308,7 +344,8 @@ __device__ void scan_steps(const int* ctx, int* base, int S, int* scratch) {
 
 // ------------------------------------------------------------ the main kernel
 template <typename T, int D, int B>
-__global__ void __launch_bounds__(Cfg<D, B>::THREADS) paged_decode_main(const DecodeArgs a) {
+__global__ void __launch_bounds__(Cfg<D, B>::THREADS, PKV_DECODE_MIN_CTAS)
+    paged_decode_main(const DecodeArgs a) {
     using C = Cfg<D, B>;
     extern __shared__ __align__(1024) unsigned char smem[];
     unsigned char* ring = smem;
@@ -316,7 +353,7 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS) paged_decode_main(const De
     uint64_t* empty = full + C::NSTAGE;
     float* merge = reinterpret_cast<float*>(smem + C::MERGE_OFF);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF);
-    int* scratch = reinterpret_cast<int*>(smem + C::MISC_OFF) + 4;   // 8 ints
+    int* scratch = reinterpret_cast<int*>(smem + C::MISC_OFF) + 4;   // NW + 1 ints
     int* s_ctx = reinterpret_cast<int*>(smem + C::CTX_OFF);
     int* s_base = s_ctx + a.S;
 
@@ -324,6 +361,7 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS) paged_decode_main(const De
     const int S = a.S, H = a.H;
 
     // 1. context lengths (validated and clamped) and the step prefix
+    grid_dependency_wait();
     const int cap = a.max_blocks * B;
     for (int s = tid; s < S; s += C::THREADS) {
         int c = a.context_lens[s];
@@ -363,6 +401,7 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS) paged_decode_main(const De
             if (!ws_ok) atomicOr(a.err, PKV_DEVERR_WORKSPACE);
         }
     }
+    grid_launch_dependents();
     if (!ws_ok || total == 0) return;
     const int64_t kb = (int64_t)blockIdx.x * K / gridDim.x;
     const int64_t ke = (int64_t)(blockIdx.x + 1) * K / gridDim.x;
@@ -378,7 +417,10 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS) paged_decode_main(const De
         int stage = 0;
         uint32_t phase = 0;
         int issued = 0;
-        int tc_s = -1, tc_win = 0, tc_val = 0, tn_val = 0;
+        // block-table cache, warp-wide: the current 32-entry window, the next
+        // window of the same sequence, and the first window of the next
+        // sequence (both prefetched so no table read sits on the copy path)
+        int tc_s = -1, tc_win = 0, tc_val = 0, tn_val = 0, ts_s = -1, ts_val = 0;
         bool tn_ok = false;
         bool stop = false;
         for (int64_t x = xb; x < xe && !stop;) {
@@ -395,8 +437,21 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS) paged_decode_main(const De
                 if (p.s != tc_s || win != tc_win) {
                     if (p.s == tc_s && win == tc_win + 32 && tn_ok) {
                         tc_val = tn_val;
+                    } else if (p.s == ts_s && win == 0) {
+                        tc_val = ts_val;
                     } else {
                         tc_val = (win + lane < nblk) ? __ldg(row + win + lane) : 0;
+                    }
+                    if (p.s != tc_s) {
+                        int s2 = p.s + 1;
+                        while (s2 < S && s_base[s2 + 1] == s_base[s2]) ++s2;
+                        ts_s = -1;
+                        if (s2 < S) {
+                            const int nb2 = (s_ctx[s2] + B - 1) / B;
+                            ts_val = lane < nb2 ? __ldg(a.block_tables + (int64_t)s2 * a.max_blocks + lane)
+                                                : 0;
+                            ts_s = s2;
+                        }
                     }
                     tc_s = p.s;
                     tc_win = win;
@@ -406,7 +461,7 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS) paged_decode_main(const De
                 const int phys_raw = __shfl_sync(kFull, tc_val, jb - win);
                 int ok = 1;
                 if (lane == 0) {
-                    ok = wait_bounded(&empty[stage], phase ^ 1u, abort_flag) ? 1 : 0;
+                    ok = wait_phase(&empty[stage], phase ^ 1u, abort_flag) ? 1 : 0;
                     if (ok) {
                         int64_t phys = phys_raw;
                         if (phys < 0 || phys >= a.num_blocks) {
@@ -472,6 +527,8 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS) paged_decode_main(const De
     int64_t x = xb;
     uint32_t g0 = 0;
     int pbuf = 0;
+    // the query slice of the next piece is loaded one piece ahead
+    uint4 q_next = ld_nc_v4(qptr + ((int64_t)p.s * H + p.h) * D + dl * 8);
     while (x < xe) {
         const int ns = s_base[p.s + 1] - s_base[p.s];
         const int64_t chunk = x / L;
@@ -483,10 +540,15 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS) paged_decode_main(const De
         const int ctx = s_ctx[p.s];
         const int64_t row = (int64_t)p.s * H + p.h;
 
+        const uint4 q_raw = q_next;
+        if (x + len < xe && p.j + len == ns) {
+            Pos pn = p;
+            next_segment(pn, s_base, S, H);
+            q_next = ld_nc_v4(qptr + ((int64_t)pn.s * H + pn.h) * D + dl * 8);
+        }
         float qf[8];
         {
-            const uint4 raw = ld_nc_v4(qptr + row * D + dl * 8);
-            Elem<T>::to_f32x8(raw, qf);
+            Elem<T>::to_f32x8(q_raw, qf);
 #pragma unroll
             for (int e = 0; e < 8; ++e) qf[e] *= a.scale_log2;
         }
@@ -501,7 +563,7 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS) paged_decode_main(const De
             const int stage = (int)(g % C::NSTAGE);
             const uint32_t par = (g / C::NSTAGE) & 1u;
             if (!*abort_flag) {
-                if (!wait_bounded(&full[stage], par, abort_flag)) {
+                if (!wait_phase(&full[stage], par, abort_flag)) {
                     if (lane == 0) {
                         if (!*abort_flag) atomicOr(a.err, PKV_DEVERR_TIMEOUT);
                         *abort_flag = 1;
@@ -565,24 +627,29 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS) paged_decode_main(const De
             mrow[D + 1] = l;
         }
         named_bar_sync(1, C::NW * 32);
-        if (tid < D && !*abort_flag) {
+        if (!*abort_flag) {
             const float* mb = merge + pbuf * C::NW * C::MROW;
             float M = -INFINITY;
 #pragma unroll
             for (int w = 0; w < C::NW; ++w) M = fmaxf(M, mb[w * C::MROW + D]);
-            float ls = 0.f, av = 0.f;
+            float sc[C::NW];
+            float ls = 0.f;
 #pragma unroll
             for (int w = 0; w < C::NW; ++w) {
-                const float sc = exp2f(mb[w * C::MROW + D] - M);
-                ls = fmaf(sc, mb[w * C::MROW + D + 1], ls);
-                av = fmaf(sc, mb[w * C::MROW + tid], av);
+                sc[w] = exp2f(mb[w * C::MROW + D] - M);
+                ls = fmaf(sc[w], mb[w * C::MROW + D + 1], ls);
             }
-            if (whole) {
-                optr[row * D + tid] = Elem<T>::from_f32(av / ls);
-            } else {
-                const int64_t slot = row + chunk;
-                ws_acc[slot * D + tid] = av;
-                if (tid == 0) ws_ml[slot] = make_float2(M, ls);
+            for (int d = tid; d < D; d += C::NW * 32) {
+                float av = 0.f;
+#pragma unroll
+                for (int w = 0; w < C::NW; ++w) av = fmaf(sc[w], mb[w * C::MROW + d], av);
+                if (whole) {
+                    optr[row * D + d] = Elem<T>::from_f32(av / ls);
+                } else {
+                    const int64_t slot = row + chunk;
+                    ws_acc[slot * D + d] = av;
+                    if (d == 0) ws_ml[slot] = make_float2(M, ls);
+                }
             }
         }
         pbuf ^= 1;
@@ -602,6 +669,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(128) paged_decode_merge(const DecodeArgs a) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t sh = (int64_t)blockIdx.x * 4 + warp;
+    grid_dependency_wait();
     if (sh >= (int64_t)a.S * a.H) return;
     const int64_t L = reinterpret_cast<const int64_t*>(a.ws)[0];
     if (L <= 0) return;
@@ -661,13 +729,28 @@ struct Launcher {
         return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, paged_decode_main<T, D, B>,
                                                              C::THREADS, smem);
     }
+    // Both kernels are launched as programmatic dependents of their
+    // predecessor in the stream: each waits (griddepcontrol.wait) before it
+    // reads anything, so only the launch latency overlaps the predecessor.
     static cudaError_t launch(const DecodeArgs& a, int grid, cudaStream_t stream) {
-        const size_t smem = C::smem(a.S);
-        paged_decode_main<T, D, B><<<grid, C::THREADS, smem, stream>>>(a);
-        cudaError_t e = cudaGetLastError();
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)grid);
+        cfg.blockDim = dim3(C::THREADS);
+        cfg.dynamicSmemBytes = C::smem(a.S);
+        cfg.stream = stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaError_t e = cudaLaunchKernelEx(&cfg, paged_decode_main<T, D, B>, a);
         if (e != cudaSuccess) return e;
         const int64_t warps = (int64_t)a.S * a.H;
-        paged_decode_merge<T, D><<<(unsigned)((warps + 3) / 4), 128, 0, stream>>>(a);
+        cfg.gridDim = dim3((unsigned)((warps + 3) / 4));
+        cfg.blockDim = dim3(128);
+        cfg.dynamicSmemBytes = 0;
+        e = cudaLaunchKernelEx(&cfg, paged_decode_merge<T, D>, a);
+        if (e != cudaSuccess) return e;
         return cudaGetLastError();
     }
     static const DecodeKernel* get() {
