@@ -132,6 +132,38 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* k_ca
                                       int partition_size, void* workspace,
                                       size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * The same decode attention for callers that cannot allocate device memory
+ * (the paper has no counterpart; this is an interface convenience).  Some
+ * callers can neither allocate nor be handed a workspace -- a serving loop
+ * whose device memory is planned once at start-up, or a plugin whose enqueue
+ * callback must not allocate -- so this entry point keeps its scratch in a
+ * fixed array of the library's own static device memory,
+ * PKV_NOALLOC_SCRATCH_BYTES per device, held by every GPU that loads the
+ * library until the process exits.  It allocates nothing itself (no
+ * cudaMalloc, cudaFree or allocating library routine).
+ *
+ * Arguments as for pkv_paged_attention_decode, without the workspace.  Sizes
+ * whose workspace (pkv_decode_workspace_size) exceeds the array are rejected
+ * with PKV_ERR_INVALID and nothing is launched.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  All calls on a device share the array, which
+ * keeps the last call's contents (nothing in it needs to start at zero):
+ * calls whose work overlaps on the GPU (other streams, other host threads)
+ * race on it and must be serialised by the caller.
+ */
+#define PKV_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+pkv_status pkv_paged_attention_decode_noalloc(void* out, const void* q, const void* k_cache,
+                                              const void* v_cache, const int32_t* block_tables,
+                                              const int32_t* context_lens, float scale,
+                                              int num_seqs, int num_heads, int head_dim,
+                                              int block_size, int max_blocks_per_seq,
+                                              int64_t num_blocks, pkv_dtype dtype,
+                                              int partition_size, cudaStream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Cache maintenance                                                         */
 /* ------------------------------------------------------------------------ */

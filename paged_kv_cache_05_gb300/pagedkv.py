@@ -57,6 +57,8 @@ def lib():
             "pkv_decode_workspace_size": ([i32, i32, i32, i32, i32, i32, ctypes.POINTER(sz)], i32),
             "pkv_paged_attention_decode": ([P, P, P, P, P, P, f32, i32, i32, i32, i32, i32, i64,
                                             i32, i32, P, sz, P], i32),
+            "pkv_paged_attention_decode_noalloc": ([P, P, P, P, P, P, f32, i32, i32, i32, i32,
+                                                    i32, i64, i32, i32, P], i32),
             "pkv_reshape_and_cache": ([P, P, P, P, P, i32, i32, i32, i32, i64, i32, P], i32),
             "pkv_copy_blocks": ([P, P, P, i32, i32, i32, i32, i64, i32, P], i32),
             "pkv_get_device_error": ([ctypes.POINTER(ctypes.c_int32), i32, P], i32),
@@ -177,6 +179,35 @@ def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens,
                                             int(partition_size), wsp,
                                             workspace.numel() * workspace.element_size(),
                                             _stream(stream)))
+    return out
+
+
+NOALLOC_SCRATCH_BYTES = 16 << 20
+
+
+def paged_attention_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens, scale,
+                                   partition_size=0, stream=None):
+    """paged_attention_decode without a workspace, for callers that cannot
+    allocate device memory: the library's static per-device scratch array
+    (NOALLOC_SCRATCH_BYTES) is used instead.  Calls that overlap on the GPU
+    share that array and must not run concurrently."""
+    torch = _torch()
+    S, H, D = q.shape
+    nb, H2, B, D2 = k_cache.shape
+    if (H2, D2) != (H, D) or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("q / cache shape mismatch")
+    if tuple(out.shape) != (S, H, D) or out.dtype != q.dtype or k_cache.dtype != q.dtype:
+        raise ValueError("out/q/cache dtype or shape mismatch")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S:
+        raise ValueError("block_tables must be [num_seqs, max_blocks]")
+    ptrs = [_dev(out, "out"), _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+            _dev(block_tables, "block_tables", torch.int32),
+            _dev(context_lens, "context_lens", torch.int32, 1)]
+    _check("pkv_paged_attention_decode_noalloc",
+           lib().pkv_paged_attention_decode_noalloc(*ptrs, float(scale), S, H, D, B,
+                                                    block_tables.shape[1], nb,
+                                                    _dtype_code(q.dtype), int(partition_size),
+                                                    _stream(stream)))
     return out
 
 
