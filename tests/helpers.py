@@ -64,35 +64,47 @@ def to_dev(w: np.ndarray, dtype: str):
     return W.words_to_torch(w, dtype).cuda()
 
 
-def sampled_oracle(q, k_cache, v_cache, tables: np.ndarray, ctx: np.ndarray, seqs, scale,
-                   dtype: str, heads=None) -> np.ndarray:
-    """fp64 oracle for selected sequences (and heads) of a device-resident batch.
-
-    The blocks those sequences use are copied to the host into a compact pool
-    and their tables renumbered (placement does not change the result); the
-    oracle then computes each selected row.  Returns [len(seqs), len(heads), D].
-    """
-    import torch
-    H = q.shape[1]
-    B = k_cache.shape[2]
-    heads = list(range(H)) if heads is None else list(heads)
+def compact_rows(kc: np.ndarray, vc: np.ndarray, tables: np.ndarray, ctx, seqs, B: int):
+    """Host pools restricted to the blocks the selected sequences use, with their
+    tables renumbered (placement does not change the result)."""
     used = []
     for s in seqs:
         n = -(-int(ctx[s]) // B)
         used.extend(int(b) for b in tables[s, :n])
     uniq = sorted(set(used)) or [0]
     remap = {b: i for i, b in enumerate(uniq)}
-    idx = torch.tensor(uniq, dtype=torch.long, device=k_cache.device)
-    hidx = torch.tensor(heads, dtype=torch.long, device=k_cache.device)
-    kc = W.torch_to_words(k_cache.index_select(0, idx).index_select(1, hidx))
-    vc = W.torch_to_words(v_cache.index_select(0, idx).index_select(1, hidx))
-    sidx = torch.tensor(list(seqs), dtype=torch.long, device=q.device)
-    qh = W.torch_to_words(q.index_select(0, sidx).index_select(1, hidx))
     mb = max(1, max(-(-int(ctx[s]) // B) for s in seqs))
     bt = np.full((len(seqs), mb), -1, np.int32)
     for i, s in enumerate(seqs):
         n = -(-int(ctx[s]) // B)
         bt[i, :n] = [remap[int(b)] for b in tables[s, :n]]
-    cl = np.array([ctx[s] for s in seqs], np.int32)
-    return oracle.paged_attention_decode_threaded(qh, kc, vc, bt, cl, float(np.float32(scale)),
-                                                  ORC_DTYPE[dtype], threads=8)
+    idx = np.array(uniq)
+    return kc[idx], vc[idx], bt, np.array([ctx[s] for s in seqs], np.int32), uniq
+
+
+def sampled_oracle(q_host: np.ndarray, kc_host: np.ndarray, vc_host: np.ndarray,
+                   tables: np.ndarray, ctx, seqs, scale, dtype: str) -> np.ndarray:
+    """fp64 oracle rows [len(seqs), H, D] for selected sequences of a batch whose
+    pools are given on the host (full pools or any superset of the used blocks)."""
+    B = kc_host.shape[2]
+    kc, vc, bt, cl, _ = compact_rows(kc_host, vc_host, tables, ctx, seqs, B)
+    return oracle.paged_attention_decode_threaded(q_host[list(seqs)], kc, vc, bt, cl,
+                                                  float(np.float32(scale)), ORC_DTYPE[dtype],
+                                                  threads=8)
+
+
+def device_blocks_to_host(k_cache, v_cache, block_ids):
+    """Host words of selected physical blocks of device pools: a dict-like pair
+    of arrays indexed by position in ``block_ids``."""
+    import torch
+    idx = torch.tensor(list(block_ids), dtype=torch.long, device=k_cache.device)
+    return (W.torch_to_words(k_cache.index_select(0, idx)),
+            W.torch_to_words(v_cache.index_select(0, idx)))
+
+
+def spread(ctx, n):
+    """n sequence indices spread over the range of context lengths (shortest and
+    longest included)."""
+    order = np.argsort(ctx, kind="stable")
+    pick = np.unique(np.linspace(0, len(ctx) - 1, n).round().astype(int))
+    return sorted(int(order[i]) for i in pick)
