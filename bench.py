@@ -240,19 +240,20 @@ class Workload:
                 blocks.update(tables[s, :-(-int(ctx[s]) // B)].tolist())
             self.unique_kv_bytes = len(blocks) * H * B * D * 2 * e
 
-    def step(self, i: int, ev=None):
+    def step(self, i: int):
         pkv = self.pkv
         layer = i % self.layers
         kc, vc = self.kc[layer], self.vc[layer]
         if len(self.pairs_host):
             pkv.copy_blocks(kc, vc, self.pairs)
         pkv.reshape_and_cache(self.k_new, self.v_new, kc, vc, self.slots)
-        if ev is not None:
-            ev[0].record()
         pkv.paged_attention_decode(self.out, self.q, kc, vc, self.tables, self.ctx, self.scale,
                                    self.partition, self.ws)
-        if ev is not None:
-            ev[1].record()
+
+    def attention(self, i: int):
+        layer = i % self.layers
+        self.pkv.paged_attention_decode(self.out, self.q, self.kc[layer], self.vc[layer],
+                                        self.tables, self.ctx, self.scale, self.partition, self.ws)
 
     def describe(self) -> str:
         sp = self.spec
@@ -265,15 +266,14 @@ class Workload:
 
 
 # ------------------------------------------------------------------ oracle leg
-def oracle_sample(wl: Workload, max_seconds: float = 20.0):
-    """Host copies of a bounded sample of the workload, for the CPU oracle."""
+def oracle_sample(wl: Workload, seqs=None):
+    """Host copies of the blocks a subset of the workload's sequences use (all
+    heads, layer 0), for the CPU oracle; default: every sequence."""
     import torch
-    order = np.argsort(wl.ctx_host)          # a spread of lengths: every k-th sequence
-    S = wl.S
-    pick = sorted(order[::max(1, S // 8)].tolist())
-    heads = list(range(wl.H))
+    pick = list(range(wl.S)) if seqs is None else sorted(seqs)
     B = wl.B
-    used = sorted(set(int(b) for s in pick for b in wl.tables_host[s, :-(-int(wl.ctx_host[s]) // B)]))
+    used = sorted(set(int(b) for s in pick
+                      for b in wl.tables_host[s, :-(-int(wl.ctx_host[s]) // B)]))
     remap = {b: i for i, b in enumerate(used)}
     idx = torch.tensor(used, dtype=torch.long, device=wl.kc[0].device)
     kc = W.torch_to_words(wl.kc[0].index_select(0, idx))
@@ -288,7 +288,7 @@ def oracle_sample(wl: Workload, max_seconds: float = 20.0):
     H, D, e = wl.H, wl.D, 2
     nbytes = (int(cl.astype(np.int64).sum()) * H * D * 2 * e + 2 * len(pick) * H * D * e
               + sum(-(-int(c) // B) for c in cl) * 4 + 4 * len(pick))
-    return dict(q=q, kc=kc, vc=vc, bt=bt, cl=cl, bytes=nbytes, seqs=len(pick), heads=len(heads))
+    return dict(q=q, kc=kc, vc=vc, bt=bt, cl=cl, bytes=nbytes, seqs=len(pick), heads=H)
 
 
 def run_oracle(sample, scale, dtype, threads):
@@ -300,6 +300,24 @@ def run_oracle(sample, scale, dtype, threads):
                                            threads=threads)
     return time.perf_counter() - t0
 
+
+def sized_sample(wl: Workload, budget_s: float, threads: int):
+    """The largest length-spread subset of sequences whose oracle pass is
+    expected to fit in budget_s (calibrated on a small subset), at least one."""
+    order = [int(i) for i in np.argsort(wl.ctx_host, kind="stable")]
+    probe = sorted(order[::max(1, wl.S // 8)])
+    p = oracle_sample(wl, probe)
+    t = run_oracle(p, wl.scale, wl.dtype, threads)
+    per_byte = t / p["bytes"] * max(1, min(threads, len(probe))) / max(1, min(threads, wl.S))
+    allowed = budget_s / max(per_byte, 1e-15)
+    take, acc = [], 0
+    for k in range(1, wl.S + 1):
+        sel = sorted(order[::max(1, wl.S // k)])[:k]
+        b = sum(int(wl.ctx_host[s]) for s in sel) * wl.H * wl.D * 4
+        if b > allowed and take:
+            break
+        take, acc = sel, b
+    return take
 
 def host_cores() -> int:
     try:
@@ -355,8 +373,6 @@ def main():
         raise SystemExit("bench.py: device error bits after warm-up")
 
     K = args.steps
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(K)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(device.index if device.index is not None else 0)
     sampler.start()
@@ -364,23 +380,31 @@ def main():
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
+    # timed region 1: K whole steps back to back (no events between kernels,
+    # which would break the programmatic-dependent-launch chain)
     t_start.record(stream)
     for i in range(K):
-        wl.step(args.warmup + i, evs[i])
+        wl.step(args.warmup + i)
     t_end.record(stream)
+    torch.cuda.synchronize()
+    # timed region 2: K launches of the dominant operation alone, bracketed
+    # by events on the launching stream: its average duration per launch
+    a_start, a_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a_start.record(stream)
+    for i in range(K):
+        wl.attention(args.warmup + i)
+    a_end.record(stream)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
     clocks = sampler.stop()
     ms_total = t_start.elapsed_time(t_end)
-    attn_ms = [a.elapsed_time(b) for a, b in evs]
+    attn_avg = a_start.elapsed_time(a_end) / K
     if dist is not None:
         t = torch.tensor([ms_total], dtype=torch.float64, device=device)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms_total = float(t.item())
     ms_step = ms_total / K
-    attn_avg = statistics.mean(attn_ms)
-    attn_med = statistics.median(attn_ms)
     value = world * wl.step_bytes / (ms_step * 1e-3) / 1e9
 
     # ---- end to end: host (pinned) inputs -> C ABI -> host output, every step
@@ -408,7 +432,6 @@ def main():
         "ms_per_step": round(ms_step, 5),
         "us_per_layer_step": round(ms_step * 1e3, 2),
         "attention_us_per_call": round(attn_avg * 1e3, 2),
-        "attention_us_median": round(attn_med * 1e3, 2),
         "pct_of_peak": round(100 * value / world / peak, 1),
         "seq_heads_per_s": round(world * wl.S * wl.H / (ms_step * 1e-3), 1),
         "higher_is_better": True,
@@ -438,6 +461,11 @@ def main():
             "peak_source": peak_note,
         },
         "gpu_launches": K * wl.launches_per_step,
+        "gpu_launches_note": "timed region 1: %d per step (%s); region 2 adds %d attention "
+                             "launches (2 kernels each) for the roofline" % (
+                                 wl.launches_per_step,
+                                 "copy_blocks, " * bool(len(wl.pairs_host))
+                                 + "reshape_and_cache, paged_decode_main, paged_decode_merge", K),
         "clocks": clocks,
     }
     if wl.unique_kv_bytes is not None:
@@ -446,7 +474,9 @@ def main():
         line["e2e"] = {"value": round(world * wl.step_bytes / (e2e["seconds"] / e2e["steps"]) / 1e9, 1),
                        "unit": "GB/s", "h2d_bytes_per_step": e2e["h2d"],
                        "d2h_bytes_per_step": e2e["d2h"], "steps": e2e["steps"],
-                       "us_per_step": round(1e6 * e2e["seconds"] / e2e["steps"], 2)}
+                       "us_per_step": round(1e6 * e2e["seconds"] / e2e["steps"], 2),
+                       "how": "CUDA-graph replay per step: one pinned H2D copy of the step's "
+                              "inputs, the step's kernels, D2H of out, stream sync"}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl)
     if rank == 0:
@@ -456,85 +486,119 @@ def main():
 
 
 def measure_e2e(wl: Workload, steps: int, device, dist):
-    """Per step: pinned host inputs -> device (q, new K/V, slots, tables,
-    context lengths), the step's kernels through the C ABI, the output back to
-    pinned host memory, stream synchronised."""
+    """End to end through the public API with host buffers, every step: the
+    step's inputs (q, new K/V, slot mapping, block tables, context lengths,
+    copy pairs) copied from pinned host memory in one transfer, the step's
+    kernels, the output copied back to pinned host memory, and a stream
+    synchronise.  Each layer's step is captured once in a CUDA graph (copies
+    and kernels); the timed loop replays the graphs."""
     import torch
-    host = {n: t.detach().cpu().pin_memory() for n, t in (
-        ("q", wl.q), ("k_new", wl.k_new), ("v_new", wl.v_new), ("slots", wl.slots),
-        ("tables", wl.tables), ("ctx", wl.ctx), ("pairs", wl.pairs))}
-    dev = {n: torch.empty_like(t, device=device) for n, t in host.items()}
+    parts = [("q", wl.q), ("k_new", wl.k_new), ("v_new", wl.v_new), ("slots", wl.slots),
+             ("tables", wl.tables), ("ctx", wl.ctx), ("pairs", wl.pairs)]
+    sizes = [t.numel() * t.element_size() for _, t in parts]
+    offs, o = [], 0
+    for n in sizes:
+        offs.append(o)
+        o += (n + 255) // 256 * 256
+    host = torch.empty(o, dtype=torch.uint8).pin_memory()
+    dev = torch.empty(o, dtype=torch.uint8, device=device)
+    views = {}
+    for (name, t), off, n in zip(parts, offs, sizes):
+        host[off:off + n].copy_(t.detach().cpu().contiguous().view(-1).view(torch.uint8))
+        views[name] = dev[off:off + n].view(t.dtype).view(t.shape)
     out_host = torch.empty(wl.out.shape, dtype=wl.out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    h2d = sum(sizes)
     d2h = out_host.numel() * out_host.element_size()
     pkv = wl.pkv
 
-    def one(i):
-        layer = i % wl.layers
-        for n in host:
-            if host[n].numel():
-                dev[n].copy_(host[n], non_blocking=True)
+    def body(layer):
+        dev.copy_(host, non_blocking=True)
         kc, vc = wl.kc[layer], wl.vc[layer]
         if len(wl.pairs_host):
-            pkv.copy_blocks(kc, vc, dev["pairs"])
-        pkv.reshape_and_cache(dev["k_new"], dev["v_new"], kc, vc, dev["slots"])
-        pkv.paged_attention_decode(wl.out, dev["q"], kc, vc, dev["tables"], dev["ctx"], wl.scale,
-                                   wl.partition, wl.ws)
+            pkv.copy_blocks(kc, vc, views["pairs"])
+        pkv.reshape_and_cache(views["k_new"], views["v_new"], kc, vc, views["slots"])
+        pkv.paged_attention_decode(wl.out, views["q"], kc, vc, views["tables"], views["ctx"],
+                                   wl.scale, wl.partition, wl.ws)
         out_host.copy_(wl.out, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
 
+    layers = min(wl.layers, steps)
+    for layer in range(layers):           # first calls outside capture
+        body(layer)
+    torch.cuda.synchronize()
+    graphs = []
+    side = torch.cuda.Stream(device=device)
+    for layer in range(layers):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            body(layer)
+        graphs.append(g)
+    torch.cuda.synchronize()
     for i in range(3):
-        one(i)
+        graphs[i % layers].replay()
+        torch.cuda.current_stream().synchronize()
     if dist is not None:
         dist.barrier()
     t0 = time.perf_counter()
     for i in range(steps):
-        one(i)
+        graphs[i % layers].replay()
+        torch.cuda.current_stream().synchronize()
     sec = time.perf_counter() - t0
     return {"seconds": sec, "steps": steps, "h2d": h2d, "d2h": d2h}
 
 
 def cpu_baseline(wl: Workload) -> dict:
+    """The oracle, as it stands, on the host cores over the whole layer-0 batch,
+    repeated until about 10 s of CPU work has been done."""
+    threads = min(host_cores(), wl.S)
     sample = oracle_sample(wl)
-    threads = host_cores()
-    sec = run_oracle(sample, wl.scale, wl.dtype, threads)
-    return {"value": round(sample["bytes"] / sec / 1e9, 4), "unit": "GB/s", "cores": threads,
-            "kind": "oracle",
-            "sample": "%d of %d sequences (every %d-th by length), all %d heads, layer 0; %.2f s" % (
-                sample["seqs"], wl.S, max(1, wl.S // 8), wl.H, sec)}
+    first = run_oracle(sample, wl.scale, wl.dtype, threads)
+    reps = max(1, min(30, int(10.0 / max(first, 1e-3))))
+    total, done = first, 1
+    while done < reps and total < 10.0:
+        total += run_oracle(sample, wl.scale, wl.dtype, threads)
+        done += 1
+    return {"value": round(sample["bytes"] * done / total / 1e9, 4), "unit": "GB/s",
+            "cores": threads, "kind": "oracle",
+            "sample": "all %d sequences x %d heads of layer 0, %d pass(es), %.1f s" % (
+                wl.S, wl.H, done, total)}
 
 
 def reference_arm(args, world, rank, dist):
-    """The CPU fp64 oracle as the reference arm, on the host cores."""
+    """The CPU fp64 oracle as the reference arm, on the host cores: W warm-up
+    and K timed steps, each over a length-spread subset of the workload sized
+    so that the whole run takes about a minute."""
     import torch
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
         return
-    device = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
-    if device.type == "cuda":
-        from paged_kv_cache_05_gb300 import build
-        build.build()
-        wl = Workload(args.workload, device, args.partition, args.block_size, layers=1)
-        sample = oracle_sample(wl)
-    else:
-        raise SystemExit("bench.py --impl reference: needs the device workload generator")
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py --impl reference: the workload generator needs the GPU")
+    device = torch.device("cuda", 0)
+    from paged_kv_cache_05_gb300 import build
+    build.build()
+    wl = Workload(args.workload, device, args.partition, args.block_size, layers=1)
     threads = host_cores()
-    for _ in range(min(args.warmup, 1)):
+    K, Wu = max(1, args.steps), max(0, args.warmup)
+    seqs = sized_sample(wl, 60.0 / (K + Wu), threads)
+    sample = oracle_sample(wl, seqs)
+    threads = min(threads, len(seqs))
+    for _ in range(Wu):
         run_oracle(sample, wl.scale, wl.dtype, threads)
-    times = [run_oracle(sample, wl.scale, wl.dtype, threads) for _ in range(max(1, min(args.steps, 3)))]
+    times = [run_oracle(sample, wl.scale, wl.dtype, threads) for _ in range(K)]
     sec = statistics.mean(times)
     v = sample["bytes"] / sec / 1e9
+    desc = "%d of %d sequences (length-spread), all %d heads, layer 0, per step" % (
+        len(seqs), wl.S, wl.H)
     line = {
         "impl": "reference",
         "metric": "paged-attn decode: achieved HBM GB/s (% of GB300 peak), us/layer-step at OPT-13B",
-        "value": round(v, 4), "unit": "GB/s", "n_gpus": world, "steps": len(times),
-        "warmup": min(args.warmup, 1), "ms_per_step": round(sec * 1e3, 3),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded)",
-        "config": {"workload": wl.describe(), "sample_seqs": sample["seqs"]},
-        "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-                         "sample": "%d of %d sequences, all heads, layer 0" % (sample["seqs"], wl.S)},
+        "value": round(v, 4), "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": Wu,
+        "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": wl.describe(), "sample": desc},
+        "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle", "sample": desc},
         "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

@@ -17,6 +17,30 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
     return r;
 }
 
+// Programmatic dependent launch: wait for the preceding kernel in the stream
+// before touching memory (a no-op without the dependency), then let the next
+// kernel's CTAs be scheduled while this one runs.
+__device__ __forceinline__ void pdl_wait_then_release() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Args...), dim3 grid, dim3 block, cudaStream_t stream,
+                       Args... args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // One thread per (token, head, 16-byte piece): copies that piece of K and of V.
 // Destination: slot / B is the physical block, slot % B the offset inside it
 // (ricepunchb garden, section 3.2).
@@ -24,6 +48,7 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
     const uint4* __restrict__ k, const uint4* __restrict__ v, uint4* __restrict__ k_cache,
     uint4* __restrict__ v_cache, const int64_t* __restrict__ slots, int T, int H, int vecs_per_row,
     int B, int64_t num_slots, int32_t* err) {
+    pdl_wait_then_release();
     const int64_t total = (int64_t)T * H * vecs_per_row;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
@@ -54,6 +79,7 @@ constexpr int kCopyUnroll = 4;
 __global__ void __launch_bounds__(kCopyThreads) copy_blocks_kernel(
     uint4* __restrict__ k_cache, uint4* __restrict__ v_cache, const int32_t* __restrict__ pairs,
     int64_t vecs_per_block, int64_t num_blocks, int32_t* err) {
+    pdl_wait_then_release();
     const int p = blockIdx.y;
     const int64_t src = pairs[2 * p], dst = pairs[2 * p + 1];
     if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
@@ -89,9 +115,11 @@ cudaError_t launch_reshape_and_cache(const void* k, const void* v, void* k_cache
     const int64_t total = (int64_t)T * H * vecs;
     int64_t blocks = (total + 255) / 256;
     if (blocks > 65535LL * 16) blocks = 65535LL * 16;
-    reshape_and_cache_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
-        static_cast<const uint4*>(k), static_cast<const uint4*>(v), static_cast<uint4*>(k_cache),
-        static_cast<uint4*>(v_cache), slots, T, H, vecs, B, num_blocks * B, err);
+    cudaError_t e = launch_pdl(reshape_and_cache_kernel, dim3((unsigned)blocks), dim3(256), stream,
+                               static_cast<const uint4*>(k), static_cast<const uint4*>(v),
+                               static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), slots,
+                               T, H, vecs, B, num_blocks * B, err);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -101,9 +129,10 @@ cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pair
     const int64_t vecs = (int64_t)H * B * D / 8;
     const int64_t per_cta = kCopyThreads * kCopyUnroll;
     dim3 grid((unsigned)((vecs + per_cta - 1) / per_cta), (unsigned)P, 2);
-    copy_blocks_kernel<<<grid, kCopyThreads, 0, stream>>>(static_cast<uint4*>(k_cache),
-                                                         static_cast<uint4*>(v_cache), pairs,
-                                                         vecs, num_blocks, err);
+    cudaError_t e = launch_pdl(copy_blocks_kernel, grid, dim3(kCopyThreads), stream,
+                               static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), pairs,
+                               vecs, num_blocks, err);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -153,6 +153,7 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* k_ca
     a.num_blocks = num_blocks;
     a.L_steps = partition_size > 0 ? partition_size / pkv::step_tokens(head_dim, block_size) : 0;
     a.min_chunk_steps = kMinChunkSteps;
+    a.main_grid = grid;
     a.ws = static_cast<char*>(workspace);
     a.ws_l = wl;
     a.err = err;

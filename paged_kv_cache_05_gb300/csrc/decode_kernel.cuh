@@ -661,21 +661,71 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, PKV_DECODE_MIN_CTAS)
 }
 
 // ------------------------------------------------------------ the merge kernel
-// One warp per (sequence, head).  Rows whose (s, h) fell inside one chunk were
-// written by the main kernel; a zero-length sequence gets a zero row; the rest
-// combine their partials: M = max_k m_k, out = sum_k 2^(m_k - M) acc_k /
-// sum_k 2^(m_k - M) l_k.
-template <typename T, int D>
+// One warp per (sequence, head).  Before waiting for the main kernel, every
+// CTA rebuilds the step prefix from context_lens (an input the main kernel
+// only reads) and so knows which of its rows fell inside one chunk -- the main
+// kernel wrote those -- and returns for them at once.  A zero-length sequence
+// gets a zero row.  The other rows wait, then combine their partials with the
+// log-sum-exp rule, online and 8 partials per batch of loads:
+//   M = max_k m_k,  out = sum_k 2^(m_k - M) acc_k / sum_k 2^(m_k - M) l_k.
+constexpr int kMergeBatch = 8;
+
+template <typename T, int D, int B>
 __global__ void __launch_bounds__(128) paged_decode_merge(const DecodeArgs a) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    using C = Cfg<D, B>;
+    extern __shared__ int msm[];            // base[S + 1], then 8 scan partials
+    int* base = msm;
+    int* scratch = msm + a.S + 1;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int S = a.S, H = a.H;
+
+    // the step prefix, as the main kernel forms it (same clamping)
+    {
+        const int cap = a.max_blocks * B;
+        const int per = (S + 127) / 128;
+        const int b = min(tid * per, S), e = min(b + per, S);
+        int local = 0;
+        for (int i = b; i < e; ++i) {
+            int c = a.context_lens[i];
+            c = c < 0 ? 0 : (c > cap ? cap : c);
+            local += (c + C::SUB - 1) / C::SUB;
+        }
+        int incl = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (lane == 31) scratch[warp] = incl;
+        __syncthreads();
+        int run = incl - local;
+        for (int i = 0; i < warp; ++i) run += scratch[i];
+        for (int i = b; i < e; ++i) {
+            base[i] = run;
+            int c = a.context_lens[i];
+            c = c < 0 ? 0 : (c > cap ? cap : c);
+            run += (c + C::SUB - 1) / C::SUB;
+        }
+        if (tid == 127) base[S] = run;
+        __syncthreads();
+    }
     const int64_t sh = (int64_t)blockIdx.x * 4 + warp;
-    grid_dependency_wait();
-    if (sh >= (int64_t)a.S * a.H) return;
-    const int64_t L = reinterpret_cast<const int64_t*>(a.ws)[0];
-    if (L <= 0) return;
-    const int* base = reinterpret_cast<const int*>(a.ws + a.ws_l.base_off);
-    const int s = (int)(sh / a.H), h = (int)(sh - (int64_t)s * a.H);
+    if (sh >= (int64_t)S * H) return;
+    const int s = (int)(sh / H), h = (int)(sh - (int64_t)s * H);
     const int ns = base[s + 1] - base[s];
+    const int64_t total = (int64_t)H * base[S];
+    int64_t L = a.L_steps;
+    if (L <= 0) {
+        L = (total + a.main_grid - 1) / a.main_grid;
+        if (L < a.min_chunk_steps) L = a.min_chunk_steps;
+    }
+    const int64_t x0 = (int64_t)H * base[s] + (int64_t)h * ns;
+    const int64_t kf = ns ? x0 / L : 0, kl = ns ? (x0 + ns - 1) / L : 0;
+    if (ns > 0 && kf == kl) return;          // written by the main kernel
+
+    grid_dependency_wait();
+    // the main kernel writes L = 0 when it could not run (workspace too small)
+    if (reinterpret_cast<const int64_t*>(a.ws)[0] != L) return;
     constexpr int PER = D / 32;
     T* o = static_cast<T*>(a.out) + sh * D + lane * PER;
     if (ns == 0) {
@@ -683,33 +733,45 @@ __global__ void __launch_bounds__(128) paged_decode_merge(const DecodeArgs a) {
         for (int e = 0; e < PER; ++e) o[e] = Elem<T>::zero();
         return;
     }
-    const int64_t x0 = (int64_t)a.H * base[s] + (int64_t)h * ns;
-    const int64_t kf = x0 / L, kl = (x0 + ns - 1) / L;
-    if (kf == kl) return;
-    const float2* ml = reinterpret_cast<const float2*>(a.ws + a.ws_l.ml_off);
-    const float* accw = reinterpret_cast<const float*>(a.ws + a.ws_l.acc_off);
-    float M = -INFINITY;
-    for (int64_t k = kf + lane; k <= kl; k += 32) M = fmaxf(M, ml[sh + k].x);
-    M = warp_max(M);
-    float ls = 0.f, acc[PER];
+    const float2* ml = reinterpret_cast<const float2*>(a.ws + a.ws_l.ml_off) + sh;
+    const float* accw = reinterpret_cast<const float*>(a.ws + a.ws_l.acc_off) + sh * D + lane * PER;
+    const int nk = (int)(kl - kf + 1);
+    float M = -INFINITY, ls = 0.f, acc[PER];
 #pragma unroll
     for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-#pragma unroll 4
-    for (int64_t k = kf; k <= kl; ++k) {
-        const float2 v = ml[sh + k];
-        const float sc = exp2f(v.x - M);
-        ls = fmaf(sc, v.y, ls);
-        const float* r = accw + (sh + k) * D + lane * PER;
-        if constexpr (PER == 4) {
-            const float4 f = *reinterpret_cast<const float4*>(r);
-            acc[0] = fmaf(sc, f.x, acc[0]);
-            acc[1] = fmaf(sc, f.y, acc[1]);
-            acc[2] = fmaf(sc, f.z, acc[2]);
-            acc[3] = fmaf(sc, f.w, acc[3]);
-        } else {
-            const float2 f = *reinterpret_cast<const float2*>(r);
-            acc[0] = fmaf(sc, f.x, acc[0]);
-            acc[1] = fmaf(sc, f.y, acc[1]);
+    for (int k0 = 0; k0 < nk; k0 += kMergeBatch) {
+        float2 mv[kMergeBatch];
+        float av[kMergeBatch][PER];
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; ++u) {
+            if (k0 + u < nk) {
+                const int64_t k = kf + k0 + u;
+                mv[u] = ml[k];
+                const float* r = accw + k * D;
+                if constexpr (PER == 4) {
+                    const float4 f = *reinterpret_cast<const float4*>(r);
+                    av[u][0] = f.x; av[u][1] = f.y; av[u][2] = f.z; av[u][3] = f.w;
+                } else {
+                    const float2 f = *reinterpret_cast<const float2*>(r);
+                    av[u][0] = f.x; av[u][1] = f.y;
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; ++u) {
+            if (k0 + u < nk) {
+                if (mv[u].x > M) {
+                    const float r = exp2f(M - mv[u].x);
+                    ls *= r;
+#pragma unroll
+                    for (int e = 0; e < PER; ++e) acc[e] *= r;
+                    M = mv[u].x;
+                }
+                const float sc = exp2f(mv[u].x - M);
+                ls = fmaf(sc, mv[u].y, ls);
+#pragma unroll
+                for (int e = 0; e < PER; ++e) acc[e] = fmaf(sc, av[u][e], acc[e]);
+            }
         }
     }
 #pragma unroll
@@ -721,7 +783,14 @@ template <typename T, int D, int B>
 struct Launcher {
     using C = Cfg<D, B>;
     static size_t smem_bytes(int S) { return C::smem(S); }
+    static size_t merge_smem(int S) { return 4 * (size_t)(S + 1 + 8); }
     static cudaError_t occupancy(int* ctas, size_t smem) {
+        // the merge kernel's shared memory grows with the batch (64 KiB at the
+        // largest batch): allow it above the 48 KiB default
+        cudaError_t em = cudaFuncSetAttribute(paged_decode_merge<T, D, B>,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              (int)merge_smem(PKV_MAX_SEQS));
+        if (em != cudaSuccess) return em;
         cudaError_t e = cudaFuncSetAttribute(paged_decode_main<T, D, B>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)smem);
@@ -732,7 +801,9 @@ struct Launcher {
     // Both kernels are launched as programmatic dependents of their
     // predecessor in the stream: each waits (griddepcontrol.wait) before it
     // reads anything, so only the launch latency overlaps the predecessor.
-    static cudaError_t launch(const DecodeArgs& a, int grid, cudaStream_t stream) {
+    static cudaError_t launch(const DecodeArgs& args, int grid, cudaStream_t stream) {
+        DecodeArgs a = args;
+        a.main_grid = grid;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -748,8 +819,8 @@ struct Launcher {
         const int64_t warps = (int64_t)a.S * a.H;
         cfg.gridDim = dim3((unsigned)((warps + 3) / 4));
         cfg.blockDim = dim3(128);
-        cfg.dynamicSmemBytes = 0;
-        e = cudaLaunchKernelEx(&cfg, paged_decode_merge<T, D>, a);
+        cfg.dynamicSmemBytes = merge_smem(a.S);
+        e = cudaLaunchKernelEx(&cfg, paged_decode_merge<T, D, B>, a);
         if (e != cudaSuccess) return e;
         return cudaGetLastError();
     }

@@ -65,6 +65,7 @@ struct DecodeArgs {
     int64_t num_blocks;
     int64_t L_steps;         // fixed chunk length in steps, 0 = balanced
     int min_chunk_steps;     // balanced mode: lower bound of the chunk length
+    int main_grid;           // CTAs of the main kernel (the balanced chunk count)
     char* ws;
     WsLayout ws_l;
     int32_t* err;
