@@ -319,6 +319,26 @@ def sized_sample(wl: Workload, budget_s: float, threads: int):
         take, acc = sel, b
     return take
 
+def max_over_ranks(x: float, dist) -> float:
+    """The maximum of x over all ranks (x itself without a process group)."""
+    if dist is None:
+        return x
+    import torch
+    if dist.get_backend() == "nccl":
+        dev = torch.device("cuda", torch.cuda.current_device())
+    else:
+        dev = torch.device("cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(bytes_per_rank: int, seconds: float, world: int) -> float:
+    """Weak scaling: every rank processes the same per-rank work; the job's
+    rate is all ranks' bytes over the slowest rank's time, in GB/s."""
+    return world * bytes_per_rank / seconds / 1e9
+
+
 def host_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -398,23 +418,16 @@ def main():
     if dist is not None:
         dist.barrier()
     clocks = sampler.stop()
-    ms_total = t_start.elapsed_time(t_end)
+    ms_total = max_over_ranks(t_start.elapsed_time(t_end), dist)
     attn_avg = a_start.elapsed_time(a_end) / K
-    if dist is not None:
-        t = torch.tensor([ms_total], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
     ms_step = ms_total / K
-    value = world * wl.step_bytes / (ms_step * 1e-3) / 1e9
+    value = whole_job_rate(wl.step_bytes, ms_step * 1e-3, world)
 
     # ---- end to end: host (pinned) inputs -> C ABI -> host output, every step
     e2e = None
     if args.e2e_steps > 0:
         e2e = measure_e2e(wl, args.e2e_steps, device, dist)
-        if dist is not None:
-            t = torch.tensor([e2e["seconds"]], dtype=torch.float64, device=device)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e["seconds"] = float(t.item())
+        e2e["seconds"] = max_over_ranks(e2e["seconds"], dist)
 
     if wl.pkv.get_device_error() != 0:
         raise SystemExit("bench.py: device error bits after the timed region")
@@ -471,7 +484,8 @@ def main():
     if wl.unique_kv_bytes is not None:
         line["config"]["unique_kv_bytes"] = wl.unique_kv_bytes
     if e2e is not None:
-        line["e2e"] = {"value": round(world * wl.step_bytes / (e2e["seconds"] / e2e["steps"]) / 1e9, 1),
+        line["e2e"] = {"value": round(whole_job_rate(wl.step_bytes, e2e["seconds"] / e2e["steps"],
+                                                    world), 1),
                        "unit": "GB/s", "h2d_bytes_per_step": e2e["h2d"],
                        "d2h_bytes_per_step": e2e["d2h"], "steps": e2e["steps"],
                        "us_per_step": round(1e6 * e2e["seconds"] / e2e["steps"], 2),
