@@ -100,8 +100,9 @@ typedef enum { PKV_F16 = 0, PKV_BF16 = 1 } pkv_dtype;
  * partition_size: split length in tokens of the split-K pass, or 0 for the
  * balanced split (each CTA of a persistent grid takes an equal share of the
  * batch's K/V).  A nonzero value must be a positive multiple of the kernel's
- * step (16 tokens for head_dim 128, 32 for head_dim 64, or block_size if
- * smaller).  Host only; never touches the GPU.
+ * step: 16 tokens for head_dim 128, 32 for head_dim 64 (4 KiB of K per step,
+ * gathered from several blocks when block_size is smaller).  Host only; never
+ * touches the GPU.
  */
 pkv_status pkv_decode_workspace_size(int num_seqs, int num_heads, int head_dim,
                                      int block_size, int max_blocks_per_seq,

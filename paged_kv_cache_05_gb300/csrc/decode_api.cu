@@ -51,8 +51,8 @@ pkv_status check_shape(int S, int H, int D, int B, int max_blocks, int partition
     if (B != 8 && B != 16 && B != 32 && B != 64)
         return pkv::fail(PKV_ERR_INVALID, "%s: block_size must be 8, 16, 32 or 64", fn);
     if (max_blocks < 1) return pkv::fail(PKV_ERR_INVALID, "%s: max_blocks_per_seq must be >= 1", fn);
-    const int sub = pkv::step_tokens(D, B);
-    const int64_t steps = (int64_t)S * max_blocks * (B / sub);
+    const int sub = pkv::step_tokens(D);
+    const int64_t steps = (int64_t)S * pkv::max_steps_per_seq(D, B, max_blocks);
     if (steps >= (1LL << 31) || steps * H >= (1LL << 62))
         return pkv::fail(PKV_ERR_INVALID, "%s: batch too large (step count overflows)", fn);
     if (partition_size < 0 || (partition_size > 0 && partition_size % sub != 0))
@@ -64,9 +64,8 @@ pkv_status check_shape(int S, int H, int D, int B, int max_blocks, int partition
 
 int64_t max_chunks(int S, int H, int D, int B, int max_blocks, int partition_size) {
     if (partition_size == 0) return PKV_MAX_GRID;
-    const int sub = pkv::step_tokens(D, B);
-    const int64_t L = partition_size / sub;
-    const int64_t steps = (int64_t)S * H * max_blocks * (B / sub);
+    const int64_t L = partition_size / pkv::step_tokens(D);
+    const int64_t steps = (int64_t)S * H * pkv::max_steps_per_seq(D, B, max_blocks);
     return (steps + L - 1) / L;
 }
 
@@ -136,6 +135,15 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* k_ca
     int grid = pkv::sm_count(dev) * per_sm;
     if (grid < 1) return pkv::fail(PKV_ERR_CUDA, "%s: no multiprocessors", fn);
     if (grid > PKV_MAX_GRID) grid = PKV_MAX_GRID;
+    {
+        // small batches: no more CTAs than balanced chunks of the minimum length
+        // the batch could fill (the bound uses max_blocks_per_seq, not the
+        // device-side lengths)
+        const int64_t steps_bound = (int64_t)num_seqs * num_heads *
+                                    pkv::max_steps_per_seq(head_dim, block_size, max_blocks_per_seq);
+        const int64_t useful = (steps_bound + kMinChunkSteps - 1) / kMinChunkSteps;
+        if (useful < grid) grid = (int)(useful > 0 ? useful : 1);
+    }
     int32_t* err = pkv::device_error_word();
     if (!err) return pkv::fail(PKV_ERR_CUDA, "%s: no device error word", fn);
 
@@ -151,7 +159,7 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* k_ca
     a.H = num_heads;
     a.max_blocks = max_blocks_per_seq;
     a.num_blocks = num_blocks;
-    a.L_steps = partition_size > 0 ? partition_size / pkv::step_tokens(head_dim, block_size) : 0;
+    a.L_steps = partition_size > 0 ? partition_size / pkv::step_tokens(head_dim) : 0;
     a.min_chunk_steps = kMinChunkSteps;
     a.main_grid = grid;
     a.ws = static_cast<char*>(workspace);

@@ -211,8 +211,10 @@ template <int D, int B>
 struct Cfg {
     static constexpr int NW = PKV_DECODE_WARPS;         // consumer warps
     static constexpr int THREADS = (NW + 1) * 32;       // + one producer warp
-    static constexpr int SUB = step_tokens(D, B);       // tokens per step
-    static constexpr int SPB = B / SUB;                 // steps per block
+    static constexpr int SUB = step_tokens(D);          // tokens per step
+    static constexpr int SPB = B > SUB ? B / SUB : 1;   // steps per block
+    static constexpr int BPS = B < SUB ? SUB / B : 1;   // blocks per step
+    static constexpr int TPC = B < SUB ? B : SUB;       // tokens per bulk copy
     static constexpr int CHUNK = SUB * D * 2;           // bytes of K (or V) per step
     static constexpr int STAGE = 2 * CHUNK;
     // Step g uses stage g % NSTAGE and is consumed by warp g % NW.  NSTAGE must
@@ -238,7 +240,8 @@ struct Cfg {
     static_assert(NL >= 1 && NL <= LPT, "step layout");
     static_assert(NSTAGE >= NW && NSTAGE % NW == 0, "ring depth: a multiple of the warps");
     static_assert(TPL * NL == SUB, "tokens per step");
-    static_assert(B % SUB == 0, "steps per block");
+    static_assert(B % SUB == 0 || SUB % B == 0, "steps and blocks nest");
+    static_assert(BPS <= 32 && 32 % BPS == 0, "a step's blocks share one table window");
     static __host__ __device__ size_t smem(int S) {
         return CTX_OFF + 4 * (size_t)S + 4 * (size_t)(S + 1);
     }
@@ -431,8 +434,9 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, PKV_DECODE_MIN_CTAS)
             const int32_t* row = a.block_tables + (int64_t)p.s * a.max_blocks;
             for (int i = 0; i < run; ++i) {
                 const int j = p.j + i;
-                const int jb = j / C::SPB;
-                const int sub = j - jb * C::SPB;
+                // first logical block of the step, and the step's token offset in it
+                const int jb = C::BPS > 1 ? j * C::BPS : j / C::SPB;
+                const int sub = C::BPS > 1 ? 0 : j - jb * C::SPB;
                 const int win = jb & ~31;
                 if (p.s != tc_s || win != tc_win) {
                     if (p.s == tc_s && win == tc_win + 32 && tn_ok) {
@@ -458,22 +462,43 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, PKV_DECODE_MIN_CTAS)
                     tn_ok = win + 32 < nblk;
                     if (tn_ok) tn_val = (win + 32 + lane < nblk) ? __ldg(row + win + 32 + lane) : 0;
                 }
-                const int phys_raw = __shfl_sync(kFull, tc_val, jb - win);
+                int phys_raw[C::BPS];
+#pragma unroll
+                for (int b = 0; b < C::BPS; ++b)
+                    phys_raw[b] = __shfl_sync(kFull, tc_val, jb + b - win);
                 int ok = 1;
                 if (lane == 0) {
                     ok = wait_phase(&empty[stage], phase ^ 1u, abort_flag) ? 1 : 0;
                     if (ok) {
-                        int64_t phys = phys_raw;
-                        if (phys < 0 || phys >= a.num_blocks) {
-                            atomicOr(a.err, PKV_DEVERR_BAD_BLOCK);
-                            phys = 0;
+                        // only the step's valid tokens move (the last step of a
+                        // row is usually partial); the rest of the stage keeps
+                        // stale bytes that the consumers mask out
+                        const int tok0 = j * C::SUB;
+                        uint32_t bytes[C::BPS];
+                        uint32_t tx = 0;
+#pragma unroll
+                        for (int b = 0; b < C::BPS; ++b) {
+                            int valid = s_ctx[p.s] - (tok0 + b * C::TPC);
+                            valid = valid < 0 ? 0 : (valid > C::TPC ? C::TPC : valid);
+                            bytes[b] = (uint32_t)valid * (uint32_t)(D * 2);
+                            tx += 2 * bytes[b];
                         }
-                        const int64_t off =
-                            ((phys * H + p.h) * B + (int64_t)sub * C::SUB) * (int64_t)D * 2;
                         unsigned char* dst = ring + (size_t)stage * C::STAGE;
-                        mbar_arrive_expect_tx(&full[stage], C::STAGE);
-                        bulk_g2s(dst, kpool + off, C::CHUNK, &full[stage]);
-                        bulk_g2s(dst + C::CHUNK, vpool + off, C::CHUNK, &full[stage]);
+                        mbar_arrive_expect_tx(&full[stage], tx);
+#pragma unroll
+                        for (int b = 0; b < C::BPS; ++b) {
+                            if (bytes[b] == 0) continue;
+                            int64_t phys = phys_raw[b];
+                            if (phys < 0 || phys >= a.num_blocks) {
+                                atomicOr(a.err, PKV_DEVERR_BAD_BLOCK);
+                                phys = 0;
+                            }
+                            const int64_t off =
+                                ((phys * H + p.h) * B + (int64_t)sub * C::SUB) * (int64_t)D * 2;
+                            const uint32_t doff = (uint32_t)(b * C::TPC * D * 2);
+                            bulk_g2s(dst + doff, kpool + off, bytes[b], &full[stage]);
+                            bulk_g2s(dst + C::CHUNK + doff, vpool + off, bytes[b], &full[stage]);
+                        }
                     }
                 }
                 ok = __shfl_sync(kFull, ok, 0);

@@ -46,10 +46,14 @@ __host__ __device__ inline WsLayout ws_layout(int S, int H, int D, int64_t max_c
     return w;
 }
 
-// Tokens per pipeline step: a step moves SUB tokens of one (block, head) for K
-// and for V, at most 4 KiB each.
-__host__ __device__ constexpr int step_tokens(int D, int B) {
-    return B < 2048 / D ? B : 2048 / D;
+// Tokens per pipeline step: a step moves 4 KiB of K and 4 KiB of V (16 tokens
+// at head_dim 128, 32 at head_dim 64), from one block or from several
+// consecutive logical blocks when the block size is smaller.
+__host__ __device__ constexpr int step_tokens(int D) { return 2048 / D; }
+
+// Upper bound of the steps one sequence can have.
+__host__ __device__ inline int64_t max_steps_per_seq(int D, int B, int max_blocks) {
+    return ((int64_t)max_blocks * B + step_tokens(D) - 1) / step_tokens(D);
 }
 
 // ---- decode kernel dispatch ---------------------------------------------------

@@ -42,7 +42,7 @@ def run_oracle(case, scale):
 
 
 def step_tokens(D, B):
-    return min(B, 2048 // D)
+    return 2048 // D
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
@@ -189,7 +189,7 @@ def test_tiny_workload_full_step(pkv):
         bt_model[s, :len(t)] = t
     expect = oracle.paged_attention_decode(q, kc, vc, bt_model, ctx, scale)
     dq = to_dev(q, "f16")
-    for part in (0, 16, 32):
+    for part in (0, 32, 64):
         out = torch.empty_like(dq)
         pkv.paged_attention_decode(out, dq, dk, dv, torch.from_numpy(tables).cuda(),
                                    torch.from_numpy(ctx).cuda(), scale, partition_size=part)
