@@ -142,7 +142,8 @@ class ClockSampler:
 class Workload:
     """Device-resident inputs of one workload plus the algorithmic byte counts."""
 
-    def __init__(self, name: str, device, partition=None, block_size=None, layers=None):
+    def __init__(self, name: str, device, partition=None, block_size=None, layers=None,
+                 placement: str = "scattered"):
         import torch
         import paged_kv_cache_05_gb300 as pkv
         self.pkv = pkv
@@ -191,6 +192,21 @@ class Workload:
         self.max_blocks = max(1, max(-(-int(c) // B) for c in ctx))
         tables, ctx2 = bm.export(ids, self.max_blocks)
         assert np.array_equal(ctx2, ctx)
+        self.placement = placement
+        if placement == "contiguous":
+            # every sequence's blocks consecutive in the pool, in logical order
+            # (the contiguous-allocation baseline the pages compare against)
+            if name == "shared_prefix":
+                raise SystemExit("bench.py: contiguous placement is not defined with sharing")
+            nxt = 0
+            tables = np.full_like(tables, -1)
+            for s_ in ids:
+                n = -(-int(ctx[s_]) // B)
+                tables[s_, :n] = np.arange(nxt, nxt + n)
+                nxt += n
+            pos = ctx.astype(np.int64) - 1
+            slots = tables[np.arange(len(ids)), pos // B].astype(np.int64) * B + pos % B
+            pairs = np.zeros((0, 2), np.int32)
         self.tables_host = tables
         self.slots_host = slots
         self.pairs_host = pairs
@@ -259,10 +275,11 @@ class Workload:
         sp = self.spec
         c = self.ctx_host
         return ("%s: %d seqs x %d heads x %d, %s K/V, B=%d, ctx %d..%d (sum %d), pool %d blocks"
-                " x %d layer pool(s), split %s" % (
+                " x %d layer pool(s), split %s, %s placement" % (
                     self.name, self.S, self.H, self.D, sp.dtype, self.B, int(c.min()),
                     int(c.max()), int(c.sum()), self.nb, self.layers,
-                    "balanced" if self.partition == 0 else "%d tokens" % self.partition))
+                    "balanced" if self.partition == 0 else "%d tokens" % self.partition,
+                    self.placement))
 
 
 # ------------------------------------------------------------------ oracle leg
@@ -358,6 +375,9 @@ def main():
                     help="split length in tokens (0 = balanced); default: the workload's")
     ap.add_argument("--block-size", type=int, default=None)
     ap.add_argument("--layers", type=int, default=None)
+    ap.add_argument("--placement", choices=["scattered", "contiguous"], default="scattered",
+                    help="physical block placement: the block manager's scattered free list, "
+                         "or every sequence's blocks consecutive (contiguous baseline)")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -383,7 +403,8 @@ def main():
     torch.cuda.set_device(device)
     from paged_kv_cache_05_gb300 import build
     build.build()
-    wl = Workload(args.workload, device, args.partition, args.block_size, args.layers)
+    wl = Workload(args.workload, device, args.partition, args.block_size, args.layers,
+                  args.placement)
     stream = torch.cuda.current_stream()
 
     for i in range(args.warmup):
