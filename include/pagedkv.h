@@ -193,6 +193,26 @@ pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, i
                            int num_heads, int head_dim, int block_size, int64_t num_blocks,
                            pkv_dtype dtype, cudaStream_t stream);
 
+/*
+ * Block swap between a GPU pool and a CPU pool (either direction): for each
+ * pair, dst_k_cache[dst] = src_k_cache[src] and the same for V, whole blocks.
+ * Swapping evicts a preempted sequence's blocks to CPU RAM and brings them
+ * back (wywy.jp notes, "Swapping" and the preemption section: the block
+ * engine keeps a CPU pool split into blocks like the GPU one; swap space is
+ * bounded by the GPU KV pool; zhaifeiyue.github.io detail page, Scheduling
+ * table).  One kernel moves every pair at once, its SMs reading and writing
+ * the host pool over the CPU-GPU link, so small blocks do not turn into many
+ * small transfers.  Pools and pairs may be device memory, pinned (registered)
+ * host memory or managed memory (checked with cudaPointerGetAttributes;
+ * pageable host memory is refused with PKV_ERR_INVALID).  Both pools share
+ * the [blocks][H][B][D] layout; destinations must be distinct.  A bad id
+ * skips its pair and sets PKV_DEVERR_BAD_BLOCK.
+ */
+pkv_status pkv_swap_blocks(void* dst_k_cache, void* dst_v_cache, const void* src_k_cache,
+                           const void* src_v_cache, const int32_t* pairs, int num_pairs,
+                           int num_heads, int head_dim, int block_size, int64_t src_num_blocks,
+                           int64_t dst_num_blocks, pkv_dtype dtype, cudaStream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Errors                                                                    */
 /* ------------------------------------------------------------------------ */
@@ -269,6 +289,31 @@ pkv_status pkv_bm_export(const pkv_bm* bm, const int64_t* seq_ids, int n, int32_
 /* Reference count of a block (-1 if out of range); number of free blocks. */
 int32_t pkv_bm_refcount(const pkv_bm* bm, int32_t block);
 int64_t pkv_bm_num_free(const pkv_bm* bm);
+
+/*
+ * Swapping (wywy.jp notes, "Swapping", "All-or-nothing eviction" and the
+ * preemption section; zhaifeiyue.github.io detail page, Scheduling table).
+ * pkv_bm_add_cpu_pool gives the manager a CPU pool of num_cpu_blocks blocks
+ * (its own seeded free list, same policy).  pkv_bm_swap_out moves a group of
+ * resident sequences to the CPU pool, pkv_bm_swap_in moves swapped-out ones
+ * back: all of the group's blocks move together; a block shared with a
+ * sequence outside the group is refused (PKV_ERR_INVALID); each distinct
+ * block (first-seen order: group order, then table order) gets a fresh block
+ * in the other pool with the same reference count, the pair (old, new) is
+ * written to pairs[cap][2] for pkv_swap_blocks, and the old block is freed.
+ * Swapped-out sequences cannot append, fork or be exported until swapped in;
+ * freeing one releases its CPU blocks.  All-or-nothing: on failure (OOM when
+ * the other pool lacks blocks) nothing changes.
+ */
+pkv_status pkv_bm_add_cpu_pool(pkv_bm* bm, int64_t num_cpu_blocks, uint64_t seed);
+pkv_status pkv_bm_swap_out(pkv_bm* bm, const int64_t* seq_ids, int n, int32_t* pairs,
+                           int32_t cap, int32_t* num_pairs);
+pkv_status pkv_bm_swap_in(pkv_bm* bm, const int64_t* seq_ids, int n, int32_t* pairs, int32_t cap,
+                          int32_t* num_pairs);
+/* 1 if swapped out, 0 if resident, -1 if unknown. */
+int32_t pkv_bm_is_swapped(const pkv_bm* bm, int64_t seq_id);
+int32_t pkv_bm_cpu_refcount(const pkv_bm* bm, int32_t block);
+int64_t pkv_bm_num_free_cpu(const pkv_bm* bm);
 
 #ifdef __cplusplus
 }

@@ -72,6 +72,8 @@ def _load():
         lib.orc_reshape_and_cache.restype = i32
         lib.orc_copy_blocks.argtypes = [P, P, P, i32, i32, i32, i32, i64]
         lib.orc_copy_blocks.restype = i32
+        lib.orc_swap_blocks.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i64, i64]
+        lib.orc_swap_blocks.restype = i32
         _lib = lib
         return lib
 
@@ -215,3 +217,21 @@ def copy_blocks(k_cache, v_cache, pairs) -> None:
     rc = lib.orc_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(pr), pr.shape[0], H, D, B, nb)
     if rc != 0:
         raise ValueError("oracle: block id out of the pool")
+
+
+def swap_blocks(dst_k, dst_v, src_k, src_v, pairs) -> None:
+    """In place on dst: for each (src, dst) pair copy the whole block, K and V."""
+    lib = _load()
+    for c in (dst_k, dst_v):
+        if not (c.flags.c_contiguous and c.dtype in (np.uint16, np.float16, np.int16)):
+            raise TypeError("destination pools must be C-contiguous 16-bit arrays")
+    sk, sv = _words(src_k), _words(src_v)
+    pr = np.ascontiguousarray(pairs, dtype=np.int32).reshape(-1, 2)
+    snb, H, B, D = sk.shape
+    dnb = dst_k.shape[0]
+    if tuple(dst_k.shape[1:]) != (H, B, D) or sv.shape != sk.shape or dst_v.shape != dst_k.shape:
+        raise ValueError("pool shape mismatch")
+    rc = lib.orc_swap_blocks(_ptr(dst_k), _ptr(dst_v), _ptr(sk), _ptr(sv), _ptr(pr), pr.shape[0],
+                             H, D, B, snb, dnb)
+    if rc != 0:
+        raise ValueError("oracle: block id out of a pool")

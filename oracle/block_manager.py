@@ -73,8 +73,12 @@ class BlockManagerModel:
         self.B = block_size
         self.free = deque(seeded_permutation(num_blocks, seed))
         self.ref = [0] * num_blocks
-        self.tables = {}   # seq_id -> list of physical block ids
+        self.tables = {}   # seq_id -> list of physical block ids (CPU ids while swapped)
         self.ctx = {}      # seq_id -> number of tokens written
+        self.swapped = {}  # seq_id -> True while the sequence's blocks are in the CPU pool
+        self.num_cpu_blocks = 0
+        self.cpu_free = deque()
+        self.cpu_ref = []
 
     # -- queries ---------------------------------------------------------
     def num_free(self) -> int:
@@ -112,16 +116,18 @@ class BlockManagerModel:
         table = [self._take() for _ in range(need)]
         self.tables[seq_id] = table
         self.ctx[seq_id] = prompt_len
+        self.swapped[seq_id] = False
         return [self._slot(table, p) for p in range(prompt_len)]
 
     def fork(self, parent: int, child: int) -> None:
-        if parent not in self.tables or child in self.tables:
-            raise InvalidRequest("unknown parent or existing child")
+        if parent not in self.tables or child in self.tables or self.swapped[parent]:
+            raise InvalidRequest("unknown or swapped-out parent, or existing child")
         table = list(self.tables[parent])
         for blk in table:
             self.ref[blk] += 1
         self.tables[child] = table
         self.ctx[child] = self.ctx[parent]
+        self.swapped[child] = False
 
     def append_slot(self, seq_id: int):
         """Reserve the slot of the sequence's next token.
@@ -129,8 +135,8 @@ class BlockManagerModel:
         Returns (slot, cow_src, cow_dst); cow_src = cow_dst = -1 when no copy
         is needed.
         """
-        if seq_id not in self.tables:
-            raise InvalidRequest("unknown sequence")
+        if seq_id not in self.tables or self.swapped[seq_id]:
+            raise InvalidRequest("unknown or swapped-out sequence")
         table = self.tables[seq_id]
         pos = self.ctx[seq_id]
         src = dst = -1
@@ -155,8 +161,58 @@ class BlockManagerModel:
     def free_sequence(self, seq_id: int) -> None:
         if seq_id not in self.tables:
             raise InvalidRequest("unknown sequence")
+        ref, free = (self.cpu_ref, self.cpu_free) if self.swapped[seq_id] else (self.ref, self.free)
         for blk in self.tables.pop(seq_id):
-            self.ref[blk] -= 1
-            if self.ref[blk] == 0:
-                self.free.append(blk)
+            ref[blk] -= 1
+            if ref[blk] == 0:
+                free.append(blk)
         del self.ctx[seq_id]
+        del self.swapped[seq_id]
+
+    # -- swapping (wywy.jp notes: "Swapping", all-or-nothing eviction) ---------
+    def add_cpu_pool(self, num_cpu_blocks: int, seed: int) -> None:
+        if self.num_cpu_blocks or num_cpu_blocks <= 0:
+            raise InvalidRequest("CPU pool exists or has no blocks")
+        self.num_cpu_blocks = num_cpu_blocks
+        self.cpu_free = deque(seeded_permutation(num_cpu_blocks, seed))
+        self.cpu_ref = [0] * num_cpu_blocks
+
+    def _swap(self, seq_ids, out: bool):
+        if not self.num_cpu_blocks:
+            raise InvalidRequest("no CPU pool")
+        if len(set(seq_ids)) != len(seq_ids):
+            raise InvalidRequest("repeated sequence")
+        for sid in seq_ids:
+            if sid not in self.tables or self.swapped[sid] == out:
+                raise InvalidRequest("unknown sequence or already in the target pool")
+        uses = {}
+        for sid in seq_ids:
+            for blk in self.tables[sid]:
+                uses[blk] = uses.get(blk, 0) + 1     # dict keeps first-seen order
+        src_ref, src_free = (self.ref, self.free) if out else (self.cpu_ref, self.cpu_free)
+        dst_ref, dst_free = (self.cpu_ref, self.cpu_free) if out else (self.ref, self.free)
+        if any(src_ref[b] != n for b, n in uses.items()):
+            raise InvalidRequest("a block is shared outside the group")
+        if len(uses) > len(dst_free):
+            raise OutOfBlocks()
+        moved, pairs = {}, []
+        for blk in uses:
+            new = dst_free.popleft()
+            dst_ref[new] = src_ref[blk]
+            moved[blk] = new
+            pairs.append((blk, new))
+        for blk in uses:
+            src_ref[blk] = 0
+            src_free.append(blk)
+        for sid in seq_ids:
+            self.tables[sid] = [moved[b] for b in self.tables[sid]]
+            self.swapped[sid] = out
+        return pairs
+
+    def swap_out(self, seq_ids) -> list:
+        """Move a group of resident sequences to the CPU pool; returns (gpu, cpu) pairs."""
+        return self._swap(list(seq_ids), True)
+
+    def swap_in(self, seq_ids) -> list:
+        """Move a group of swapped-out sequences back; returns (cpu, gpu) pairs."""
+        return self._swap(list(seq_ids), False)

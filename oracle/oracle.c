@@ -251,3 +251,23 @@ int orc_copy_blocks(uint16_t* k_cache, uint16_t* v_cache, const int32_t* pairs, 
     }
     return 0;
 }
+
+/*
+ * Swap between two pools (GPU and CPU swap space, wywy.jp notes, "Swapping"):
+ * for each pair (src, dst), dst pool block dst = src pool block src, whole
+ * blocks, K and V.
+ */
+int orc_swap_blocks(uint16_t* dst_k, uint16_t* dst_v, const uint16_t* src_k,
+                    const uint16_t* src_v, const int32_t* pairs, int P, int H, int D, int B,
+                    int64_t src_blocks, int64_t dst_blocks) {
+    int64_t words = (int64_t)H * B * D;
+    for (int p = 0; p < P; ++p) {
+        int64_t src = pairs[2 * p], dst = pairs[2 * p + 1];
+        if (src < 0 || src >= src_blocks || dst < 0 || dst >= dst_blocks) return -1;
+        for (int64_t w = 0; w < words; ++w) {
+            dst_k[dst * words + w] = src_k[src * words + w];
+            dst_v[dst * words + w] = src_v[src * words + w];
+        }
+    }
+    return 0;
+}

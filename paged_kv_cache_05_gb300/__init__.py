@@ -6,8 +6,8 @@ seeded synthetic inputs.  Build with ``python -m paged_kv_cache_05_gb300.build``
 """
 from .pagedkv import (BlockManager, OutOfBlocks, PagedKVError, alloc_workspace, copy_blocks,
                       decode_workspace_size, get_device_error, lib, paged_attention_decode,
-                      reshape_and_cache, version)
+                      reshape_and_cache, swap_blocks, version)
 
 __all__ = ["BlockManager", "OutOfBlocks", "PagedKVError", "alloc_workspace", "copy_blocks",
            "decode_workspace_size", "get_device_error", "lib", "paged_attention_decode",
-           "reshape_and_cache", "version"]
+           "reshape_and_cache", "swap_blocks", "version"]

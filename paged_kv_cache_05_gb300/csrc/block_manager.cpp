@@ -36,9 +36,23 @@ struct SplitMix64 {
 };
 
 struct Sequence {
-    std::vector<int32_t> table;
+    std::vector<int32_t> table;   // GPU block ids, or CPU block ids while swapped out
     int32_t ctx = 0;
+    bool swapped = false;
 };
+
+std::vector<int32_t> seeded_permutation(int64_t n, uint64_t seed) {
+    std::vector<int32_t> perm((size_t)n);
+    for (int64_t i = 0; i < n; ++i) perm[(size_t)i] = (int32_t)i;
+    SplitMix64 rng{seed};
+    for (int64_t i = n - 1; i > 0; --i) {
+        const int64_t j = (int64_t)(rng.next() % (uint64_t)(i + 1));
+        const int32_t t = perm[(size_t)i];
+        perm[(size_t)i] = perm[(size_t)j];
+        perm[(size_t)j] = t;
+    }
+    return perm;
+}
 
 }  // namespace
 
@@ -48,6 +62,10 @@ struct pkv_bm {
     std::deque<int32_t> free_list;
     std::vector<int32_t> ref;
     std::unordered_map<int64_t, Sequence> seqs;
+    // CPU swap pool (empty until pkv_bm_add_cpu_pool)
+    int64_t num_cpu_blocks = 0;
+    std::deque<int32_t> cpu_free;
+    std::vector<int32_t> cpu_ref;
 
     int64_t slot_of(const Sequence& sq, int64_t pos) const {
         return (int64_t)sq.table[pos / B] * B + pos % B;
@@ -97,15 +115,7 @@ pkv_status pkv_bm_create(int64_t num_blocks, int block_size, uint64_t seed, pkv_
     if (!bm) return pkv::fail(PKV_ERR_OOM, "pkv_bm_create: host allocation failed");
     bm->num_blocks = num_blocks;
     bm->B = block_size;
-    std::vector<int32_t> perm((size_t)num_blocks);
-    for (int64_t i = 0; i < num_blocks; ++i) perm[(size_t)i] = (int32_t)i;
-    SplitMix64 rng{seed};
-    for (int64_t i = num_blocks - 1; i > 0; --i) {
-        const int64_t j = (int64_t)(rng.next() % (uint64_t)(i + 1));
-        const int32_t t = perm[(size_t)i];
-        perm[(size_t)i] = perm[(size_t)j];
-        perm[(size_t)j] = t;
-    }
+    std::vector<int32_t> perm = seeded_permutation(num_blocks, seed);
     bm->free_list.assign(perm.begin(), perm.end());
     bm->ref.assign((size_t)num_blocks, 0);
     *out = bm;
@@ -140,6 +150,8 @@ pkv_status pkv_bm_fork(pkv_bm* bm, int64_t parent, int64_t child) {
     auto it = bm->seqs.find(parent);
     if (it == bm->seqs.end() || bm->seqs.count(child))
         return pkv::fail(PKV_ERR_INVALID, "pkv_bm_fork: unknown parent or existing child");
+    if (it->second.swapped)
+        return pkv::fail(PKV_ERR_INVALID, "pkv_bm_fork: parent is swapped out");
     Sequence sq = it->second;
     for (int32_t b : sq.table) bm->ref[b] += 1;
     bm->seqs.emplace(child, std::move(sq));
@@ -154,8 +166,8 @@ pkv_status pkv_bm_append_slot(pkv_bm* bm, int64_t seq_id, int64_t* slot, int32_t
     if (it == bm->seqs.end())
         return pkv::fail(PKV_ERR_INVALID, "pkv_bm_append_slot: unknown sequence %lld",
                          (long long)seq_id);
-    if (it->second.ctx == INT32_MAX)
-        return pkv::fail(PKV_ERR_INVALID, "pkv_bm_append_slot: sequence full");
+    if (it->second.ctx == INT32_MAX || it->second.swapped)
+        return pkv::fail(PKV_ERR_INVALID, "pkv_bm_append_slot: sequence full or swapped out");
     if (bm->blocks_for_append(it->second) > (int)bm->free_list.size())
         return pkv::fail(PKV_ERR_OOM, "pkv_bm_append_slot: no free block");
     bm->append(it->second, slot, cow_src, cow_dst);
@@ -171,9 +183,11 @@ pkv_status pkv_bm_append_slots(pkv_bm* bm, const int64_t* seq_ids, int n, int64_
     int64_t need = 0;
     for (int i = 0; i < n; ++i) {
         auto it = bm->seqs.find(seq_ids[i]);
-        if (it == bm->seqs.end() || seen.count(seq_ids[i]) || it->second.ctx == INT32_MAX)
+        if (it == bm->seqs.end() || seen.count(seq_ids[i]) || it->second.ctx == INT32_MAX ||
+            it->second.swapped)
             return pkv::fail(PKV_ERR_INVALID,
-                             "pkv_bm_append_slots: unknown, repeated or full sequence %lld",
+                             "pkv_bm_append_slots: unknown, repeated, full or swapped-out "
+                             "sequence %lld",
                              (long long)seq_ids[i]);
         seen[seq_ids[i]] = i;
     }
@@ -219,8 +233,12 @@ pkv_status pkv_bm_free_sequence(pkv_bm* bm, int64_t seq_id) {
     if (it == bm->seqs.end())
         return pkv::fail(PKV_ERR_INVALID, "pkv_bm_free_sequence: unknown sequence %lld",
                          (long long)seq_id);
-    for (int32_t b : it->second.table) {
-        if (--bm->ref[b] == 0) bm->free_list.push_back(b);
+    if (it->second.swapped) {
+        for (int32_t b : it->second.table)
+            if (--bm->cpu_ref[b] == 0) bm->cpu_free.push_back(b);
+    } else {
+        for (int32_t b : it->second.table)
+            if (--bm->ref[b] == 0) bm->free_list.push_back(b);
     }
     bm->seqs.erase(it);
     return PKV_OK;
@@ -262,6 +280,9 @@ pkv_status pkv_bm_export(const pkv_bm* bm, const int64_t* seq_ids, int n, int32_
                              (long long)seq_ids[i]);
         if ((int64_t)it->second.table.size() > max_blocks)
             return pkv::fail(PKV_ERR_INVALID, "pkv_bm_export: table longer than max_blocks");
+        if (it->second.swapped)
+            return pkv::fail(PKV_ERR_INVALID, "pkv_bm_export: sequence %lld is swapped out",
+                             (long long)seq_ids[i]);
     }
     for (int i = 0; i < n; ++i) {
         const Sequence& sq = bm->seqs.find(seq_ids[i])->second;
@@ -273,6 +294,102 @@ pkv_status pkv_bm_export(const pkv_bm* bm, const int64_t* seq_ids, int n, int32_
     }
     return PKV_OK;
 }
+
+pkv_status pkv_bm_add_cpu_pool(pkv_bm* bm, int64_t num_cpu_blocks, uint64_t seed) {
+    if (!bm) return pkv::fail(PKV_ERR_INVALID, "pkv_bm_add_cpu_pool: NULL manager");
+    if (bm->num_cpu_blocks != 0)
+        return pkv::fail(PKV_ERR_INVALID, "pkv_bm_add_cpu_pool: the manager has a CPU pool");
+    if (num_cpu_blocks < 1 || num_cpu_blocks > INT32_MAX)
+        return pkv::fail(PKV_ERR_INVALID, "pkv_bm_add_cpu_pool: num_cpu_blocks out of range");
+    std::vector<int32_t> perm = seeded_permutation(num_cpu_blocks, seed);
+    bm->cpu_free.assign(perm.begin(), perm.end());
+    bm->cpu_ref.assign((size_t)num_cpu_blocks, 0);
+    bm->num_cpu_blocks = num_cpu_blocks;
+    return PKV_OK;
+}
+
+// Swap a group of sequences between the pools (out: GPU -> CPU, in: CPU -> GPU).
+// All of their blocks move together (all-or-nothing eviction); a block shared
+// with a sequence outside the group cannot move.  Distinct blocks are taken in
+// first-seen order (group order, then table order); each gets a fresh block in
+// the other pool with the same reference count; the old blocks are freed in
+// the same order.
+static pkv_status swap_group(pkv_bm* bm, const int64_t* seq_ids, int n, int32_t* pairs,
+                             int32_t cap, int32_t* num_pairs, bool out, const char* fn) {
+    if (!bm || n < 0 || (n > 0 && !seq_ids) || !num_pairs || cap < 0 || (cap > 0 && !pairs))
+        return pkv::fail(PKV_ERR_INVALID, "%s: bad argument", fn);
+    if (bm->num_cpu_blocks == 0) return pkv::fail(PKV_ERR_INVALID, "%s: no CPU pool", fn);
+    std::unordered_map<int64_t, int> seen;
+    std::vector<int32_t> order;                        // distinct blocks, first-seen order
+    std::unordered_map<int32_t, int32_t> uses;         // references from within the group
+    for (int i = 0; i < n; ++i) {
+        auto it = bm->seqs.find(seq_ids[i]);
+        if (it == bm->seqs.end() || seen.count(seq_ids[i]) || it->second.swapped == out)
+            return pkv::fail(PKV_ERR_INVALID, "%s: unknown, repeated or %s sequence %lld", fn,
+                             out ? "already swapped-out" : "resident", (long long)seq_ids[i]);
+        seen[seq_ids[i]] = i;
+        for (int32_t b : it->second.table) {
+            if (uses[b]++ == 0) order.push_back(b);
+        }
+    }
+    const std::vector<int32_t>& from_ref = out ? bm->ref : bm->cpu_ref;
+    for (int32_t b : order)
+        if (from_ref[(size_t)b] != uses[b])
+            return pkv::fail(PKV_ERR_INVALID, "%s: block %d is shared outside the group", fn, b);
+    std::deque<int32_t>& to_free = out ? bm->cpu_free : bm->free_list;
+    if ((int64_t)order.size() > (int64_t)to_free.size())
+        return pkv::fail(PKV_ERR_OOM, "%s: %zu blocks needed, %zu free", fn, order.size(),
+                         to_free.size());
+    if ((int64_t)order.size() > cap)
+        return pkv::fail(PKV_ERR_INVALID, "%s: %zu pairs, capacity %d", fn, order.size(), cap);
+    std::vector<int32_t>& fref = out ? bm->ref : bm->cpu_ref;
+    std::vector<int32_t>& tref = out ? bm->cpu_ref : bm->ref;
+    std::deque<int32_t>& from_free = out ? bm->free_list : bm->cpu_free;
+    std::unordered_map<int32_t, int32_t> moved;
+    for (size_t k = 0; k < order.size(); ++k) {
+        const int32_t b = order[k];
+        const int32_t nb = to_free.front();
+        to_free.pop_front();
+        tref[(size_t)nb] = fref[(size_t)b];
+        moved[b] = nb;
+        pairs[2 * k] = b;
+        pairs[2 * k + 1] = nb;
+    }
+    for (int32_t b : order) {
+        fref[(size_t)b] = 0;
+        from_free.push_back(b);
+    }
+    for (int i = 0; i < n; ++i) {
+        Sequence& sq = bm->seqs.find(seq_ids[i])->second;
+        for (int32_t& b : sq.table) b = moved[b];
+        sq.swapped = out;
+    }
+    *num_pairs = (int32_t)order.size();
+    return PKV_OK;
+}
+
+pkv_status pkv_bm_swap_out(pkv_bm* bm, const int64_t* seq_ids, int n, int32_t* pairs,
+                           int32_t cap, int32_t* num_pairs) {
+    return swap_group(bm, seq_ids, n, pairs, cap, num_pairs, true, "pkv_bm_swap_out");
+}
+
+pkv_status pkv_bm_swap_in(pkv_bm* bm, const int64_t* seq_ids, int n, int32_t* pairs, int32_t cap,
+                          int32_t* num_pairs) {
+    return swap_group(bm, seq_ids, n, pairs, cap, num_pairs, false, "pkv_bm_swap_in");
+}
+
+int32_t pkv_bm_is_swapped(const pkv_bm* bm, int64_t seq_id) {
+    if (!bm) return -1;
+    auto it = bm->seqs.find(seq_id);
+    return it == bm->seqs.end() ? -1 : (it->second.swapped ? 1 : 0);
+}
+
+int32_t pkv_bm_cpu_refcount(const pkv_bm* bm, int32_t block) {
+    if (!bm || block < 0 || block >= bm->num_cpu_blocks) return -1;
+    return bm->cpu_ref[(size_t)block];
+}
+
+int64_t pkv_bm_num_free_cpu(const pkv_bm* bm) { return bm ? (int64_t)bm->cpu_free.size() : -1; }
 
 int32_t pkv_bm_refcount(const pkv_bm* bm, int32_t block) {
     if (!bm || block < 0 || block >= bm->num_blocks) return -1;

@@ -104,9 +104,56 @@ __global__ void __launch_bounds__(kCopyThreads) copy_blocks_kernel(
     }
 }
 
+// Block swap between two pools, one of which may live in pinned host memory
+// (reached over NVLink-C2C / PCIe through unified addressing): grid =
+// (pieces, pairs, 2), blockIdx.z picks K or V.  Plain (coherent) loads, since
+// the source may be host memory; each thread keeps kCopyUnroll vectors in flight.
+__global__ void __launch_bounds__(kCopyThreads) swap_blocks_kernel(
+    uint4* __restrict__ dst_k, uint4* __restrict__ dst_v, const uint4* __restrict__ src_k,
+    const uint4* __restrict__ src_v, const int32_t* __restrict__ pairs, int64_t vecs_per_block,
+    int64_t src_blocks, int64_t dst_blocks, int32_t* err) {
+    pdl_wait_then_release();
+    const int p = blockIdx.y;
+    const int64_t src = pairs[2 * p], dst = pairs[2 * p + 1];
+    if (src < 0 || src >= src_blocks || dst < 0 || dst >= dst_blocks) {
+        if (blockIdx.x == 0 && blockIdx.z == 0 && threadIdx.x == 0)
+            atomicOr(err, PKV_DEVERR_BAD_BLOCK);
+        return;
+    }
+    const uint4* s = (blockIdx.z == 0 ? src_k : src_v) + src * vecs_per_block;
+    uint4* d = (blockIdx.z == 0 ? dst_k : dst_v) + dst * vecs_per_block;
+    const int64_t base = (int64_t)blockIdx.x * kCopyThreads * kCopyUnroll + threadIdx.x;
+    uint4 buf[kCopyUnroll];
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+        const int64_t i = base + (int64_t)u * kCopyThreads;
+        if (i < vecs_per_block) buf[u] = s[i];
+    }
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+        const int64_t i = base + (int64_t)u * kCopyThreads;
+        if (i < vecs_per_block) d[i] = buf[u];
+    }
+}
+
 }  // namespace
 
 namespace pkv {
+
+cudaError_t launch_swap_blocks(void* dst_k, void* dst_v, const void* src_k, const void* src_v,
+                               const int32_t* pairs, int P, int H, int D, int B,
+                               int64_t src_blocks, int64_t dst_blocks, int32_t* err,
+                               cudaStream_t stream) {
+    const int64_t vecs = (int64_t)H * B * D / 8;
+    const int64_t per_cta = kCopyThreads * kCopyUnroll;
+    dim3 grid((unsigned)((vecs + per_cta - 1) / per_cta), (unsigned)P, 2);
+    cudaError_t e = launch_pdl(swap_blocks_kernel, grid, dim3(kCopyThreads), stream,
+                               static_cast<uint4*>(dst_k), static_cast<uint4*>(dst_v),
+                               static_cast<const uint4*>(src_k), static_cast<const uint4*>(src_v),
+                               pairs, vecs, src_blocks, dst_blocks, err);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
 
 cudaError_t launch_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,
                                      const int64_t* slots, int T, int H, int D, int B,
@@ -141,6 +188,18 @@ cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pair
 namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// Device memory, pinned (registered) host memory or managed memory: what a
+// kernel may dereference.  Pageable host memory is refused.
+bool device_reachable(const void* p) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeHost ||
+           at.type == cudaMemoryTypeManaged;
+}
 
 pkv_status check_common(int H, int D, int B, int64_t num_blocks, pkv_dtype dtype,
                         const char* fn) {
@@ -198,6 +257,37 @@ pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, i
     if (!err) return pkv::fail(PKV_ERR_CUDA, "%s: no CUDA device", fn);
     cudaError_t e = pkv::launch_copy_blocks(k_cache, v_cache, pairs, num_pairs, num_heads,
                                             head_dim, block_size, num_blocks, err, stream);
+    if (e != cudaSuccess) return pkv::cuda_fail(e, fn);
+    return PKV_OK;
+}
+
+pkv_status pkv_swap_blocks(void* dst_k_cache, void* dst_v_cache, const void* src_k_cache,
+                           const void* src_v_cache, const int32_t* pairs, int num_pairs,
+                           int num_heads, int head_dim, int block_size, int64_t src_num_blocks,
+                           int64_t dst_num_blocks, pkv_dtype dtype, cudaStream_t stream) {
+    const char* fn = "pkv_swap_blocks";
+    pkv_status st = check_common(num_heads, head_dim, block_size,
+                                 src_num_blocks < dst_num_blocks ? src_num_blocks : dst_num_blocks,
+                                 dtype, fn);
+    if (st != PKV_OK) return st;
+    if (num_pairs < 0 || num_pairs > 65535)
+        return pkv::fail(PKV_ERR_INVALID, "%s: num_pairs must be in [0, 65535]", fn);
+    if (num_pairs == 0) return PKV_OK;
+    if (!dst_k_cache || !dst_v_cache || !src_k_cache || !src_v_cache || !pairs)
+        return pkv::fail(PKV_ERR_INVALID, "%s: NULL pointer", fn);
+    if (!aligned16(dst_k_cache) || !aligned16(dst_v_cache) || !aligned16(src_k_cache) ||
+        !aligned16(src_v_cache))
+        return pkv::fail(PKV_ERR_INVALID, "%s: the pools must be 16-byte aligned", fn);
+    if (!device_reachable(dst_k_cache) || !device_reachable(dst_v_cache) ||
+        !device_reachable(src_k_cache) || !device_reachable(src_v_cache) ||
+        !device_reachable(pairs))
+        return pkv::fail(PKV_ERR_INVALID,
+                         "%s: pools and pairs must be device, pinned host or managed memory", fn);
+    int32_t* err = pkv::device_error_word();
+    if (!err) return pkv::fail(PKV_ERR_CUDA, "%s: no CUDA device", fn);
+    cudaError_t e = pkv::launch_swap_blocks(dst_k_cache, dst_v_cache, src_k_cache, src_v_cache,
+                                            pairs, num_pairs, num_heads, head_dim, block_size,
+                                            src_num_blocks, dst_num_blocks, err, stream);
     if (e != cudaSuccess) return pkv::cuda_fail(e, fn);
     return PKV_OK;
 }

@@ -810,16 +810,24 @@ struct Launcher {
     static size_t smem_bytes(int S) { return C::smem(S); }
     static size_t merge_smem(int S) { return 4 * (size_t)(S + 1 + 8); }
     static cudaError_t occupancy(int* ctas, size_t smem) {
-        // the merge kernel's shared memory grows with the batch (64 KiB at the
-        // largest batch): allow it above the 48 KiB default
-        cudaError_t em = cudaFuncSetAttribute(paged_decode_merge<T, D, B>,
-                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              (int)merge_smem(PKV_MAX_SEQS));
-        if (em != cudaSuccess) return em;
-        cudaError_t e = cudaFuncSetAttribute(paged_decode_main<T, D, B>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
+        // Both kernels' shared memory grows with the batch: allow each the
+        // device's opt-in maximum once, so that any batch size launches
+        // whatever size an earlier call used.
+        int dev = 0, max_optin = 0;
+        cudaError_t e = cudaGetDevice(&dev);
         if (e != cudaSuccess) return e;
+        e = cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(paged_decode_merge<T, D, B>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, max_optin);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(paged_decode_main<T, D, B>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, max_optin);
+        if (e != cudaSuccess) return e;
+        if (smem > (size_t)max_optin) {
+            *ctas = 0;
+            return cudaSuccess;
+        }
         return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, paged_decode_main<T, D, B>,
                                                              C::THREADS, smem);
     }

@@ -92,6 +92,10 @@ const DecodeKernel* decode_kernel_bf16(int D, int B);
 cudaError_t launch_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,
                                      const int64_t* slots, int T, int H, int D, int B,
                                      int64_t num_blocks, int32_t* err, cudaStream_t stream);
+cudaError_t launch_swap_blocks(void* dst_k, void* dst_v, const void* src_k, const void* src_v,
+                               const int32_t* pairs, int P, int H, int D, int B,
+                               int64_t src_blocks, int64_t dst_blocks, int32_t* err,
+                               cudaStream_t stream);
 cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int P,
                                int H, int D, int B, int64_t num_blocks, int32_t* err,
                                cudaStream_t stream);

@@ -61,6 +61,7 @@ def lib():
                                                     i32, i64, i32, i32, P], i32),
             "pkv_reshape_and_cache": ([P, P, P, P, P, i32, i32, i32, i32, i64, i32, P], i32),
             "pkv_copy_blocks": ([P, P, P, i32, i32, i32, i32, i64, i32, P], i32),
+            "pkv_swap_blocks": ([P, P, P, P, P, i32, i32, i32, i32, i64, i64, i32, P], i32),
             "pkv_get_device_error": ([ctypes.POINTER(ctypes.c_int32), i32, P], i32),
             "pkv_last_error": ([], ctypes.c_char_p),
             "pkv_version": ([], ctypes.c_char_p),
@@ -79,6 +80,14 @@ def lib():
             "pkv_bm_export": ([P, P, i32, P, ctypes.c_int32, P], i32),
             "pkv_bm_refcount": ([P, ctypes.c_int32], ctypes.c_int32),
             "pkv_bm_num_free": ([P], i64),
+            "pkv_bm_add_cpu_pool": ([P, i64, u64], i32),
+            "pkv_bm_swap_out": ([P, P, i32, P, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)],
+                                i32),
+            "pkv_bm_swap_in": ([P, P, i32, P, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)],
+                               i32),
+            "pkv_bm_is_swapped": ([P, i64], ctypes.c_int32),
+            "pkv_bm_cpu_refcount": ([P, ctypes.c_int32], ctypes.c_int32),
+            "pkv_bm_num_free_cpu": ([P], i64),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -242,6 +251,38 @@ def copy_blocks(k_cache, v_cache, pairs, stream=None):
                                  _dtype_code(k_cache.dtype), _stream(stream)))
 
 
+def _reachable(t, name):
+    """A CUDA tensor or a pinned host tensor (the kernel dereferences it)."""
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if not (t.is_cuda or t.is_pinned()):
+        raise ValueError("%s must be a CUDA tensor or pinned host memory" % name)
+    return t.data_ptr()
+
+
+def swap_blocks(dst_k, dst_v, src_k, src_v, pairs, stream=None):
+    """Whole-block copies between two pools (GPU <-> pinned CPU, either way):
+    dst[pairs[p, 1]] = src[pairs[p, 0]] for K and V."""
+    torch = _torch()
+    snb, H, B, D = src_k.shape
+    dnb = dst_k.shape[0]
+    if tuple(dst_k.shape[1:]) != (H, B, D) or src_v.shape != src_k.shape or \
+            dst_v.shape != dst_k.shape:
+        raise ValueError("pool shape mismatch")
+    if not (src_k.dtype == src_v.dtype == dst_k.dtype == dst_v.dtype):
+        raise TypeError("the pools must share a dtype")
+    P = pairs.shape[0] if pairs.numel() else 0
+    if P == 0:
+        return
+    if pairs.dim() != 2 or pairs.shape[1] != 2 or pairs.dtype != torch.int32:
+        raise ValueError("pairs must be int32 [num_pairs, 2]")
+    _check("pkv_swap_blocks",
+           lib().pkv_swap_blocks(_reachable(dst_k, "dst_k"), _reachable(dst_v, "dst_v"),
+                                 _reachable(src_k, "src_k"), _reachable(src_v, "src_v"),
+                                 _reachable(pairs, "pairs"), P, H, D, B, snb, dnb,
+                                 _dtype_code(src_k.dtype), _stream(stream)))
+
+
 def get_device_error(clear=True, stream=None) -> int:
     """Device error bits (PKV_DEVERR_*) of the current device; syncs the stream."""
     bits = ctypes.c_int32(0)
@@ -337,3 +378,39 @@ class BlockManager:
 
     def num_free(self) -> int:
         return lib().pkv_bm_num_free(self._h)
+
+    # -- swapping ------------------------------------------------------------
+    def add_cpu_pool(self, num_cpu_blocks: int, seed: int) -> None:
+        _check("pkv_bm_add_cpu_pool", lib().pkv_bm_add_cpu_pool(self._h, int(num_cpu_blocks),
+                                                                int(seed) & ((1 << 64) - 1)))
+        self.num_cpu_blocks = num_cpu_blocks
+
+    def _swap(self, fn, seq_ids):
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        cap = sum(len(self.block_table(int(s))) for s in ids)
+        pairs = np.empty((max(cap, 1), 2), dtype=np.int32)
+        n = ctypes.c_int32(0)
+        _check(fn, getattr(lib(), fn)(self._h, ids.ctypes.data_as(ctypes.c_void_p), ids.shape[0],
+                                      pairs.ctypes.data_as(ctypes.c_void_p), cap,
+                                      ctypes.byref(n)))
+        return pairs[:n.value]
+
+    def swap_out(self, seq_ids) -> np.ndarray:
+        """Move a group of resident sequences to the CPU pool; (gpu, cpu) pairs."""
+        return self._swap("pkv_bm_swap_out", seq_ids)
+
+    def swap_in(self, seq_ids) -> np.ndarray:
+        """Move a group of swapped-out sequences back to the GPU pool; (cpu, gpu) pairs."""
+        return self._swap("pkv_bm_swap_in", seq_ids)
+
+    def is_swapped(self, seq_id: int) -> bool:
+        r = lib().pkv_bm_is_swapped(self._h, int(seq_id))
+        if r < 0:
+            raise PagedKVError("pkv_bm_is_swapped", PKV_ERR_INVALID, "unknown sequence")
+        return bool(r)
+
+    def cpu_refcount(self, block: int) -> int:
+        return lib().pkv_bm_cpu_refcount(self._h, int(block))
+
+    def num_free_cpu(self) -> int:
+        return lib().pkv_bm_num_free_cpu(self._h)

@@ -145,6 +145,95 @@ def test_manager_matches_model_on_random_churn(pkv, seed):
     same_state(bm, model, live)
 
 
+@pytest.mark.parametrize("seed", [3, 44])
+def test_manager_matches_model_with_swapping(pkv, seed):
+    from oracle.block_manager import InvalidRequest
+
+    def both(model_call, cpp_call):
+        """Run one operation on both sides; failures must match in kind."""
+        try:
+            ref = model_call()
+        except ModelOOM:
+            with pytest.raises(pkv.OutOfBlocks):
+                cpp_call()
+            return None
+        except InvalidRequest:
+            with pytest.raises(pkv.PagedKVError) as e:
+                cpp_call()
+            assert e.value.status == 1
+            return None
+        return ref, cpp_call()
+
+    rs = np.random.default_rng(seed)
+    nb, ncpu, B = 120, 60, 8
+    bm = pkv.BlockManager(nb, B, seed)
+    model = BlockManagerModel(nb, B, seed)
+    bm.add_cpu_pool(ncpu, seed + 1)
+    model.add_cpu_pool(ncpu, seed + 1)
+    live, nxt = [], 0
+    for step in range(1200):
+        op = int(rs.integers(0, 12))
+        if op < 2 or not live:
+            n = int(rs.integers(0, 50))
+            r = both(lambda: model.add_sequence(nxt, n), lambda: bm.add_sequence(nxt, n))
+            if r:
+                assert r[1].tolist() == r[0]
+                live.append(nxt)
+                nxt += 1
+        elif op < 3:
+            parent = live[int(rs.integers(len(live)))]
+            r = both(lambda: model.fork(parent, nxt), lambda: bm.fork(parent, nxt))
+            if r:
+                live.append(nxt)
+                nxt += 1
+        elif op < 4:
+            sid = live.pop(int(rs.integers(len(live))))
+            model.free_sequence(sid)
+            bm.free_sequence(sid)
+        elif op < 6:
+            k = int(rs.integers(1, min(4, len(live)) + 1))
+            group = [live[i] for i in rs.choice(len(live), k, replace=False)]
+            if model.swapped[group[0]]:
+                r = both(lambda: model.swap_in(group), lambda: bm.swap_in(group))
+            else:
+                r = both(lambda: model.swap_out(group), lambda: bm.swap_out(group))
+            if r:
+                assert r[1].tolist() == [list(p) for p in r[0]]
+        else:
+            sid = live[int(rs.integers(len(live)))]
+            r = both(lambda: model.append_slot(sid), lambda: bm.append_slot(sid))
+            if r:
+                assert r[1] == r[0]
+        if step % 40 == 0:
+            for s_ in live:
+                assert bm.block_table(s_) == model.block_table(s_)
+                assert bm.is_swapped(s_) == model.swapped[s_]
+            assert bm.num_free() == model.num_free()
+            assert bm.num_free_cpu() == len(model.cpu_free)
+            for b in range(ncpu):
+                assert bm.cpu_refcount(b) == model.cpu_ref[b]
+
+
+def test_swap_failures_match(pkv):
+    bm = pkv.BlockManager(32, 16, 5)
+    with pytest.raises(pkv.PagedKVError):
+        bm.swap_out([0])                       # no CPU pool yet
+    bm.add_cpu_pool(3, 6)
+    bm.add_sequence(0, 64)                     # 4 blocks
+    bm.add_sequence(1, 10)
+    bm.fork(1, 2)
+    with pytest.raises(pkv.OutOfBlocks):
+        bm.swap_out([0])
+    with pytest.raises(pkv.PagedKVError):
+        bm.swap_out([1])                       # block shared with 2
+    assert not bm.is_swapped(0) and bm.num_free_cpu() == 3
+    bm.swap_out([1, 2])
+    with pytest.raises(pkv.PagedKVError):
+        bm.append_slot(1)
+    with pytest.raises(pkv.PagedKVError):
+        bm.export([1], 4)
+
+
 def test_batched_append_matches_sequential_model(pkv):
     B = 16
     bm = pkv.BlockManager(400, B, 77)
@@ -184,3 +273,14 @@ def test_batched_append_is_all_or_nothing(pkv):
     with pytest.raises(pkv.PagedKVError):
         bm.append_slots([9])                 # unknown sequence
     assert bm.context_len(1) == 4
+
+
+def test_swap_refuses_pageable_host_memory(pkv):
+    """Pools the kernel could not dereference are refused before any launch."""
+    L = pkv.lib()
+    pool = np.zeros((4, 2, 16, 64), np.float16)            # ordinary (pageable) host memory
+    pairs = np.array([[0, 1]], np.int32)
+    p = pool.ctypes.data
+    st = L.pkv_swap_blocks(p, p, p, p, pairs.ctypes.data, 1, 2, 64, 16, 4, 4, 0, None)
+    assert st == 1 and "pinned" in pkv.pagedkv.last_error()
+    assert L.pkv_swap_blocks(p, p, p, p, pairs.ctypes.data, 0, 2, 64, 16, 4, 4, 0, None) == 0

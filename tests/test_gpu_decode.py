@@ -197,3 +197,18 @@ def test_tiny_workload_full_step(pkv):
         attn_check(out, expect, "tiny partition=%d" % part)
         # the 1-token sequence sees only its new token: out == v exactly
         assert torch.equal(out[0].cpu(), W.words_to_torch(vnew[0], "f16"))
+
+
+def test_alternating_batch_sizes(pkv):
+    """Batches of different sizes (so different shared-memory sizes) in any order."""
+    rs = np.random.default_rng(16)
+    cases = {}
+    for S in (3, 700, 40, 3, 700, 1500, 40):
+        if S not in cases:
+            ctx = list(rs.integers(0, 120, size=S))
+            cases[S] = (random_case(rs, S, 2, 128, 16, ctx, "f16"), None)
+        case, ref = cases[S]
+        if ref is None:
+            ref = run_oracle(case, 0.09)
+            cases[S] = (case, ref)
+        attn_check(run_gpu(pkv, case, 0.09), ref, "S=%d" % S)

@@ -183,3 +183,72 @@ def test_random_churn_keeps_invariants():
         except OutOfBlocks:
             pass
         check_invariants(bm)
+
+
+# ---- swapping (wywy.jp notes: "Swapping", all-or-nothing eviction) -----------------
+
+def groups_of(bm):
+    """Sharing pattern of the live tables: sequence -> tuple of block-class labels."""
+    label, out = {}, {}
+    for sid in sorted(bm.tables):
+        out[sid] = tuple(label.setdefault((bm.swapped[sid], b), len(label))
+                         for b in bm.tables[sid])
+    return out
+
+
+def test_swap_round_trip_keeps_sharing_and_counts():
+    bm = BlockManagerModel(64, 16, seed=8)
+    bm.add_cpu_pool(64, seed=9)
+    bm.add_sequence(0, 70)
+    for c in (1, 2):
+        bm.fork(0, c)
+    bm.append_slot(1)                     # 1 gets its own copy of the partial block
+    bm.add_sequence(5, 20)                # an unrelated resident sequence
+    before = groups_of(bm)
+    free_gpu = bm.num_free()
+    pairs = bm.swap_out([0, 1, 2])
+    distinct = {b for s in (0, 1, 2) for b in bm.tables[s]}
+    assert len(pairs) == len(distinct) == 6
+    assert all(bm.swapped[s] for s in (0, 1, 2)) and not bm.swapped[5]
+    assert bm.num_free() == free_gpu + 6
+    assert [bm.cpu_ref[b] for b in bm.tables[0]] == [3, 3, 3, 3, 2]
+    with pytest.raises(InvalidRequest):
+        bm.append_slot(0)                 # swapped-out sequences do not grow
+    with pytest.raises(InvalidRequest):
+        bm.fork(1, 9)
+    back = bm.swap_in([0, 1, 2])
+    assert [c for c, _ in back] == [n for _, n in pairs]
+    assert groups_of(bm) == before
+    assert [bm.ref[b] for b in bm.tables[0]] == [3, 3, 3, 3, 2]
+    assert bm.cpu_free and len(bm.cpu_free) == 64
+
+
+def test_swap_refuses_blocks_shared_outside_the_group():
+    bm = BlockManagerModel(32, 16, seed=10)
+    bm.add_cpu_pool(32, seed=11)
+    bm.add_sequence(0, 40)
+    bm.fork(0, 1)
+    snapshot = (list(bm.free), list(bm.ref), dict(bm.swapped))
+    with pytest.raises(InvalidRequest):
+        bm.swap_out([0])                  # 1 still holds 0's blocks
+    assert snapshot == (list(bm.free), list(bm.ref), dict(bm.swapped))
+    bm.swap_out([1, 0])
+
+
+def test_swap_is_all_or_nothing_on_oom():
+    bm = BlockManagerModel(32, 16, seed=12)
+    bm.add_cpu_pool(3, seed=13)
+    bm.add_sequence(0, 64)                # 4 blocks > 3 CPU blocks
+    with pytest.raises(OutOfBlocks):
+        bm.swap_out([0])
+    assert not bm.swapped[0] and len(bm.cpu_free) == 3 and bm.num_free() == 28
+
+
+def test_freeing_a_swapped_sequence_releases_cpu_blocks():
+    bm = BlockManagerModel(16, 8, seed=14)
+    bm.add_cpu_pool(16, seed=15)
+    bm.add_sequence(0, 20)
+    bm.swap_out([0])
+    assert len(bm.cpu_free) == 13
+    bm.free_sequence(0)
+    assert len(bm.cpu_free) == 16 and sum(bm.cpu_ref) == 0 and bm.num_free() == 16

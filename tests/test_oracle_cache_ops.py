@@ -82,3 +82,25 @@ def test_copy_blocks_rejects_bad_ids():
     kc = np.zeros((3, 1, 4, 8), np.uint16)
     with pytest.raises(ValueError):
         oracle.copy_blocks(kc, kc.copy(), np.array([[0, 3]]))
+
+
+def test_swap_blocks_between_two_pools():
+    rs = np.random.default_rng(32)
+    H, B, D = 2, 8, 16
+    gpu = rs.integers(0, 65536, size=(10, H, B, D), dtype=np.uint16)
+    gpv = rs.integers(0, 65536, size=(10, H, B, D), dtype=np.uint16)
+    cpu = np.zeros((6, H, B, D), np.uint16)
+    cpv = np.zeros_like(cpu)
+    pairs = np.array([[7, 2], [1, 5], [9, 0]], np.int32)
+    oracle.swap_blocks(cpu, cpv, gpu, gpv, pairs)
+    for s, d in pairs:
+        assert np.array_equal(cpu[d], gpu[s]) and np.array_equal(cpv[d], gpv[s])
+    untouched = [b for b in range(6) if b not in pairs[:, 1]]
+    assert not cpu[untouched].any() and not cpv[untouched].any()
+    back = np.zeros_like(gpu)
+    backv = np.zeros_like(gpv)
+    oracle.swap_blocks(back, backv, cpu, cpv, pairs[:, ::-1])
+    for s, _ in pairs:
+        assert np.array_equal(back[s], gpu[s]) and np.array_equal(backv[s], gpv[s])
+    with pytest.raises(ValueError):
+        oracle.swap_blocks(cpu, cpv, gpu, gpv, np.array([[10, 0]]))
