@@ -370,6 +370,8 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--op", choices=["step", "swap"], default="step",
+                    help="step: the decode layer-step (default); swap: block swap GPU<->CPU")
     ap.add_argument("--workload", default="opt13b", choices=sorted(W.SPECS))
     ap.add_argument("--partition", type=int, default=None,
                     help="split length in tokens (0 = balanced); default: the workload's")
@@ -396,6 +398,8 @@ def main():
 
     if args.impl == "reference":
         return reference_arm(args, world, rank, dist)
+    if args.op == "swap":
+        return bench_swap(args)
 
     if not torch.cuda.is_available():
         raise SystemExit("bench.py: no CUDA device")
@@ -596,6 +600,72 @@ def cpu_baseline(wl: Workload) -> dict:
             "cores": threads, "kind": "oracle",
             "sample": "all %d sequences x %d heads of layer 0, %d pass(es), %.1f s" % (
                 wl.S, wl.H, done, total)}
+
+
+def bench_swap(args):
+    """Block swap GPU pool <-> pinned CPU pool at the OPT-13B layer shape (40 heads
+    x 128, fp16) for block sizes 8..64: pkv_swap_blocks (one launch for every
+    block) against the copy engine (one cudaMemcpyAsync per block and pool, and
+    one bulk copy of the same bytes as its best case)."""
+    import torch
+    import paged_kv_cache_05_gb300 as pkv
+    from paged_kv_cache_05_gb300 import build
+    build.build()
+    dev = torch.device("cuda", 0)
+    H, D = 40, 128
+    total = 512 << 20                       # bytes of K+V moved per direction
+    rows = []
+    for B in ([args.block_size] if args.block_size else [8, 16, 32, 64]):
+        per_pool = H * B * D * 2
+        n = total // (2 * per_pool)
+        gk = W.device_normal((n, H, B, D), "f16", 11, dev)
+        gv = W.device_normal((n, H, B, D), "f16", 12, dev)
+        ck = torch.empty((n, H, B, D), dtype=torch.float16).pin_memory()
+        cv = torch.empty_like(ck).pin_memory()
+        perm = np.random.default_rng(B).permutation(n).astype(np.int32)
+        p_out = torch.from_numpy(np.stack([np.arange(n, dtype=np.int32), perm], 1)).to(dev)
+        p_in = torch.from_numpy(np.stack([perm, np.arange(n, dtype=np.int32)], 1)).to(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+        def timed(fn, reps):
+            for _ in range(2):
+                fn()
+            torch.cuda.synchronize()
+            a.record()
+            for _ in range(reps):
+                fn()
+            b.record()
+            torch.cuda.synchronize()
+            return a.elapsed_time(b) / reps * 1e-3
+
+        reps = max(3, args.steps // 100)
+        t_out = timed(lambda: pkv.swap_blocks(ck, cv, gk, gv, p_out), reps)
+        t_in = timed(lambda: pkv.swap_blocks(gk, gv, ck, cv, p_in), reps)
+        if pkv.get_device_error() != 0:
+            raise SystemExit("bench.py --op swap: device error bits")
+
+        def per_block_out():
+            for i in range(n):
+                ck[int(perm[i])].copy_(gk[i], non_blocking=True)
+                cv[int(perm[i])].copy_(gv[i], non_blocking=True)
+        t_ce_blocks = timed(per_block_out, 1)
+        flat_g = gk.view(-1)
+        flat_c = ck.view(-1)
+        t_ce_bulk = timed(lambda: (flat_c.copy_(flat_g, non_blocking=True),
+                                   cv.view(-1).copy_(gv.view(-1), non_blocking=True)), reps)
+        nbytes = 2 * n * per_pool
+        rows.append({"block_size": B, "blocks": int(n), "block_bytes_kv": 2 * per_pool,
+                     "swap_out_gbs": round(nbytes / t_out / 1e9, 1),
+                     "swap_in_gbs": round(nbytes / t_in / 1e9, 1),
+                     "copy_engine_per_block_gbs": round(nbytes / t_ce_blocks / 1e9, 1),
+                     "copy_engine_bulk_gbs": round(nbytes / t_ce_bulk / 1e9, 1)})
+        del gk, gv, ck, cv
+        torch.cuda.empty_cache()
+    print(json.dumps({"op": "swap_blocks", "metric": "block swap GB/s (K+V bytes moved)",
+                      "unit": "GB/s", "value": rows[-1]["swap_out_gbs"],
+                      "config": {"heads": H, "head_dim": D, "dtype": "f16",
+                                 "bytes_per_direction": total},
+                      "results": rows}), flush=True)
 
 
 def reference_arm(args, world, rank, dist):
