@@ -370,8 +370,9 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--op", choices=["step", "swap"], default="step",
-                    help="step: the decode layer-step (default); swap: block swap GPU<->CPU")
+    ap.add_argument("--op", choices=["step", "swap", "sharing"], default="step",
+                    help="step: the decode layer-step (default); swap: block swap GPU<->CPU; "
+                         "sharing: memory saved by block sharing (host only)")
     ap.add_argument("--workload", default="opt13b", choices=sorted(W.SPECS))
     ap.add_argument("--partition", type=int, default=None,
                     help="split length in tokens (0 = balanced); default: the workload's")
@@ -396,6 +397,13 @@ def main():
             torch.cuda.set_device(local)
         dist.init_process_group(backend)
 
+    if args.op == "sharing":
+        from paged_kv_cache_05_gb300 import build
+        build.build()
+        print(json.dumps({"op": "sharing", "metric": "KV blocks saved by sharing (fraction)",
+                          "block_size": 16, "data": "synthetic (seeded)",
+                          "results": sharing_savings()}), flush=True)
+        return
     if args.impl == "reference":
         return reference_arm(args, world, rank, dist)
     if args.op == "swap":
@@ -666,6 +674,74 @@ def bench_swap(args):
                       "config": {"heads": H, "head_dim": D, "dtype": "f16",
                                  "bytes_per_direction": total},
                       "results": rows}), flush=True)
+
+
+def sharing_savings(seed: int = 2024, block_size: int = 16):
+    """Memory the block manager saves by sharing, on synthetic decoding runs
+    (host only).  Parallel sampling: k samples of one prompt share the prompt's
+    blocks, the partial last one copied on write.  Beam-search-like churn:
+    every step each of W beams appends a token, then W survivors are drawn at
+    random (no model decides) and forked from their parents while the old
+    beams are freed.  Saving = 1 - blocks in use / blocks needed if every
+    sequence held its own copy, averaged over the run's steps."""
+    import paged_kv_cache_05_gb300 as pkv
+    rng = np.random.default_rng(seed)
+    B = block_size
+    out = {"parallel_sampling": {}, "beam_search": {}}
+    for k in (2, 4, 6):
+        bm = pkv.BlockManager(200_000, B, seed)
+        savings = []
+        for g in range(16):
+            P = int(rng.integers(128, 1025))
+            O = rng.integers(1, 513, size=k)
+            base = g * 100
+            bm.add_sequence(base, P)
+            for c in range(1, k):
+                bm.fork(base, base + c)
+            for t in range(int(O.max())):
+                act = [base + c for c in range(k) if t < O[c]]
+                bm.append_slots(act)
+            used_before = 200_000 - bm.num_free()
+            unshared = sum(-(-(P + int(o)) // B) for o in O)
+            shared = sum(len(bm.block_table(base + c)) for c in range(k))
+            distinct = len({b for c in range(k) for b in bm.block_table(base + c)})
+            savings.append(1 - distinct / unshared)
+            assert shared == unshared and used_before > 0
+            for c in range(k):
+                bm.free_sequence(base + c)
+        out["parallel_sampling"][k] = round(float(np.mean(savings)), 4)
+    for W_ in (4, 8):
+        bm = pkv.BlockManager(200_000, B, seed + W_)
+        savings = []
+        for g in range(8):
+            P = int(rng.integers(128, 1025))
+            nxt = g * 100_000
+            bm.add_sequence(nxt, P)
+            beams = [nxt]
+            nxt += 1
+            for c in range(1, W_):
+                bm.fork(beams[0], nxt)
+                beams.append(nxt)
+                nxt += 1
+            for t in range(256):
+                bm.append_slots(beams)
+                parents = rng.integers(0, W_, size=W_)
+                new = []
+                for p_ in parents:
+                    bm.fork(beams[int(p_)], nxt)
+                    new.append(nxt)
+                    nxt += 1
+                for b_ in beams:
+                    bm.free_sequence(b_)
+                beams = new
+                distinct = len({b for s_ in beams for b in bm.block_table(s_)})
+                unshared = W_ * -(-(P + t + 1) // B)
+                savings.append(1 - distinct / unshared)
+            for b_ in beams:
+                bm.free_sequence(b_)
+            assert bm.num_free() == 200_000
+        out["beam_search"][W_] = round(float(np.mean(savings)), 4)
+    return out
 
 
 def reference_arm(args, world, rank, dist):
