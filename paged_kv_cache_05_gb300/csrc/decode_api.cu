@@ -10,6 +10,9 @@ constexpr int kMaxDevices = 64;
 // Lower bound of a balanced chunk, in steps: keeps tiny batches from being cut
 // into one-step pieces that would all need the merge pass.
 constexpr int kMinChunkSteps = 8;
+#ifndef PKV_DECODE_WAVES
+#define PKV_DECODE_WAVES 1
+#endif
 
 struct OccEntry {
     const pkv::DecodeKernel* k;
@@ -132,7 +135,7 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* k_ca
     if (per_sm < 1)
         return pkv::fail(PKV_ERR_INVALID, "%s: %d sequences need %zu bytes of shared memory", fn,
                          num_seqs, smem);
-    int grid = pkv::sm_count(dev) * per_sm;
+    int grid = pkv::sm_count(dev) * per_sm * PKV_DECODE_WAVES;
     if (grid < 1) return pkv::fail(PKV_ERR_CUDA, "%s: no multiprocessors", fn);
     if (grid > PKV_MAX_GRID) grid = PKV_MAX_GRID;
     {
