@@ -74,6 +74,9 @@ def _load():
         lib.orc_copy_blocks.restype = i32
         lib.orc_swap_blocks.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i64, i64]
         lib.orc_swap_blocks.restype = i32
+        lib.orc_paged_attention_prefill.argtypes = [P, P, P, P, P, P, P, f64, i32, i32, i32, i32,
+                                                    i32, i64, i32]
+        lib.orc_paged_attention_prefill.restype = i32
         _lib = lib
         return lib
 
@@ -235,3 +238,31 @@ def swap_blocks(dst_k, dst_v, src_k, src_v, pairs) -> None:
                              H, D, B, snb, dnb)
     if rc != 0:
         raise ValueError("oracle: block id out of a pool")
+
+
+def paged_attention_prefill(q, k_cache, v_cache, block_tables, context_lens, query_start, scale,
+                            dtype=F16) -> np.ndarray:
+    """fp64 causal attention of each sequence's new tokens over its paged cache.
+
+    q: [total_query_tokens][H][D]; query_start: int32 [S+1] (row offsets into q);
+    the new tokens of sequence s occupy positions ctx-qlen .. ctx-1 and are
+    already in the cache.  Returns [total_query_tokens][H][D] fp64.
+    """
+    lib = _load()
+    q = _words(q)
+    kc, vc = _words(k_cache), _words(v_cache)
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    qs = np.ascontiguousarray(query_start, dtype=np.int32)
+    T, H, D = q.shape
+    nb, H2, B, D2 = kc.shape
+    S = cl.shape[0]
+    if (H2, D2) != (H, D) or qs.shape != (S + 1,) or qs[-1] != T or bt.shape[0] != S:
+        raise ValueError("shape mismatch")
+    out = np.zeros((T, H, D), dtype=np.float64)
+    rc = lib.orc_paged_attention_prefill(_ptr(out), _ptr(q), _ptr(kc), _ptr(vc), _ptr(bt),
+                                         _ptr(cl), _ptr(qs), float(scale), S, H, D, B,
+                                         bt.shape[1], nb, int(dtype))
+    if rc != 0:
+        raise ValueError("oracle: invalid table, context or query lengths (rc=%d)" % rc)
+    return out

@@ -271,3 +271,57 @@ int orc_swap_blocks(uint16_t* dst_k, uint16_t* dst_v, const uint16_t* src_k,
     }
     return 0;
 }
+
+/*
+ * Prompt phase with the paged cache (wywy.jp notes, "prompt phase": every
+ * prompt token is known, their K/V are produced together and attention runs
+ * as matrix-matrix work).  Sequence s has qlen = query_start[s+1] -
+ * query_start[s] new tokens whose K/V are already in the cache at positions
+ * ctx - qlen .. ctx - 1; query token i (row query_start[s] + i of q and out)
+ * sits at position p = ctx - qlen + i and attends positions 0 .. p (causal).
+ * Each row is the decode definition with context length p + 1.
+ */
+int orc_paged_attention_prefill(double* out, const uint16_t* q, const uint16_t* k_cache,
+                                const uint16_t* v_cache, const int32_t* block_tables,
+                                const int32_t* context_lens, const int32_t* query_start,
+                                double scale, int S, int H, int D, int B, int max_blocks,
+                                int64_t num_blocks, int dtype) {
+    for (int s = 0; s < S; ++s) {
+        const int32_t* row = block_tables + (int64_t)s * max_blocks;
+        int32_t n = context_lens[s];
+        int32_t q0 = query_start[s], qlen = query_start[s + 1] - query_start[s];
+        if (qlen < 0 || qlen > n) return -1;
+        if (check_table_row(row, n, B, max_blocks, num_blocks)) return -1;
+        for (int i = 0; i < qlen; ++i) {
+            int64_t p = (int64_t)n - qlen + i;
+            for (int h = 0; h < H; ++h) {
+                double* o = out + ((int64_t)(q0 + i) * H + h) * D;
+                const uint16_t* qrow = q + ((int64_t)(q0 + i) * H + h) * D;
+                double* z = (double*)malloc(sizeof(double) * (size_t)(p + 1));
+                if (!z) return -2;
+                double zmax = -INFINITY;
+                for (int64_t t = 0; t <= p; ++t) {
+                    double acc = 0.0;
+                    for (int d = 0; d < D; ++d)
+                        acc += widen(qrow[d], dtype) *
+                               widen(k_cache[kv_word_index(row, t, h, d, H, B, D)], dtype);
+                    z[t] = scale * acc;
+                    if (z[t] > zmax) zmax = z[t];
+                }
+                double denom = 0.0;
+                for (int64_t t = 0; t <= p; ++t) {
+                    z[t] = exp(z[t] - zmax);
+                    denom += z[t];
+                }
+                for (int d = 0; d < D; ++d) {
+                    double acc = 0.0;
+                    for (int64_t t = 0; t <= p; ++t)
+                        acc += z[t] * widen(v_cache[kv_word_index(row, t, h, d, H, B, D)], dtype);
+                    o[d] = acc / denom;
+                }
+                free(z);
+            }
+        }
+    }
+    return 0;
+}
