@@ -165,6 +165,28 @@ pkv_status pkv_paged_attention_decode_noalloc(void* out, const void* q, const vo
                                               int64_t num_blocks, pkv_dtype dtype,
                                               int partition_size, cudaStream_t stream);
 
+/*
+ * Prompt phase (wywy.jp notes, "prompt phase": every prompt token is known,
+ * their K/V are produced together and attention runs as matrix-matrix work).
+ * Sequence s has qlen = query_start[s+1] - query_start[s] new tokens whose
+ * K/V are already in the cache (pkv_reshape_and_cache) at positions
+ * ctx - qlen .. ctx - 1, ctx = context_lens[s].  Query row query_start[s] + i
+ * (position p = ctx - qlen + i) attends positions 0 .. p (causal):
+ *   out[row][h] = sum_{t <= p} softmax_t(scale * q[row][h] . K_s[t][h]) V_s[t][h]
+ * A whole prompt is qlen == ctx; a prompt continued after a cached prefix
+ * (shared prefix, chunked prefill) is qlen < ctx; qlen == 1 is one decode row.
+ * q, out: [total query rows][num_heads][head_dim]; query_start: int32
+ * [num_seqs + 1], device.  max_query_len (host) bounds every qlen; a larger
+ * one sets PKV_DEVERR_BAD_CONTEXT and its extra rows are not written.
+ * Tensor cores (mma.sync m16n8k16), fp32 accumulation, one launch, no workspace.
+ */
+pkv_status pkv_paged_attention_prefill(void* out, const void* q, const void* k_cache,
+                                       const void* v_cache, const int32_t* block_tables,
+                                       const int32_t* context_lens, const int32_t* query_start,
+                                       float scale, int num_seqs, int num_heads, int head_dim,
+                                       int block_size, int max_blocks_per_seq, int64_t num_blocks,
+                                       int max_query_len, pkv_dtype dtype, cudaStream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Cache maintenance                                                         */
 /* ------------------------------------------------------------------------ */

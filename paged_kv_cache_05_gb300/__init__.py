@@ -6,8 +6,10 @@ seeded synthetic inputs.  Build with ``python -m paged_kv_cache_05_gb300.build``
 """
 from .pagedkv import (BlockManager, OutOfBlocks, PagedKVError, alloc_workspace, copy_blocks,
                       decode_workspace_size, get_device_error, lib, paged_attention_decode,
+                      paged_attention_prefill,
                       reshape_and_cache, swap_blocks, version)
 
 __all__ = ["BlockManager", "OutOfBlocks", "PagedKVError", "alloc_workspace", "copy_blocks",
            "decode_workspace_size", "get_device_error", "lib", "paged_attention_decode",
+           "paged_attention_prefill",
            "reshape_and_cache", "swap_blocks", "version"]
