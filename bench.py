@@ -370,7 +370,7 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--op", choices=["step", "swap", "sharing"], default="step",
+    ap.add_argument("--op", choices=["step", "swap", "sharing", "prefill"], default="step",
                     help="step: the decode layer-step (default); swap: block swap GPU<->CPU; "
                          "sharing: memory saved by block sharing (host only)")
     ap.add_argument("--workload", default="opt13b", choices=sorted(W.SPECS))
@@ -408,6 +408,8 @@ def main():
         return reference_arm(args, world, rank, dist)
     if args.op == "swap":
         return bench_swap(args)
+    if args.op == "prefill":
+        return bench_prefill(args)
 
     if not torch.cuda.is_available():
         raise SystemExit("bench.py: no CUDA device")
@@ -674,6 +676,85 @@ def bench_swap(args):
                       "config": {"heads": H, "head_dim": D, "dtype": "f16",
                                  "bytes_per_direction": total},
                       "results": rows}), flush=True)
+
+
+def bench_prefill(args):
+    """The prompt phase at the OPT-13B shape: every prompt's K/V written into
+    the pool (reshape_and_cache), then causal paged attention of all prompt
+    tokens (tensor cores).  FLOPs = sum over query rows of 4 * D * H * (p + 1)
+    (Q K^T and P V, causal); peak = the measured dense bf16 tensor rate
+    (fp16 runs at the same nominal rate)."""
+    import torch
+    import paged_kv_cache_05_gb300 as pkv
+    from paged_kv_cache_05_gb300 import build
+    build.build()
+    dev = torch.device("cuda", 0)
+    spec = W.SPECS["prefill"]
+    ctx = W.context_lens(spec)
+    S, H, D, B = spec.num_seqs, spec.num_heads, spec.head_dim, spec.block_size
+    nb = W.pool_blocks(spec, ctx)
+    bm = pkv.BlockManager(nb, B, spec.seed)
+    slots = np.concatenate([bm.add_sequence(s_, int(ctx[s_])) for s_ in range(S)])
+    maxb = max(-(-int(c) // B) for c in ctx)
+    tables, _ = bm.export(list(range(S)), maxb)
+    T = int(ctx.sum())
+    kc = torch.zeros((nb, H, B, D), dtype=torch.float16, device=dev)
+    vc = torch.zeros_like(kc)
+    k = W.device_normal((T, H, D), "f16", spec.seed + 1, dev)
+    v = W.device_normal((T, H, D), "f16", spec.seed + 2, dev)
+    q = W.device_normal((T, H, D), "f16", spec.seed + 3, dev)
+    out = torch.empty_like(q)
+    qs = torch.from_numpy(np.concatenate([[0], np.cumsum(ctx)]).astype(np.int32)).to(dev)
+    bt = torch.from_numpy(tables).to(dev)
+    cl = torch.from_numpy(ctx).to(dev)
+    sl = torch.from_numpy(slots).to(dev)
+    maxq = int(ctx.max())
+
+    def step():
+        pkv.reshape_and_cache(k, v, kc, vc, sl)
+        pkv.paged_attention_prefill(out, q, kc, vc, bt, cl, qs, spec.scale, maxq)
+
+    def attn():
+        pkv.paged_attention_prefill(out, q, kc, vc, bt, cl, qs, spec.scale, maxq)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    K = max(10, args.steps // 20)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(K):
+        step()
+    b.record()
+    torch.cuda.synchronize()
+    t_step = a.elapsed_time(b) / K * 1e-3
+    a.record()
+    for _ in range(K):
+        attn()
+    b.record()
+    torch.cuda.synchronize()
+    t_attn = a.elapsed_time(b) / K * 1e-3
+    if pkv.get_device_error() != 0:
+        raise SystemExit("bench.py --op prefill: device error bits")
+    flops = float(sum(4.0 * D * H * (c * (c + 1) / 2.0) for c in ctx))
+    try:
+        peak = float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["bf16_tflops"])
+        src = "measured (MEASURED_PEAKS.json bf16_tflops, cuBLAS burst)"
+    except Exception:
+        peak, src = 1900.0, "fallback"
+    tf = flops / t_attn / 1e12
+    print(json.dumps({
+        "op": "prefill", "metric": "prompt-phase paged attention TFLOP/s", "unit": "TFLOP/s",
+        "value": round(tf, 1), "us_per_call": round(t_attn * 1e6, 1),
+        "us_per_step_with_cache_write": round(t_step * 1e6, 1),
+        "tokens_per_s": round(T / t_step, 1), "dtype": "f16 in, f32 accumulate",
+        "config": {"workload": "prefill: %d prompts, lengths %d..%d (sum %d), 40 heads x 128, "
+                               "B=16, fp16" % (S, int(ctx.min()), int(ctx.max()), T),
+                   "flops_per_call": flops},
+        "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(tf / peak, 4), "peak_source": src,
+                     "note": "mma.sync (the legacy tensor path), not tcgen05"},
+    }), flush=True)
 
 
 def sharing_savings(seed: int = 2024, block_size: int = 16):

@@ -25,6 +25,8 @@ and uniform draws because those traces are not available):
   long           seed 1005: 8 sequences, lengths uniform [8192, 32768], 32
                  heads, head_dim 128, fp16, B 16, an 80 GB (K+V) pool, split
                  length 512 tokens.
+  prefill        seed 1006: 16 whole prompts, lengths uniform [512, 2048], 40
+                 heads, head_dim 128, fp16, B 16 (the prompt phase).
 
 Values are N(0, 1) rounded to the storage type.  Host arrays use numpy's
 PCG64 (platform independent); device tensors use torch's CUDA generator.
@@ -74,6 +76,8 @@ SPECS = {
                                      suffix=(1, 512))),
     "long": Spec("long", 1005, 8, 32, 128, 16, "f16", partition_size=512,
                  extra=dict(lo=8192, hi=32768, pool_bytes=80 * 10**9)),
+    "prefill": Spec("prefill", 1006, 16, 40, 128, 16, "f16",
+                    extra=dict(lo=512, hi=2048)),
 }
 
 
@@ -90,7 +94,7 @@ def context_lens(spec: Spec) -> np.ndarray:
     if spec.name == "opt13b":
         x = r.lognormal(mean=math.log(e["median"]), sigma=e["sigma"], size=spec.num_seqs)
         return np.clip(np.rint(x), e["lo"], e["hi"]).astype(np.int32)
-    if spec.name in ("short", "long"):
+    if spec.name in ("short", "long", "prefill"):
         return r.integers(e["lo"], e["hi"], size=spec.num_seqs, endpoint=True).astype(np.int32)
     if spec.name == "shared_prefix":
         p, s = prompt_and_suffix_lens(spec)
