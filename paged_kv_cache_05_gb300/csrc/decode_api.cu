@@ -1,6 +1,9 @@
 // C ABI of the decode attention: argument checks, workspace sizing, grid choice.
+#include <atomic>
+#include <chrono>
 #include <cmath>
 #include <mutex>
+#include <random>
 
 #include "pkv_internal.h"
 
@@ -23,8 +26,21 @@ struct OccEntry {
 std::mutex g_mu;
 OccEntry g_occ[kMaxDevices][8] = {};
 
-// CTAs per SM for kernel k with `smem` bytes, cached per device (it also sets
-// the kernel's dynamic shared memory limit on first use on a device).
+// A 40-bit tag per call.  The call's first CTA stamps the workspace's claim
+// word with it, and a claimant starts claiming only once it sees the tag, so
+// a word left by an earlier call, or never written, is not taken for this
+// call's.  The sequence starts at a random point so that words left by
+// another process do not match either.
+uint64_t next_epoch() {
+    static std::atomic<uint64_t> counter{[] {
+        std::random_device rd;
+        const uint64_t t = (uint64_t)std::chrono::steady_clock::now().time_since_epoch().count();
+        return ((uint64_t)rd() << 20) ^ t;
+    }()};
+    return (counter.fetch_add(1) + 1) & ((1ull << 40) - 1);
+}
+
+// CTAs per SM for kernel k with `smem` bytes, cached per device.
 cudaError_t ctas_per_sm(const pkv::DecodeKernel* k, int dev, size_t smem, int* out) {
     std::lock_guard<std::mutex> lk(g_mu);
     OccEntry* row = g_occ[dev];
@@ -66,7 +82,7 @@ pkv_status check_shape(int S, int H, int D, int B, int max_blocks, int partition
 }
 
 int64_t max_chunks(int S, int H, int D, int B, int max_blocks, int partition_size) {
-    if (partition_size == 0) return PKV_MAX_GRID;
+    if (partition_size == 0) return (int64_t)PKV_MAX_GRID * (1 + PKV_DECODE_DYN_PER_CTA);
     const int64_t L = partition_size / pkv::step_tokens(D);
     const int64_t steps = (int64_t)S * H * pkv::max_steps_per_seq(D, B, max_blocks);
     return (steps + L - 1) / L;
@@ -165,6 +181,7 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* k_ca
     a.L_steps = partition_size > 0 ? partition_size / pkv::step_tokens(head_dim) : 0;
     a.min_chunk_steps = kMinChunkSteps;
     a.main_grid = grid;
+    a.epoch = next_epoch();
     a.ws = static_cast<char*>(workspace);
     a.ws_l = wl;
     a.err = err;

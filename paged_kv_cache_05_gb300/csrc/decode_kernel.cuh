@@ -52,6 +52,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "pkv_internal.h"
 
 namespace pkv {
@@ -207,6 +209,7 @@ constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
 #define PKV_DECODE_MIN_CTAS 1       // launch-bounds hint: resident CTAs per SM
 #endif
 
+
 template <int D, int B>
 struct Cfg {
     static constexpr int NW = PKV_DECODE_WARPS;         // consumer warps
@@ -236,9 +239,18 @@ struct Cfg {
     static constexpr size_t MISC_OFF = MERGE_OFF + 4 * (size_t)(2 * NW * MROW);
     // misc: the abort flag (16 B), then one scan partial per warp
     static constexpr size_t MISC_BYTES = (16 + 4 * (NW + 1) + 15) / 16 * 16;
-    static constexpr size_t CTX_OFF = MISC_OFF + MISC_BYTES;
+    // claimed-chunk queue, producer -> consumers: QN entries, each a chunk id,
+    // an mbarrier and the query slice of the chunk's first row.  QN > 2 NSTAGE
+    // + 1 so an entry is never rewritten before every consumer warp read it.
+    static constexpr int QN = 16;
+    static constexpr size_t QBAR_OFF = MISC_OFF + MISC_BYTES;
+    static constexpr size_t QID_OFF = QBAR_OFF + 8 * QN;
+    static constexpr size_t QBUF_OFF = QID_OFF + 4 * QN;
+    static constexpr size_t CTX_OFF = QBUF_OFF + (size_t)QN * D * 2;
     static_assert(NL >= 1 && NL <= LPT, "step layout");
     static_assert(NSTAGE >= NW && NSTAGE % NW == 0, "ring depth: a multiple of the warps");
+    static_assert(QN > 2 * NSTAGE + 1, "claim queue depth");
+    static_assert(QBAR_OFF % 8 == 0 && QBUF_OFF % 16 == 0, "claim queue alignment");
     static_assert(TPL * NL == SUB, "tokens per step");
     static_assert(B % SUB == 0 || SUB % B == 0, "steps and blocks nest");
     static_assert(BPS <= 32 && 32 % BPS == 0, "a step's blocks share one table window");
@@ -345,6 +357,91 @@ __device__ void scan_steps(const int* ctx, int* base, int S, int* scratch) {
     __syncthreads();
 }
 
+// ------------------------------------------------------------ the split
+// Chunks of the step space [0, total).  Fixed split length: chunks of Ls
+// steps, a contiguous run of them per CTA.  Balanced: one static chunk of Ls
+// steps per CTA over [0, X), then Kd dynamic chunks of Ld steps over
+// [X, total) claimed at run time.  Chunk indices grow along the step space
+// (static c < G, dynamic G + k), so a piece of row (s, h) in chunk k owns
+// partial slot s * H + h + k and the slots of one row are contiguous.  The
+// main and the merge kernels build the same split.
+struct Split {
+    int64_t total, X, Ls, Ld, Kd;
+    int G;
+    bool fixed;
+    __device__ __forceinline__ int64_t chunk(int64_t x) const {
+        return x < X ? x / Ls : G + (x - X) / Ld;
+    }
+    __device__ __forceinline__ int64_t chunk_end(int64_t x) const {
+        if (x < X) {
+            const int64_t e = (x / Ls + 1) * Ls;
+            return e < X ? e : X;
+        }
+        const int64_t e = X + ((x - X) / Ld + 1) * Ld;
+        return e < total ? e : total;
+    }
+    __device__ __forceinline__ int64_t last_chunk() const {
+        if (total == 0) return -1;
+        return chunk(total - 1);
+    }
+};
+
+__device__ __forceinline__ Split make_split(int64_t total, int G, int64_t L_steps,
+                                            int min_chunk) {
+    Split sp;
+    sp.total = total;
+    sp.G = G;
+    if (L_steps > 0) {
+        sp.fixed = true;
+        sp.Ls = L_steps;
+        sp.X = total;
+        sp.Ld = 1;
+        sp.Kd = 0;
+        return sp;
+    }
+    sp.fixed = false;
+    int64_t Ls = (total * PKV_DECODE_STATIC_EIGHTHS / 8) / G;
+    if (PKV_DECODE_DYN_PER_CTA == 0) Ls = (total + G - 1) / G;
+    if (Ls < min_chunk) Ls = min_chunk;
+    sp.Ls = Ls;
+    sp.X = (int64_t)G * Ls < total ? (int64_t)G * Ls : total;
+    const int64_t rem = total - sp.X;
+    if (rem > 0) {
+        int64_t kd = (int64_t)PKV_DECODE_DYN_PER_CTA * G;
+        if (kd > rem) kd = rem;
+        if (kd < 1) kd = 1;
+        sp.Ld = (rem + kd - 1) / kd;
+        sp.Kd = (rem + sp.Ld - 1) / sp.Ld;
+    } else {
+        sp.Ld = 1;
+        sp.Kd = 0;
+    }
+    return sp;
+}
+
+// Claim the next dynamic chunk.  The claim word holds (epoch << 24 | count);
+// the first CTA stamps it with this call's epoch (count 0) in its prologue,
+// and every claim is one atomicAdd.  A claimant waits (bounded)
+// until the word carries this call's epoch, so a word left by an earlier call
+// or never written is not counted.  Returns the claimed index, or -1 if the
+// stamp never came.
+__device__ __forceinline__ int64_t claim_chunk(unsigned long long* word, uint64_t epoch,
+                                               bool& stamped) {
+    if (!stamped) {
+        const uint64_t t0 = global_ns();
+        for (uint32_t it = 0;; ++it) {
+            const unsigned long long w = *reinterpret_cast<volatile unsigned long long*>(word);
+            if ((w >> 24) == epoch) break;
+            if (it >= kWaitLimitIters || global_ns() - t0 > kWaitLimitNs) return -1;
+            __nanosleep(64);
+        }
+        stamped = true;
+    }
+    const unsigned long long old = atomicAdd(word, 1ull);
+    if ((old >> 24) != epoch) return -1;
+    return (int64_t)(old & 0xffffffull);
+}
+
 // ------------------------------------------------------------ the main kernel
 template <typename T, int D, int B>
 __global__ void __launch_bounds__(Cfg<D, B>::THREADS, PKV_DECODE_MIN_CTAS)
@@ -374,49 +471,66 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, PKV_DECODE_MIN_CTAS)
         }
         s_ctx[s] = c;
     }
+    uint64_t* qfull = reinterpret_cast<uint64_t*>(smem + C::QBAR_OFF);
+    int* qid = reinterpret_cast<int*>(smem + C::QID_OFF);
+    unsigned char* qbuf = smem + C::QBUF_OFF;
     if (tid == 0) {
         for (int i = 0; i < C::NSTAGE; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], 1);
         }
+        for (int i = 0; i < C::QN; ++i) mbar_init(&qfull[i], 1);
         fence_mbar_init();
         *abort_flag = 0;
     }
     __syncthreads();
     scan_steps<C::SUB>(s_ctx, s_base, S, scratch);
 
-    // 2. this CTA's range of the step space
-    const int64_t total = (int64_t)H * s_base[S];
-    int64_t L = a.L_steps;
-    if (L <= 0) {
-        L = (total + gridDim.x - 1) / gridDim.x;
-        if (L < a.min_chunk_steps) L = a.min_chunk_steps;
-    }
-    const int64_t K = (total + L - 1) / L;
-    const bool ws_ok = (int64_t)S * H + K <= a.ws_l.cap;
+    // 2. the split of the step space, and this CTA's static range
+    const Split sp = make_split((int64_t)H * s_base[S], (int)gridDim.x, a.L_steps,
+                                a.min_chunk_steps);
+    const int64_t total = sp.total;
+    const bool ws_ok = (int64_t)S * H + sp.last_chunk() + 1 <= a.ws_l.cap;
     if (blockIdx.x == 0) {
         int64_t* hdr = reinterpret_cast<int64_t*>(a.ws);
         int* wbase = reinterpret_cast<int*>(a.ws + a.ws_l.base_off);
         for (int i = tid; i <= S; i += C::THREADS) wbase[i] = s_base[i];
         if (tid == 0) {
-            hdr[0] = ws_ok ? L : 0;
+            hdr[0] = ws_ok ? sp.Ls : 0;
             hdr[1] = total;
             if (!ws_ok) atomicOr(a.err, PKV_DEVERR_WORKSPACE);
+#if PKV_DECODE_DYN_PER_CTA != 0
+            // stamp the claim word (header word 2) with this call's epoch,
+            // count 0.  The previous call on this stream has finished (the
+            // dependency wait above), so no claim of its can land after this.
+            if (ws_ok && !sp.fixed && sp.Kd > 0) {
+                *reinterpret_cast<volatile unsigned long long*>(hdr + 2) =
+                    (unsigned long long)a.epoch << 24;
+                __threadfence();
+            }
+#endif
         }
     }
     grid_launch_dependents();
     if (!ws_ok || total == 0) return;
-    const int64_t kb = (int64_t)blockIdx.x * K / gridDim.x;
-    const int64_t ke = (int64_t)(blockIdx.x + 1) * K / gridDim.x;
-    const int64_t xb = kb * L;
-    const int64_t xe = ke * L < total ? ke * L : total;
-    if (xb >= xe) return;
-
+    int64_t xb, xe;
+    if (sp.fixed) {
+        const int64_t K = (total + sp.Ls - 1) / sp.Ls;
+        const int64_t kb = (int64_t)blockIdx.x * K / gridDim.x;
+        const int64_t ke = (int64_t)(blockIdx.x + 1) * K / gridDim.x;
+        xb = kb * sp.Ls;
+        xe = ke * sp.Ls < total ? ke * sp.Ls : total;
+        if (xb >= xe) return;
+    } else {
+        xb = (int64_t)blockIdx.x * sp.Ls;
+        xe = xb + sp.Ls < sp.X ? xb + sp.Ls : sp.X;
+        if (xb > xe) xb = xe;                    // no static share: claimed chunks only
+        if (xb >= xe && sp.Kd == 0) return;
+    }
     if (warp == C::NW) {
         // ================================================= producer warp
         const char* kpool = static_cast<const char*>(a.k_cache);
         const char* vpool = static_cast<const char*>(a.v_cache);
-        Pos p = locate(xb, s_base, S, H);
         int stage = 0;
         uint32_t phase = 0;
         int issued = 0;
@@ -426,101 +540,150 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, PKV_DECODE_MIN_CTAS)
         int tc_s = -1, tc_win = 0, tc_val = 0, tn_val = 0, ts_s = -1, ts_val = 0;
         bool tn_ok = false;
         bool stop = false;
-        for (int64_t x = xb; x < xe && !stop;) {
-            const int ns = s_base[p.s + 1] - s_base[p.s];
-            const int64_t left = xe - x;
-            const int run = (int64_t)(ns - p.j) < left ? ns - p.j : (int)left;
-            const int nblk = (s_ctx[p.s] + B - 1) / B;
-            const int32_t* row = a.block_tables + (int64_t)p.s * a.max_blocks;
-            for (int i = 0; i < run; ++i) {
-                const int j = p.j + i;
-                // first logical block of the step, and the step's token offset in it
-                const int jb = C::BPS > 1 ? j * C::BPS : j / C::SPB;
-                const int sub = C::BPS > 1 ? 0 : j - jb * C::SPB;
-                const int win = jb & ~31;
-                if (p.s != tc_s || win != tc_win) {
-                    if (p.s == tc_s && win == tc_win + 32 && tn_ok) {
-                        tc_val = tn_val;
-                    } else if (p.s == ts_s && win == 0) {
-                        tc_val = ts_val;
-                    } else {
-                        tc_val = (win + lane < nblk) ? __ldg(row + win + lane) : 0;
-                    }
-                    if (p.s != tc_s) {
-                        int s2 = p.s + 1;
-                        while (s2 < S && s_base[s2 + 1] == s_base[s2]) ++s2;
-                        ts_s = -1;
-                        if (s2 < S) {
-                            const int nb2 = (s_ctx[s2] + B - 1) / B;
-                            ts_val = lane < nb2 ? __ldg(a.block_tables + (int64_t)s2 * a.max_blocks + lane)
-                                                : 0;
-                            ts_s = s2;
+        // issue the copies of the steps [rb, re), in order, into the ring
+        auto issue_range = [&](int64_t rb, int64_t re) {
+            if (rb >= re) return;
+            Pos p = locate(rb, s_base, S, H);
+            for (int64_t x = rb; x < re && !stop;) {
+                const int ns = s_base[p.s + 1] - s_base[p.s];
+                const int64_t left = re - x;
+                const int run = (int64_t)(ns - p.j) < left ? ns - p.j : (int)left;
+                const int nblk = (s_ctx[p.s] + B - 1) / B;
+                const int32_t* row = a.block_tables + (int64_t)p.s * a.max_blocks;
+                for (int i = 0; i < run; ++i) {
+                    const int j = p.j + i;
+                    // first logical block of the step, and the step's token offset in it
+                    const int jb = C::BPS > 1 ? j * C::BPS : j / C::SPB;
+                    const int sub = C::BPS > 1 ? 0 : j - jb * C::SPB;
+                    const int win = jb & ~31;
+                    if (p.s != tc_s || win != tc_win) {
+                        if (p.s == tc_s && win == tc_win + 32 && tn_ok) {
+                            tc_val = tn_val;
+                        } else if (p.s == ts_s && win == 0) {
+                            tc_val = ts_val;
+                        } else {
+                            tc_val = (win + lane < nblk) ? __ldg(row + win + lane) : 0;
                         }
-                    }
-                    tc_s = p.s;
-                    tc_win = win;
-                    tn_ok = win + 32 < nblk;
-                    if (tn_ok) tn_val = (win + 32 + lane < nblk) ? __ldg(row + win + 32 + lane) : 0;
-                }
-                int phys_raw[C::BPS];
-#pragma unroll
-                for (int b = 0; b < C::BPS; ++b)
-                    phys_raw[b] = __shfl_sync(kFull, tc_val, jb + b - win);
-                int ok = 1;
-                if (lane == 0) {
-                    ok = wait_phase(&empty[stage], phase ^ 1u, abort_flag) ? 1 : 0;
-                    if (ok) {
-                        // only the step's valid tokens move (the last step of a
-                        // row is usually partial); the rest of the stage keeps
-                        // stale bytes that the consumers mask out
-                        const int tok0 = j * C::SUB;
-                        uint32_t bytes[C::BPS];
-                        uint32_t tx = 0;
-#pragma unroll
-                        for (int b = 0; b < C::BPS; ++b) {
-                            int valid = s_ctx[p.s] - (tok0 + b * C::TPC);
-                            valid = valid < 0 ? 0 : (valid > C::TPC ? C::TPC : valid);
-                            bytes[b] = (uint32_t)valid * (uint32_t)(D * 2);
-                            tx += 2 * bytes[b];
-                        }
-                        unsigned char* dst = ring + (size_t)stage * C::STAGE;
-                        mbar_arrive_expect_tx(&full[stage], tx);
-#pragma unroll
-                        for (int b = 0; b < C::BPS; ++b) {
-                            if (bytes[b] == 0) continue;
-                            int64_t phys = phys_raw[b];
-                            if (phys < 0 || phys >= a.num_blocks) {
-                                atomicOr(a.err, PKV_DEVERR_BAD_BLOCK);
-                                phys = 0;
+                        if (p.s != tc_s) {
+                            int s2 = p.s + 1;
+                            while (s2 < S && s_base[s2 + 1] == s_base[s2]) ++s2;
+                            ts_s = -1;
+                            if (s2 < S) {
+                                const int nb2 = (s_ctx[s2] + B - 1) / B;
+                                ts_val = lane < nb2 ? __ldg(a.block_tables + (int64_t)s2 * a.max_blocks + lane)
+                                                    : 0;
+                                ts_s = s2;
                             }
-                            const int64_t off =
-                                ((phys * H + p.h) * B + (int64_t)sub * C::SUB) * (int64_t)D * 2;
-                            const uint32_t doff = (uint32_t)(b * C::TPC * D * 2);
-                            bulk_g2s(dst + doff, kpool + off, bytes[b], &full[stage]);
-                            bulk_g2s(dst + C::CHUNK + doff, vpool + off, bytes[b], &full[stage]);
+                        }
+                        tc_s = p.s;
+                        tc_win = win;
+                        tn_ok = win + 32 < nblk;
+                        if (tn_ok) tn_val = (win + 32 + lane < nblk) ? __ldg(row + win + 32 + lane) : 0;
+                    }
+                    int phys_raw[C::BPS];
+#pragma unroll
+                    for (int b = 0; b < C::BPS; ++b)
+                        phys_raw[b] = __shfl_sync(kFull, tc_val, jb + b - win);
+                    int ok = 1;
+                    if (lane == 0) {
+                        ok = wait_phase(&empty[stage], phase ^ 1u, abort_flag) ? 1 : 0;
+                        if (ok) {
+                            // only the step's valid tokens move (the last step of a
+                            // row is usually partial); the rest of the stage keeps
+                            // stale bytes that the consumers mask out
+                            const int tok0 = j * C::SUB;
+                            uint32_t bytes[C::BPS];
+                            uint32_t tx = 0;
+#pragma unroll
+                            for (int b = 0; b < C::BPS; ++b) {
+                                int valid = s_ctx[p.s] - (tok0 + b * C::TPC);
+                                valid = valid < 0 ? 0 : (valid > C::TPC ? C::TPC : valid);
+                                bytes[b] = (uint32_t)valid * (uint32_t)(D * 2);
+                                tx += 2 * bytes[b];
+                            }
+                            unsigned char* dst = ring + (size_t)stage * C::STAGE;
+                            mbar_arrive_expect_tx(&full[stage], tx);
+#pragma unroll
+                            for (int b = 0; b < C::BPS; ++b) {
+                                if (bytes[b] == 0) continue;
+                                int64_t phys = phys_raw[b];
+                                if (phys < 0 || phys >= a.num_blocks) {
+                                    atomicOr(a.err, PKV_DEVERR_BAD_BLOCK);
+                                    phys = 0;
+                                }
+                                const int64_t off =
+                                    ((phys * H + p.h) * B + (int64_t)sub * C::SUB) * (int64_t)D * 2;
+                                const uint32_t doff = (uint32_t)(b * C::TPC * D * 2);
+                                bulk_g2s(dst + doff, kpool + off, bytes[b], &full[stage]);
+                                bulk_g2s(dst + C::CHUNK + doff, vpool + off, bytes[b], &full[stage]);
+                            }
                         }
                     }
-                }
-                ok = __shfl_sync(kFull, ok, 0);
-                if (!ok) {
-                    if (lane == 0) {
-                        if (!*abort_flag) atomicOr(a.err, PKV_DEVERR_TIMEOUT);
-                        *abort_flag = 1;
+                    ok = __shfl_sync(kFull, ok, 0);
+                    if (!ok) {
+                        if (lane == 0) {
+                            if (!*abort_flag) atomicOr(a.err, PKV_DEVERR_TIMEOUT);
+                            *abort_flag = 1;
+                        }
+                        stop = true;
+                        break;
                     }
-                    stop = true;
-                    break;
+                    ++issued;
+                    if (++stage == C::NSTAGE) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
                 }
-                ++issued;
-                if (++stage == C::NSTAGE) {
-                    stage = 0;
-                    phase ^= 1u;
+                if (stop) break;
+                x += run;
+                p.j += run;
+                if (p.j == ns && x < re) next_segment(p, s_base, S, H);
+            }
+        };
+        // the static range first; then (balanced split) claimed chunks, each
+        // handed to the consumers through the queue with the query slice of
+        // its first row
+        issue_range(xb, xe);
+#if PKV_DECODE_DYN_PER_CTA != 0
+        // (the claim state lives only here, not across the static range's loop)
+        int published = 0;
+        bool stamped = false;
+        unsigned long long* claim_word = reinterpret_cast<unsigned long long*>(a.ws) + 2;
+        const char* qbytes = static_cast<const char*>(a.q);
+        while (!stop && !sp.fixed && sp.Kd > 0) {
+            int64_t k = -1;
+            if (lane == 0) {
+                k = claim_chunk(claim_word, a.epoch, stamped);
+                if (k < 0) atomicOr(a.err, PKV_DEVERR_TIMEOUT);
+            }
+            k = __shfl_sync(kFull, k, 0);
+            const bool more = k >= 0 && k < sp.Kd;
+            const int slot = published % C::QN;
+            if (lane == 0) {
+                qid[slot] = more ? (int)k : -1;
+                if (more) {
+                    const Pos p0 = locate(sp.X + k * sp.Ld, s_base, S, H);
+                    mbar_arrive_expect_tx(&qfull[slot], D * 2);
+                    bulk_g2s(qbuf + (size_t)slot * D * 2,
+                             qbytes + ((int64_t)p0.s * H + p0.h) * (int64_t)D * 2, D * 2,
+                             &qfull[slot]);
+                } else {
+                    mbar_arrive(&qfull[slot]);
                 }
             }
-            if (stop) break;
-            x += run;
-            p.j += run;
-            if (p.j == ns && x < xe) next_segment(p, s_base, S, H);
+            ++published;
+            __syncwarp();
+            if (!more) break;
+            const int64_t rb = sp.X + k * sp.Ld;
+            issue_range(rb, rb + sp.Ld < total ? rb + sp.Ld : total);
         }
+        __syncwarp();
+        if (*abort_flag && lane == 0) {
+            // the query slices still in flight
+            for (int e = published > C::QN ? published - C::QN : 0; e < published; ++e)
+                wait_bounded(&qfull[e % C::QN], (uint32_t)(e / C::QN) & 1u, nullptr);
+        }
+#endif
         __syncwarp();
         if (*abort_flag && lane == 0) {
             // wind down: let the copies still in flight land before exiting
@@ -548,140 +711,181 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, PKV_DECODE_MIN_CTAS)
     float2* ws_ml = reinterpret_cast<float2*>(a.ws + a.ws_l.ml_off);
     float* ws_acc = reinterpret_cast<float*>(a.ws + a.ws_l.acc_off);
 
-    Pos p = locate(xb, s_base, S, H);
-    int64_t x = xb;
     uint32_t g0 = 0;
     int pbuf = 0;
-    // the query slice of the next piece is loaded one piece ahead
-    uint4 q_next = ld_nc_v4(qptr + ((int64_t)p.s * H + p.h) * D + dl * 8);
-    while (x < xe) {
-        const int ns = s_base[p.s + 1] - s_base[p.s];
-        const int64_t chunk = x / L;
-        int64_t len64 = ns - p.j;
-        if (L - (x - chunk * L) < len64) len64 = L - (x - chunk * L);
-        if (xe - x < len64) len64 = xe - x;
-        const int len = (int)len64;
-        const bool whole = (p.j == 0 && len == ns);
-        const int ctx = s_ctx[p.s];
-        const int64_t row = (int64_t)p.s * H + p.h;
-
-        const uint4 q_raw = q_next;
-        if (x + len < xe && p.j + len == ns) {
-            Pos pn = p;
-            next_segment(pn, s_base, S, H);
-            q_next = ld_nc_v4(qptr + ((int64_t)pn.s * H + pn.h) * D + dl * 8);
+    // the static range, then the claimed chunks the producer publishes; one
+    // copy of the loop serves both.  q_first is the query slice of a range's
+    // first row; the next piece's slice is loaded one piece ahead, and the
+    // chunk id and the chunk's end are carried along (no division per piece).
+    int64_t rb = xb, re = xe;
+    uint4 q_first = make_uint4(0u, 0u, 0u, 0u);
+    if (xb < xe) {
+        const Pos p0 = locate(xb, s_base, S, H);
+        q_first = ld_nc_v4(qptr + ((int64_t)p0.s * H + p0.h) * D + dl * 8);
+    }
+#if PKV_DECODE_DYN_PER_CTA != 0
+    int qe = 0;
+#endif
+    while (true) {
+        if (rb >= re) {
+#if PKV_DECODE_DYN_PER_CTA == 0
+            break;
+#else
+            if (sp.fixed || sp.Kd == 0 || *abort_flag) break;
+            const int slot = qe % C::QN;
+            if (!wait_phase(&qfull[slot], (uint32_t)(qe / C::QN) & 1u, abort_flag)) {
+                if (lane == 0) {
+                    if (!*abort_flag) atomicOr(a.err, PKV_DEVERR_TIMEOUT);
+                    *abort_flag = 1;
+                }
+                break;
+            }
+            ++qe;
+            const int k = qid[slot];
+            if (k < 0) break;
+            q_first = *reinterpret_cast<const uint4*>(qbuf + (size_t)slot * D * 2 + dl * 16);
+            rb = sp.X + (int64_t)k * sp.Ld;
+            re = rb + sp.Ld < total ? rb + sp.Ld : total;
+#endif
         }
-        float qf[8];
-        {
-            Elem<T>::to_f32x8(q_raw, qf);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) qf[e] *= a.scale_log2;
-        }
-        float m = -INFINITY, l = 0.f;
-        float acc[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-
-        const int first = (int)((uint32_t)(warp + C::NW - (int)(g0 % C::NW)) % C::NW);
-        for (int i = first; i < len; i += C::NW) {
-            const uint32_t g = g0 + (uint32_t)i;
-            const int stage = (int)(g % C::NSTAGE);
-            const uint32_t par = (g / C::NSTAGE) & 1u;
+        Pos p = locate(rb, s_base, S, H);
+        int64_t x = rb;
+        int64_t chunk = sp.chunk(rb);
+        int64_t cend = sp.chunk_end(rb);
+        uint4 q_next = q_first;
+        while (x < re) {
+            if (x == cend) {                         // fixed split: the next chunk of the run
+                ++chunk;
+                cend = cend + sp.Ls < re ? cend + sp.Ls : re;
+            }
+            const int ns = s_base[p.s + 1] - s_base[p.s];
+            int64_t len64 = ns - p.j;
+            if (cend - x < len64) len64 = cend - x;
+            if (re - x < len64) len64 = re - x;
+            const int len = (int)len64;
+            const bool whole = (p.j == 0 && len == ns);
+            const int ctx = s_ctx[p.s];
+            const int64_t row = (int64_t)p.s * H + p.h;
+    
+            const uint4 q_raw = q_next;
+            if (x + len < re && p.j + len == ns) {
+                Pos pn = p;
+                next_segment(pn, s_base, S, H);
+                q_next = ld_nc_v4(qptr + ((int64_t)pn.s * H + pn.h) * D + dl * 8);
+            }
+            float qf[8];
+            {
+                Elem<T>::to_f32x8(q_raw, qf);
+    #pragma unroll
+                for (int e = 0; e < 8; ++e) qf[e] *= a.scale_log2;
+            }
+            float m = -INFINITY, l = 0.f;
+            float acc[8];
+    #pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+    
+            const int first = (int)((uint32_t)(warp + C::NW - (int)(g0 % C::NW)) % C::NW);
+            for (int i = first; i < len; i += C::NW) {
+                const uint32_t g = g0 + (uint32_t)i;
+                const int stage = (int)(g % C::NSTAGE);
+                const uint32_t par = (g / C::NSTAGE) & 1u;
+                if (!*abort_flag) {
+                    if (!wait_phase(&full[stage], par, abort_flag)) {
+                        if (lane == 0) {
+                            if (!*abort_flag) atomicOr(a.err, PKV_DEVERR_TIMEOUT);
+                            *abort_flag = 1;
+                        }
+                    }
+                }
+                __syncwarp();
+                const uint4* Ks = reinterpret_cast<const uint4*>(ring + (size_t)stage * C::STAGE);
+                const uint4* Vs = Ks + C::CHUNK / 16;
+                const int nvalid = ctx - (p.j + i) * C::SUB;   // >= 1
+    
+                float part[C::NL];
+    #pragma unroll
+                for (int t = 0; t < C::NL; ++t) {
+                    const uint4 kv = Ks[t * 32 + lane];
+                    float kf[8];
+                    Elem<T>::to_f32x8(kv, kf);
+                    float d = 0.f;
+    #pragma unroll
+                    for (int e = 0; e < 8; ++e) d = fmaf(qf[e], kf[e], d);
+                    part[t] = d;
+                }
+                float z = reduce_scatter<C::NL, C::LOG_LPT>(part, dl);
+                if (own * C::TPL + hi >= nvalid) z = -INFINITY;
+                const float m_new = fmaxf(m, warp_max(z));
+                const float alpha = exp2f(m - m_new);
+                const float pz = exp2f(z - m_new);
+                l = fmaf(l, alpha, leader ? pz : 0.f);
+    #pragma unroll
+                for (int e = 0; e < 8; ++e) acc[e] *= alpha;
+    #pragma unroll
+                for (int t = 0; t < C::NL; ++t) {
+                    const float pt = __shfl_sync(kFull, pz, (hi << C::LOG_LPT) | (t << C::RS));
+                    if (t * C::TPL + hi < nvalid) {
+                        const uint4 vv = Vs[t * 32 + lane];
+                        float vf[8];
+                        Elem<T>::to_f32x8(vv, vf);
+    #pragma unroll
+                        for (int e = 0; e < 8; ++e) acc[e] = fmaf(pt, vf[e], acc[e]);
+                    }
+                }
+                m = m_new;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[stage]);
+            }
+    
+            // fold the token groups of the warp, then merge the warps
+    #pragma unroll
+            for (int o = C::LPT; o < 32; o <<= 1)
+    #pragma unroll
+                for (int e = 0; e < 8; ++e) acc[e] += __shfl_xor_sync(kFull, acc[e], o);
+            l = warp_sum(l);
+            float* mrow = merge + (pbuf * C::NW + warp) * C::MROW;
+            if (lane < C::LPT) {
+                float4* d4 = reinterpret_cast<float4*>(mrow + dl * 8);
+                d4[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                d4[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+            }
+            if (lane == 0) {
+                mrow[D] = m;
+                mrow[D + 1] = l;
+            }
+            named_bar_sync(1, C::NW * 32);
             if (!*abort_flag) {
-                if (!wait_phase(&full[stage], par, abort_flag)) {
-                    if (lane == 0) {
-                        if (!*abort_flag) atomicOr(a.err, PKV_DEVERR_TIMEOUT);
-                        *abort_flag = 1;
+                const float* mb = merge + pbuf * C::NW * C::MROW;
+                float M = -INFINITY;
+    #pragma unroll
+                for (int w = 0; w < C::NW; ++w) M = fmaxf(M, mb[w * C::MROW + D]);
+                float sc[C::NW];
+                float ls = 0.f;
+    #pragma unroll
+                for (int w = 0; w < C::NW; ++w) {
+                    sc[w] = exp2f(mb[w * C::MROW + D] - M);
+                    ls = fmaf(sc[w], mb[w * C::MROW + D + 1], ls);
+                }
+                for (int d = tid; d < D; d += C::NW * 32) {
+                    float av = 0.f;
+    #pragma unroll
+                    for (int w = 0; w < C::NW; ++w) av = fmaf(sc[w], mb[w * C::MROW + d], av);
+                    if (whole) {
+                        optr[row * D + d] = Elem<T>::from_f32(av / ls);
+                    } else {
+                        const int64_t slot = row + chunk;
+                        ws_acc[slot * D + d] = av;
+                        if (d == 0) ws_ml[slot] = make_float2(M, ls);
                     }
                 }
             }
-            __syncwarp();
-            const uint4* Ks = reinterpret_cast<const uint4*>(ring + (size_t)stage * C::STAGE);
-            const uint4* Vs = Ks + C::CHUNK / 16;
-            const int nvalid = ctx - (p.j + i) * C::SUB;   // >= 1
-
-            float part[C::NL];
-#pragma unroll
-            for (int t = 0; t < C::NL; ++t) {
-                const uint4 kv = Ks[t * 32 + lane];
-                float kf[8];
-                Elem<T>::to_f32x8(kv, kf);
-                float d = 0.f;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) d = fmaf(qf[e], kf[e], d);
-                part[t] = d;
-            }
-            float z = reduce_scatter<C::NL, C::LOG_LPT>(part, dl);
-            if (own * C::TPL + hi >= nvalid) z = -INFINITY;
-            const float m_new = fmaxf(m, warp_max(z));
-            const float alpha = exp2f(m - m_new);
-            const float pz = exp2f(z - m_new);
-            l = fmaf(l, alpha, leader ? pz : 0.f);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] *= alpha;
-#pragma unroll
-            for (int t = 0; t < C::NL; ++t) {
-                const float pt = __shfl_sync(kFull, pz, (hi << C::LOG_LPT) | (t << C::RS));
-                if (t * C::TPL + hi < nvalid) {
-                    const uint4 vv = Vs[t * 32 + lane];
-                    float vf[8];
-                    Elem<T>::to_f32x8(vv, vf);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[e] = fmaf(pt, vf[e], acc[e]);
-                }
-            }
-            m = m_new;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[stage]);
+            pbuf ^= 1;
+            x += len;
+            g0 += (uint32_t)len;
+            p.j += len;
+            if (p.j == ns && x < re) next_segment(p, s_base, S, H);
         }
-
-        // fold the token groups of the warp, then merge the warps
-#pragma unroll
-        for (int o = C::LPT; o < 32; o <<= 1)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] += __shfl_xor_sync(kFull, acc[e], o);
-        l = warp_sum(l);
-        float* mrow = merge + (pbuf * C::NW + warp) * C::MROW;
-        if (lane < C::LPT) {
-            float4* d4 = reinterpret_cast<float4*>(mrow + dl * 8);
-            d4[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-            d4[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-        }
-        if (lane == 0) {
-            mrow[D] = m;
-            mrow[D + 1] = l;
-        }
-        named_bar_sync(1, C::NW * 32);
-        if (!*abort_flag) {
-            const float* mb = merge + pbuf * C::NW * C::MROW;
-            float M = -INFINITY;
-#pragma unroll
-            for (int w = 0; w < C::NW; ++w) M = fmaxf(M, mb[w * C::MROW + D]);
-            float sc[C::NW];
-            float ls = 0.f;
-#pragma unroll
-            for (int w = 0; w < C::NW; ++w) {
-                sc[w] = exp2f(mb[w * C::MROW + D] - M);
-                ls = fmaf(sc[w], mb[w * C::MROW + D + 1], ls);
-            }
-            for (int d = tid; d < D; d += C::NW * 32) {
-                float av = 0.f;
-#pragma unroll
-                for (int w = 0; w < C::NW; ++w) av = fmaf(sc[w], mb[w * C::MROW + d], av);
-                if (whole) {
-                    optr[row * D + d] = Elem<T>::from_f32(av / ls);
-                } else {
-                    const int64_t slot = row + chunk;
-                    ws_acc[slot * D + d] = av;
-                    if (d == 0) ws_ml[slot] = make_float2(M, ls);
-                }
-            }
-        }
-        pbuf ^= 1;
-        x += len;
-        g0 += (uint32_t)len;
-        p.j += len;
-        if (p.j == ns && x < xe) next_segment(p, s_base, S, H);
+        rb = re;
     }
 }
 
@@ -734,23 +938,25 @@ __global__ void __launch_bounds__(128) paged_decode_merge(const DecodeArgs a) {
         if (tid == 127) base[S] = run;
         __syncthreads();
     }
+    // The first CTA always waits for the main kernel, even where its rows need
+    // no merge: then this grid cannot complete before the main kernel has,
+    // which the next call's claim-word stamp and any later reader of the
+    // output rely on.  The other CTAs wait only where they merge, so those
+    // with nothing to do leave at once.
+    const bool anchor = blockIdx.x == 0;
+    if (anchor) grid_dependency_wait();
     const int64_t sh = (int64_t)blockIdx.x * 4 + warp;
     if (sh >= (int64_t)S * H) return;
     const int s = (int)(sh / H), h = (int)(sh - (int64_t)s * H);
     const int ns = base[s + 1] - base[s];
-    const int64_t total = (int64_t)H * base[S];
-    int64_t L = a.L_steps;
-    if (L <= 0) {
-        L = (total + a.main_grid - 1) / a.main_grid;
-        if (L < a.min_chunk_steps) L = a.min_chunk_steps;
-    }
+    const Split sp = make_split((int64_t)H * base[S], a.main_grid, a.L_steps, a.min_chunk_steps);
     const int64_t x0 = (int64_t)H * base[s] + (int64_t)h * ns;
-    const int64_t kf = ns ? x0 / L : 0, kl = ns ? (x0 + ns - 1) / L : 0;
+    const int64_t kf = ns ? sp.chunk(x0) : 0, kl = ns ? sp.chunk(x0 + ns - 1) : 0;
     if (ns > 0 && kf == kl) return;          // written by the main kernel
 
-    grid_dependency_wait();
-    // the main kernel writes L = 0 when it could not run (workspace too small)
-    if (reinterpret_cast<const int64_t*>(a.ws)[0] != L) return;
+    if (!anchor) grid_dependency_wait();
+    // the main kernel writes 0 here when it could not run (workspace too small)
+    if (reinterpret_cast<const int64_t*>(a.ws)[0] != sp.Ls) return;
     constexpr int PER = D / 32;
     T* o = static_cast<T*>(a.out) + sh * D + lane * PER;
     if (ns == 0) {
@@ -804,30 +1010,51 @@ __global__ void __launch_bounds__(128) paged_decode_merge(const DecodeArgs a) {
 }
 
 // ------------------------------------------------------------ host glue
+constexpr int kLimitDevices = 64;
+
 template <typename T, int D, int B>
 struct Launcher {
     using C = Cfg<D, B>;
     static size_t smem_bytes(int S) { return C::smem(S); }
     static size_t merge_smem(int S) { return 4 * (size_t)(S + 1 + 8); }
+    // The dynamic shared memory limit of a kernel also steers the L1/shared
+    // carveout the driver picks for it: with the limit at the device maximum
+    // every launch got the largest carveout (228 KiB, the least L1), whatever
+    // its batch needed.  So each kernel's limit is kept at exactly the size
+    // of the launch in hand, re-set when the batch size changes, with the
+    // lock held across the launch so that concurrent host threads with
+    // different batch sizes cannot undercut each other.
+    struct Limits {
+        std::mutex mu;
+        int main[kLimitDevices] = {};
+        int merge[kLimitDevices] = {};
+    };
+    static Limits& limits() {
+        static Limits l;
+        return l;
+    }
+    static cudaError_t set_limit(int* cur, const void* fn, size_t bytes) {
+        if (*cur == (int)bytes) return cudaSuccess;
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)bytes);
+        if (e == cudaSuccess) *cur = (int)bytes;
+        return e;
+    }
     static cudaError_t occupancy(int* ctas, size_t smem) {
-        // Both kernels' shared memory grows with the batch: allow each the
-        // device's opt-in maximum once, so that any batch size launches
-        // whatever size an earlier call used.
         int dev = 0, max_optin = 0;
         cudaError_t e = cudaGetDevice(&dev);
         if (e != cudaSuccess) return e;
+        if (dev < 0 || dev >= kLimitDevices) return cudaErrorInvalidDevice;
         e = cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(paged_decode_merge<T, D, B>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, max_optin);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(paged_decode_main<T, D, B>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, max_optin);
         if (e != cudaSuccess) return e;
         if (smem > (size_t)max_optin) {
             *ctas = 0;
             return cudaSuccess;
         }
+        Limits& L = limits();
+        std::lock_guard<std::mutex> lk(L.mu);
+        e = set_limit(&L.main[dev], (const void*)paged_decode_main<T, D, B>, smem);
+        if (e != cudaSuccess) return e;
         return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, paged_decode_main<T, D, B>,
                                                              C::THREADS, smem);
     }
@@ -837,6 +1064,10 @@ struct Launcher {
     static cudaError_t launch(const DecodeArgs& args, int grid, cudaStream_t stream) {
         DecodeArgs a = args;
         a.main_grid = grid;
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (dev < 0 || dev >= kLimitDevices) return cudaErrorInvalidDevice;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -847,12 +1078,18 @@ struct Launcher {
         cfg.stream = stream;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        cudaError_t e = cudaLaunchKernelEx(&cfg, paged_decode_main<T, D, B>, a);
+        Limits& L = limits();
+        std::lock_guard<std::mutex> lk(L.mu);
+        e = set_limit(&L.main[dev], (const void*)paged_decode_main<T, D, B>, cfg.dynamicSmemBytes);
+        if (e != cudaSuccess) return e;
+        e = cudaLaunchKernelEx(&cfg, paged_decode_main<T, D, B>, a);
         if (e != cudaSuccess) return e;
         const int64_t warps = (int64_t)a.S * a.H;
         cfg.gridDim = dim3((unsigned)((warps + 3) / 4));
         cfg.blockDim = dim3(128);
         cfg.dynamicSmemBytes = merge_smem(a.S);
+        e = set_limit(&L.merge[dev], (const void*)paged_decode_merge<T, D, B>, cfg.dynamicSmemBytes);
+        if (e != cudaSuccess) return e;
         e = cudaLaunchKernelEx(&cfg, paged_decode_merge<T, D, B>, a);
         if (e != cudaSuccess) return e;
         return cudaGetLastError();

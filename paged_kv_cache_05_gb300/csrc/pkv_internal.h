@@ -23,8 +23,21 @@ int32_t* device_error_word();
 // ---- device facts, cached per device ---------------------------------------
 int sm_count(int device);
 
+// ---- decode work split -------------------------------------------------------
+// Balanced split: each CTA streams a static share of STATIC_EIGHTHS/8 of the
+// steps; the rest is cut into DYN_PER_CTA chunks per CTA that CTAs claim as
+// they finish (0 turns the dynamic tail off).  Shared by host (workspace
+// bound) and device (the split).
+#ifndef PKV_DECODE_STATIC_EIGHTHS
+#define PKV_DECODE_STATIC_EIGHTHS 6
+#endif
+#ifndef PKV_DECODE_DYN_PER_CTA
+#define PKV_DECODE_DYN_PER_CTA 4
+#endif
+
 // ---- decode workspace layout -------------------------------------------------
-// [0, 64)                  header: int64 L (chunk length in steps), int64 total steps
+// [0, 64)                  header: int64 static chunk length, int64 total steps,
+//                          uint64 claim word of the dynamic chunks (epoch << 24 | count)
 // [64, 64 + 4 (S + 1))     int32 step prefix per sequence (written by CTA 0)
 // then, 256-aligned:       float2 ml[cap]   (running max in log2 units, sum)
 // then, 256-aligned:       float  acc[cap][D] (unnormalised output)
@@ -69,7 +82,8 @@ struct DecodeArgs {
     int64_t num_blocks;
     int64_t L_steps;         // fixed chunk length in steps, 0 = balanced
     int min_chunk_steps;     // balanced mode: lower bound of the chunk length
-    int main_grid;           // CTAs of the main kernel (the balanced chunk count)
+    int main_grid;           // CTAs of the main kernel
+    uint64_t epoch;          // 40-bit tag of this call (claims of the dynamic chunks)
     char* ws;
     WsLayout ws_l;
     int32_t* err;

@@ -212,3 +212,43 @@ def test_alternating_batch_sizes(pkv):
             ref = run_oracle(case, 0.09)
             cases[S] = (case, ref)
         attn_check(run_gpu(pkv, case, 0.09), ref, "S=%d" % S)
+
+
+def test_dynamic_tail_repeated_calls_and_graph_replay(pkv):
+    """A batch large enough (about 57K steps) that the balanced split ends in
+    chunks claimed at run time on any grid up to the largest.  Each call is
+    checked against the oracle: repeated calls on one workspace that holds
+    garbage beforehand (the call stamps its own claim word), then CUDA graph
+    replays, where the call's arguments, its epoch included, are frozen."""
+    import torch
+    rs = np.random.default_rng(17)
+    S, H, D, B = 128, 16, 128, 16
+    ctx = [int(c) for c in rs.integers(1, 900, size=S)]
+    case = random_case(rs, S, H, D, B, ctx, "f16")
+    scale = float(np.float32(1 / math.sqrt(D)))
+    ref = run_oracle(case, scale)
+    q = to_dev(case["q"], "f16")
+    kc, vc = to_dev(case["kc"], "f16"), to_dev(case["vc"], "f16")
+    bt = torch.from_numpy(case["bt"]).cuda()
+    cl = torch.from_numpy(case["ctx"]).cuda()
+    ws = pkv.alloc_workspace(S, H, D, B, bt.shape[1], 0, q.device)
+    out = torch.empty_like(q)
+    for i in range(3):
+        ws.random_(0, 256)
+        out.fill_(float("nan"))
+        pkv.paged_attention_decode(out, q, kc, vc, bt, cl, scale, workspace=ws)
+        torch.cuda.synchronize()
+        assert pkv.get_device_error() == 0
+        attn_check(out, ref, "call %d" % i)
+        # header word 2 counts the claims of this call: the tail was dynamic
+        claims = int(ws[16:24].view(torch.int64).cpu()[0]) & 0xFFFFFF
+        assert claims > 0
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        pkv.paged_attention_decode(out, q, kc, vc, bt, cl, scale, workspace=ws)
+    for i in range(3):
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert pkv.get_device_error() == 0
+        attn_check(out, ref, "replay %d" % i)
