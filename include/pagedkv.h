@@ -175,17 +175,24 @@ pkv_status pkv_paged_attention_decode_noalloc(void* out, const void* q, const vo
  *   out[row][h] = sum_{t <= p} softmax_t(scale * q[row][h] . K_s[t][h]) V_s[t][h]
  * A whole prompt is qlen == ctx; a prompt continued after a cached prefix
  * (shared prefix, chunked prefill) is qlen < ctx; qlen == 1 is one decode row.
- * q, out: [total query rows][num_heads][head_dim]; query_start: int32
- * [num_seqs + 1], device.  max_query_len (host) bounds every qlen; a larger
- * one sets PKV_DEVERR_BAD_CONTEXT and its extra rows are not written.
- * Tensor cores (mma.sync m16n8k16), fp32 accumulation, one launch, no workspace.
+ * q, out: [num_query_tokens][num_heads][head_dim] (num_query_tokens = the
+ * rows of q and out, host); query_start: int32 [num_seqs + 1], device, with
+ * every sequence's rows inside [0, num_query_tokens) (else the sequence is
+ * skipped and PKV_DEVERR_BAD_CONTEXT set).  max_query_len (host) bounds every
+ * qlen; a larger one sets PKV_DEVERR_BAD_CONTEXT and its extra rows are not
+ * written.  num_blocks * num_heads * block_size must stay below 2^31 (the
+ * tiled copies address cache rows with 32-bit coordinates).
+ * Fifth-generation tensor cores (tcgen05, accumulators in tensor memory, TMA
+ * tiled copies through the block table), fp32 accumulation, one launch, no
+ * workspace.
  */
 pkv_status pkv_paged_attention_prefill(void* out, const void* q, const void* k_cache,
                                        const void* v_cache, const int32_t* block_tables,
                                        const int32_t* context_lens, const int32_t* query_start,
                                        float scale, int num_seqs, int num_heads, int head_dim,
                                        int block_size, int max_blocks_per_seq, int64_t num_blocks,
-                                       int max_query_len, pkv_dtype dtype, cudaStream_t stream);
+                                       int max_query_len, int num_query_tokens, pkv_dtype dtype,
+                                       cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Cache maintenance                                                         */

@@ -60,7 +60,7 @@ def lib():
             "pkv_paged_attention_decode_noalloc": ([P, P, P, P, P, P, f32, i32, i32, i32, i32,
                                                     i32, i64, i32, i32, P], i32),
             "pkv_paged_attention_prefill": ([P, P, P, P, P, P, P, f32, i32, i32, i32, i32,
-                                             i32, i64, i32, i32, P], i32),
+                                             i32, i64, i32, i32, i32, P], i32),
             "pkv_reshape_and_cache": ([P, P, P, P, P, i32, i32, i32, i32, i64, i32, P], i32),
             "pkv_copy_blocks": ([P, P, P, i32, i32, i32, i32, i64, i32, P], i32),
             "pkv_swap_blocks": ([P, P, P, P, P, i32, i32, i32, i32, i64, i64, i32, P], i32),
@@ -213,7 +213,7 @@ def paged_attention_prefill(out, q, k_cache, v_cache, block_tables, context_lens
                _dev(v_cache, "v_cache"), _dev(block_tables, "block_tables", torch.int32),
                _dev(context_lens, "context_lens", torch.int32, 1),
                _dev(query_start, "query_start", torch.int32, 1), float(scale), S, H, D, B,
-               block_tables.shape[1], nb, int(max_query_len), _dtype_code(q.dtype),
+               block_tables.shape[1], nb, int(max_query_len), T, _dtype_code(q.dtype),
                _stream(stream)))
     return out
 

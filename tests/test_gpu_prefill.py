@@ -8,6 +8,7 @@ import pytest
 
 import oracle
 from helpers import ORC_DTYPE, attn_check, random_case, to_dev, words
+from paged_kv_cache_05_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
 
@@ -76,3 +77,52 @@ def test_one_token_queries_match_decode(pkv):
                                         case["ctx"], 0.088)
     attn_check(a, ref, "decode")
     attn_check(b, ref, "prefill qlen=1")
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("B", [8, 32])
+def test_prefill_unwritten_slots_never_matter(pkv, dtype, B):
+    """Slots past each context in its last block, and every block no sequence
+    uses, hold NaN / Inf bit patterns: the result equals the one with finite
+    contents there, bit for bit (keys past the context get weight 0 and their
+    values must never be multiplied in)."""
+    import torch
+    rs = np.random.default_rng(900 + B + (dtype == "bf16"))
+    ctx = [5, 130, 255, 256, 300, 1]
+    qlen = [5, 130, 100, 256, 1, 1]
+    H, D = 2, 128
+    case = random_case(rs, len(ctx), H, D, B, ctx, dtype, spare=9)
+    qs = np.concatenate([[0], np.cumsum(qlen)]).astype(np.int32)
+    T = int(qs[-1])
+    q = words((T, H, D), dtype, rs)
+    nan = 0x7E00 if dtype == "f16" else 0x7FC0
+    inf = 0x7C00 if dtype == "f16" else 0x7F80
+
+    def run(kc, vc):
+        out = torch.full((T, H, D), float("nan"), dtype=W.torch_dtype(dtype), device="cuda")
+        pkv.paged_attention_prefill(out, to_dev(q, dtype), to_dev(kc, dtype), to_dev(vc, dtype),
+                                    torch.from_numpy(case["bt"]).cuda(),
+                                    torch.from_numpy(case["ctx"]).cuda(),
+                                    torch.from_numpy(qs).cuda(), 0.088, max(qlen))
+        assert pkv.get_device_error() == 0
+        return out
+
+    a = run(case["kc"], case["vc"])
+    kc, vc = case["kc"].copy(), case["vc"].copy()
+    used = set()
+    for s, n in enumerate(ctx):
+        nb = -(-n // B)
+        used.update(int(x) for x in case["bt"][s, :nb])
+        last = case["bt"][s, nb - 1]
+        kc[last, :, n - (nb - 1) * B:, :] = nan
+        vc[last, :, n - (nb - 1) * B:, :] = inf
+    for blk in range(case["nb"]):
+        if blk not in used:
+            kc[blk] = nan
+            vc[blk] = nan
+    b = run(kc, vc)
+    assert torch.isfinite(b.float()).all()
+    assert torch.equal(a, b)
+    ref = oracle.paged_attention_prefill(q, case["kc"], case["vc"], case["bt"], case["ctx"], qs,
+                                         0.088, ORC_DTYPE[dtype])
+    attn_check(a, ref, "prefill dtype=%s B=%d" % (dtype, B))
