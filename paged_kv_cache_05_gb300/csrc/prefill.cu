@@ -9,34 +9,34 @@
 // positions 0 .. p (causal):
 //   out[i][h] = sum_{t <= p} softmax_t(scale * q[i][h] . K[t][h]) V[t][h].
 //
-// Design.  Persistent CTAs, one per SM, walk the work items (128 query rows
-// of one (sequence, head); one query row per tensor-memory lane) longest
-// first; loads and products run ahead across item boundaries.  Eleven warps:
-//   warps 0, 10 TMA producers: the query tile of each item and the K tiles
-//               (warp 0), the V tiles (warp 10), 128 keys per tile, block by
-//               block through the block table (2-D tiled copies with the
-//               128-byte swizzle), each in a ring of two stages; a K stage is
-//               refilled once its S product is done, a V stage once its P V is;
+// Design.  Persistent CTAs, one per SM, walk the work items longest first;
+// an item is 256 query rows of one (sequence, head): two query tiles A and B
+// of 128 rows, one row per tensor-memory lane, that share every K/V tile.
+// Loads and products run ahead across item boundaries.  Eleven warps:
+//   warps 0, 10 TMA producers: the two query tiles of each item and the K
+//               tiles (warp 0), the V tiles (warp 10), 64 keys per tile, block
+//               by block through the block table (2-D tiled copies with the
+//               128-byte swizzle), each in a ring of 3-4 stages; a K stage is
+//               refilled once its S products are done, a V stage once its
+//               P V products are;
 //   warp 1      owns the tensor memory and issues the MMAs from one thread:
-//               S_j = Q K_j^T into one of two S buffers (128 x 128 fp32), and
-//               O += P_j V_j into the O accumulator (128 x D fp32);
-//   warps 2..9  softmax, two warps per row quarter, each taking half of the
-//               keys of a tile and half of O's columns: read S_j from tensor
-//               memory, causal mask (diagonal tiles only), online softmax in
-//               log2 units (the two halves agree on the running max through
-//               tensor memory), write P_j (16-bit) to shared memory in the
-//               MMA's operand layout, rescale O in tensor memory when the
-//               running max grows.
-// S_{j+1} is computed while the softmax works on S_j.  The running max is
-// only raised when a row's max grows by more than 2^8 (the weights then stay
-// below 256), so most tiles need no O rescale; the result is the same softmax.
-// For bf16, P = high part + residual (two products), so the weights keep
-// about 16 bits.
+//               S_X = Q_X K^T (X = A, B) into double-buffered 128 x 64 fp32
+//               accumulators, O_X += P_X V into 128 x D fp32 accumulators;
+//   warps 2..5  softmax of tile A, warps 6..9 of tile B, one row per thread:
+//               read S from tensor memory, causal mask (diagonal tiles only),
+//               online softmax in log2 units, write P (16-bit) to shared
+//               memory in the MMA's operand layout, rescale O in tensor
+//               memory when the running max grows.
+// While one group's softmax runs, the tensor cores work on the other group's
+// products.  The running max is only raised when a row's max grows by more
+// than 2^8 (the weights then stay below 256), so most tiles need no O
+// rescale; the result is the same softmax.  For bf16, P = high part +
+// residual (two products), so the weights keep about 16 bits.
 //
 // Operand layouts (shared memory, 1024-byte aligned atoms of 8 rows x 128 B,
 // 16-byte chunk c of row r stored at chunk c ^ (r % 8)):
 //   Q, K: K-major (row = token, 64 elements of the head dimension per slab);
-//   P:    K-major (row = query, 64 keys per slab);
+//   P:    K-major (row = query, the tile's 64 keys);
 //   V:    the same bytes as K, read as an MN-major operand (N = head dimension).
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -50,38 +50,44 @@
 
 namespace {
 
-constexpr int kBM = 128;            // query rows per CTA (MMA M, tensor-memory lanes)
-constexpr int kBN = 128;            // keys per tile (MMA N of S, K of P V)
-constexpr int kWarps = 11;          // K producer, MMA issuer, 8 softmax warps, V producer
+constexpr int kBM = 128;            // query rows per tile (MMA M, tensor-memory lanes)
+constexpr int kRows = 2 * kBM;      // query rows per work item (tiles A and B)
+constexpr int kBN = 64;             // keys per K/V tile (MMA N of S, K of P V)
+constexpr int kWarps = 11;          // K producer, MMA issuer, 2 x 4 softmax warps, V producer
 constexpr int kThreads = kWarps * 32;
-constexpr int kSoftmaxThreads = 256;
-constexpr uint32_t kTmemCols = 512;  // S0 [0,128), S1 [128,256), O [256, 256+D), exchange
-constexpr uint32_t kColO = 256;
-constexpr uint32_t kColX = 384;      // per-row exchange between the two softmax halves
+constexpr uint32_t kTmemCols = 512;
+// tensor-memory columns: S of group X buffer b at kColS + (2X + b) kBN, O of
+// group X at kColO + X D
+constexpr uint32_t kColS = 0;
+constexpr uint32_t kColO = 4 * kBN;
 constexpr float kRescaleLog2 = 8.f;  // raise the running max only past this growth
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr uint32_t kWaitLimitIters = 1u << 26;
 
-template <int D>
+template <int D, bool SPLIT>
 struct PCfg {
     static constexpr int SLABS = D / 64;               // 128-byte slabs per K/Q row
-    static constexpr int SLAB_Q = kBM * 128;           // bytes of one Q slab
+    static constexpr int SLAB_Q = kBM * 128;           // bytes of one Q slab (one tile)
     static constexpr int SLAB_KV = kBN * 128;          // bytes of one K (or V) slab
-    static constexpr int SLAB_P = kBM * 128;           // bytes of one P slab (64 keys)
+    static constexpr int P_BYTES = kBM * kBN * 2;      // one group's P (one slab)
+    static constexpr int Q_BYTES = SLABS * SLAB_Q;     // one tile's Q
     static constexpr int KV_BYTES = SLABS * SLAB_KV;
-    static constexpr int Q_OFF = 0;
-    static constexpr int K_OFF = Q_OFF + SLABS * SLAB_Q;
-    static constexpr int V_OFF = K_OFF + 2 * KV_BYTES;
-    static constexpr int P_OFF = V_OFF + 2 * KV_BYTES;
-    static constexpr int PLO_OFF = P_OFF + 2 * SLAB_P;   // bf16 residual of P
-    static constexpr int bar_off(bool split) { return PLO_OFF + (split ? 2 * SLAB_P : 0); }
+    // K and V ring depth: as deep as shared memory allows (a K/V tile takes
+    // about as long to arrive as four tiles take to compute)
+    static constexpr int NST = (D == 128 && SPLIT) ? 3 : 4;
+    static constexpr int Q_OFF = 0;                    // Q_A, Q_B
+    static constexpr int K_OFF = Q_OFF + 2 * Q_BYTES;
+    static constexpr int V_OFF = K_OFF + NST * KV_BYTES;
+    static constexpr int P_OFF = V_OFF + NST * KV_BYTES;  // P_A, P_B
+    static constexpr int PLO_OFF = P_OFF + 2 * P_BYTES;   // bf16 residuals of P_A, P_B
+    static constexpr int BAR_OFF = PLO_OFF + (SPLIT ? 2 * P_BYTES : 0);
     // dynamic shared memory: 1 KiB of alignment slack, the buffers, 256 B of
     // barriers; never below 116 KiB so that one CTA holds an SM (each CTA
     // allocates 512 tensor-memory columns, the SM's whole tensor memory)
-    static constexpr size_t smem(bool split) {
-        const size_t n = 1024 + (size_t)bar_off(split) + 256;
-        return n < (116u << 10) ? (116u << 10) : n;
-    }
+    static constexpr size_t SMEM_NEED = 1024 + (size_t)BAR_OFF + 256;
+    static constexpr size_t SMEM = SMEM_NEED < (116u << 10) ? (116u << 10) : SMEM_NEED;
+    static_assert(SMEM <= 232448, "shared memory");
+    static_assert(kColO + 2 * D <= kTmemCols, "tensor memory columns");
 };
 
 // ------------------------------------------------------------ PTX helpers
@@ -102,14 +108,17 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
                  : "memory");
 }
 
+// One test of the phase; a thread whose phase is not complete is suspended
+// (up to the hint, 1 ms) until it completes, so waiting threads do not take
+// issue slots from the softmax warps beside them.
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
     uint32_t done;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(done)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(1000000u)
         : "memory");
     return done != 0;
 }
@@ -121,7 +130,8 @@ __device__ __forceinline__ uint64_t global_ns() {
 }
 
 // Wait for the phase of `bar` with the given parity.  Gives up (false) after
-// 1 s, after kWaitLimitIters polls, or once *abort is set (when given).
+// 1 s, after kWaitLimitIters tests, or once *abort is set (when given; a
+// suspended test notices it after its hint at the latest).
 __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int* abort) {
     const uint64_t t0 = global_ns();
     for (uint32_t it = 1; it < kWaitLimitIters; ++it) {
@@ -215,6 +225,30 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         : "memory");
 }
 
+// 64 consecutive columns of this warp's lanes, load and wait in one statement.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+        "%28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, "
+        "%45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, "
+        "%62, %63}, [%64];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]),
+          "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]),
+          "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]),
+          "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]),
+          "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]),
+          "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        : "r"(taddr)
+        : "memory");
+}
+
 // Store 32 columns of this warp's lanes and wait for the store to complete.
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
@@ -234,25 +268,6 @@ __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
-}
-
-// One column of this warp's lanes, stored (and waited for) / loaded.
-__device__ __forceinline__ void tmem_st1(uint32_t taddr, float v) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};\n\t"
-        "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
-        "r"(__float_as_uint(v))
-        : "memory");
-}
-__device__ __forceinline__ float tmem_ld1(uint32_t taddr) {
-    uint32_t v;
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];\n\t"
-        "tcgen05.wait::ld.sync.aligned;"
-        : "=r"(v)
-        : "r"(taddr)
-        : "memory");
-    return __uint_as_float(v);
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
@@ -304,7 +319,7 @@ struct PrefillArgs {
     const int32_t* query_start;
     float scale_log2;
     int S, H, B, max_blocks, max_query_len, num_tokens;
-    int q_tiles;             // query tiles per sequence: ceil(max_query_len / kBM)
+    int q_items;             // work items per sequence: ceil(max_query_len / kRows)
     int64_t num_blocks;
     int32_t* err;
 };
@@ -313,32 +328,41 @@ struct PrefillArgs {
 enum : int {
     kBarQFull = 0,
     kBarQEmpty = 1,
-    kBarKFull = 2,    // + stage
-    kBarKEmpty = 4,   // + stage
-    kBarVFull = 6,    // + stage
-    kBarVEmpty = 8,   // + stage
-    kBarSFull = 10,   // + buffer
-    kBarPFull = 12,
-    kBarPvDone = 13,
-    kBarMmaDone = 14,
-    kBarXch = 15,     // + lane quarter: the two softmax warps of a quarter
-    kBarCount = 19
+    kBarKFull = 2,    // + stage (up to 4)
+    kBarKEmpty = 6,   // + stage
+    kBarVFull = 10,   // + stage
+    kBarVEmpty = 14,  // + stage
+    kBarSFull = 18,   // + 2 group + buffer
+    kBarPFull = 22,   // + group
+    kBarPvDone = 24,  // + group
+    kBarMmaDone = 26,
+    kBarCount = 27
 };
 
-// One work item: 128 query rows of one (sequence, head).
+// One work item: 256 query rows (tiles A and B) of one (sequence, head).
 struct Item {
-    int s, h, q0, qlen, ctx, q_begin, rows, pos0, n_tiles;
+    int s, h, q0, qlen, ctx, q_begin;
+    int rows[2], pos0[2], n[2];      // per tile: rows, first position, key tiles
+    int n_kv;                        // key tiles loaded: the larger of n[0], n[1]
 };
 
-// Work items in longest-first order: index w -> query tile q_tiles-1 - w/(S H),
-// then sequence, then head.  False for an empty item (past the sequence's
-// query rows) or a sequence whose lengths are out of range (flagged once).
+// Work items: (sequence, head) pairs in groups of kGroupPairs, and within a
+// group longest first (item q_items-1 down to 0, then pair), so that the CTAs
+// running at one time share the K/V of few pairs in L2.  False for an empty
+// item (past the sequence's query rows) or a sequence whose lengths are out
+// of range (flagged once).
+constexpr int kGroupPairs = 16;
 __device__ __forceinline__ bool item_at(const PrefillArgs& a, int64_t w, bool flag, Item& it) {
     const int64_t sh = (int64_t)a.S * a.H;
-    const int t = a.q_tiles - 1 - (int)(w / sh);
-    const int64_t rem = w - (w / sh) * sh;
-    it.s = (int)(rem / a.H);
-    it.h = (int)(rem - (int64_t)it.s * a.H);
+    const int64_t per_group = (int64_t)a.q_items * kGroupPairs;
+    const int64_t grp = w / per_group;
+    const int64_t r = w - grp * per_group;
+    const int64_t first = grp * kGroupPairs;
+    const int gs = (int)(sh - first < kGroupPairs ? sh - first : kGroupPairs);
+    const int t = a.q_items - 1 - (int)(r / gs);
+    const int64_t pair = first + r % gs;
+    it.s = (int)(pair / a.H);
+    it.h = (int)(pair - (int64_t)it.s * a.H);
     it.q0 = a.query_start[it.s];
     it.qlen = a.query_start[it.s + 1] - it.q0;
     it.ctx = a.context_lens[it.s];
@@ -348,12 +372,16 @@ __device__ __forceinline__ bool item_at(const PrefillArgs& a, int64_t w, bool fl
         return false;
     }
     if (flag && t == 0 && it.h == 0 && it.qlen > a.max_query_len)
-        atomicOr(a.err, PKV_DEVERR_BAD_CONTEXT);     // rows past the last tile stay unwritten
-    it.q_begin = t * kBM;
+        atomicOr(a.err, PKV_DEVERR_BAD_CONTEXT);     // rows past the last item stay unwritten
+    it.q_begin = t * kRows;
     if (it.q_begin >= it.qlen) return false;
-    it.rows = min(kBM, it.qlen - it.q_begin);
-    it.pos0 = it.ctx - it.qlen + it.q_begin;         // position of the item's first query
-    it.n_tiles = (it.pos0 + it.rows - 1) / kBN + 1;  // key tiles up to the causal limit
+    for (int x = 0; x < 2; ++x) {
+        const int b = it.q_begin + x * kBM;
+        it.rows[x] = it.qlen - b < kBM ? (it.qlen - b > 0 ? it.qlen - b : 0) : kBM;
+        it.pos0[x] = it.ctx - it.qlen + b;           // position of the tile's first query
+        it.n[x] = it.rows[x] > 0 ? (it.pos0[x] + it.rows[x] - 1) / kBN + 1 : 0;
+    }
+    it.n_kv = it.n[1] > it.n[0] ? it.n[1] : it.n[0];
     return true;
 }
 
@@ -362,28 +390,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     paged_prefill_tc(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const PrefillArgs a) {
-    using C = PCfg<D>;
     constexpr bool kSplit = Pk<T>::kSplit;
+    using C = PCfg<D, kSplit>;
+    constexpr int NST = C::NST;
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;                 // 1024-aligned
     unsigned char* gbase = smem_raw + (base - raw);               // same, generic
     const uint32_t sQ = base + C::Q_OFF, sK = base + C::K_OFF, sV = base + C::V_OFF;
     const uint32_t sP = base + C::P_OFF, sPlo = base + C::PLO_OFF;
-    const uint32_t bars = base + C::bar_off(kSplit);
+    const uint32_t bars = base + C::BAR_OFF;
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::bar_off(kSplit) + 8 * kBarCount);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::BAR_OFF + 8 * kBarCount);
     volatile int* abort_flag =
-        reinterpret_cast<volatile int*>(gbase + C::bar_off(kSplit) + 8 * kBarCount + 4);
+        reinterpret_cast<volatile int*>(gbase + C::BAR_OFF + 8 * kBarCount + 4);
 
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int64_t n_items = (int64_t)a.q_tiles * a.S * a.H;
+    const int64_t n_items = (int64_t)a.q_items * a.S * a.H;
     const int64_t w0 = blockIdx.x, dw = gridDim.x;
 
     if (tid == 0) {
         for (int i = 0; i < kBarCount; ++i)
-            mbar_init(bar(i), i == kBarPFull ? (uint32_t)kSoftmaxThreads : i >= kBarXch ? 64u : 1u);
+            mbar_init(bar(i), (i == kBarPFull || i == kBarPFull + 1) ? 128u : 1u);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -406,8 +435,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0 || warp == kWarps - 1) {
         // ============================================ TMA producers
         // warp 0: the query tiles and the K tiles; the last warp: the V tiles.
-        // Both walk the same items and the same global tile sequence g; tile g
-        // uses stage g & 1 of its ring.
+        // Both walk the same items and the same global key-tile sequence g;
+        // tile g uses stage g % NST of its ring.
         const bool kq = warp == 0;
         if (lane == 0) {
             const CUtensorMap* map = kq ? &tm_k : &tm_v;
@@ -420,22 +449,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 Item it;
                 if (!item_at(a, w, false, it)) continue;
                 if (kq) {
-                    // the query tile, once the previous item's S products are done
+                    // both query tiles, once the previous item's S products are done
                     if (items > 0 && !mbar_wait(bar(kBarQEmpty), (items - 1) & 1, abort_flag)) {
                         ok = false;
                         break;
                     }
-                    mbar_expect_tx(bar(kBarQFull), (uint32_t)(C::SLABS * C::SLAB_Q));
-                    for (int sl = 0; sl < C::SLABS; ++sl)
-                        tma_3d(sQ + sl * C::SLAB_Q, &tm_q, sl * 64, it.h, it.q0 + it.q_begin,
-                               bar(kBarQFull));
+                    mbar_expect_tx(bar(kBarQFull), (uint32_t)(2 * C::Q_BYTES));
+                    for (int x = 0; x < 2; ++x)
+                        for (int sl = 0; sl < C::SLABS; ++sl)
+                            tma_3d(sQ + x * C::Q_BYTES + sl * C::SLAB_Q, &tm_q, sl * 64, it.h,
+                                   it.q0 + it.q_begin + x * kBM, bar(kBarQFull));
                 }
                 ++items;
                 const int32_t* row_tab = a.block_tables + (int64_t)it.s * a.max_blocks;
-                for (int j = 0; j < it.n_tiles; ++j, ++g) {
-                    const int st = (int)(g & 1);
-                    if (g >= 2 &&
-                        !mbar_wait(bar(empty0 + st), (uint32_t)(((g >> 1) - 1) & 1), abort_flag)) {
+                for (int j = 0; j < it.n_kv; ++j, ++g) {
+                    const int st = (int)(g % NST);
+                    if (g >= NST &&
+                        !mbar_wait(bar(empty0 + st), (uint32_t)((g / NST - 1) & 1), abort_flag)) {
                         ok = false;
                         break;
                     }
@@ -461,8 +491,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (*abort_flag) {
                 // let the copies in flight land before the CTA can exit
                 if (kq && items > 0) mbar_wait(bar(kBarQFull), (items - 1) & 1, nullptr);
-                for (int64_t t = g - 2 < 0 ? 0 : g - 2; t < g; ++t)
-                    mbar_wait(bar(full0 + (int)(t & 1)), (uint32_t)((t >> 1) & 1), nullptr);
+                for (int64_t t = g - NST < 0 ? 0 : g - NST; t < g; ++t)
+                    mbar_wait(bar(full0 + (int)(t % NST)), (uint32_t)((t / NST) & 1), nullptr);
             }
         }
     } else if (warp == 1) {
@@ -470,35 +500,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             constexpr uint32_t ID_S = idesc(Pk<T>::kType, false, kBN, kBM);
             constexpr uint32_t ID_PV = idesc(Pk<T>::kType, true, D, kBM);
-            // S_g for global tile g (j = its index in the item, item = the
-            // item count); the last S of an item frees the query buffer
-            auto issue_s = [&](int64_t g, int j, int n_tiles, int item) -> bool {
+            // descriptors of each buffer's start, computed once; an operand's
+            // descriptor is its buffer's plus the (16-byte unit) offset, which
+            // never carries out of the 14-bit address field (addresses stay
+            // below 256 KiB)
+            const uint64_t dQ = sdesc(sQ, 16, 1024), dK = sdesc(sK, 16, 1024);
+            const uint64_t dP = sdesc(sP, 16, 1024), dPlo = sdesc(sPlo, 16, 1024);
+            const uint64_t dV = sdesc(sV, C::SLAB_KV, 1024);
+            // S products of key tile j of an item (global key tile gk): for
+            // each group whose rows reach the tile, into its next S buffer
+            int64_t gsx[2] = {0, 0};         // S products issued per group
+            auto issue_s = [&](const Item& it, int j, int64_t gk, int item) -> bool {
                 if (j == 0 && !mbar_wait(bar(kBarQFull), (uint32_t)(item & 1), abort_flag))
                     return false;
-                const int st = (int)(g & 1);
-                if (!mbar_wait(bar(kBarKFull + st), (uint32_t)((g >> 1) & 1), abort_flag))
+                const int st = (int)(gk % NST);
+                if (!mbar_wait(bar(kBarKFull + st), (uint32_t)((gk / NST) & 1), abort_flag))
                     return false;
                 tc_fence_after();
-                const uint32_t d = tmem + (uint32_t)st * kBN;
+                const uint64_t dk = dK + (uint64_t)((st * C::KV_BYTES) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (uint32_t)(kk >> 2) * C::SLAB_Q + (uint32_t)(kk & 3) * 32u;
-                    const uint32_t koff =
-                        (uint32_t)(kk >> 2) * C::SLAB_KV + (uint32_t)(kk & 3) * 32u;
-                    umma(d, sdesc(sQ + off, 16, 1024),
-                         sdesc(sK + st * C::KV_BYTES + koff, 16, 1024), ID_S, kk > 0);
+                for (int x = 0; x < 2; ++x) {
+                    if (j >= it.n[x]) continue;
+                    const int b = (int)(gsx[x] & 1);
+                    const uint32_t d = tmem + kColS + (uint32_t)(2 * x + b) * kBN;
+                    const uint64_t dq = dQ + (uint64_t)((x * C::Q_BYTES) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t qo = ((kk >> 2) * C::SLAB_Q + (kk & 3) * 32) >> 4;
+                        const uint32_t ko = ((kk >> 2) * C::SLAB_KV + (kk & 3) * 32) >> 4;
+                        umma(d, dq + qo, dk + ko, ID_S, kk > 0);
+                    }
+                    umma_commit(bar(kBarSFull + 2 * x + b));
+                    ++gsx[x];
                 }
-                umma_commit(bar(kBarSFull + st));
                 umma_commit(bar(kBarKEmpty + st));
-                if (j == n_tiles - 1) umma_commit(bar(kBarQEmpty));
+                if (j == it.n_kv - 1) umma_commit(bar(kBarQEmpty));
                 return true;
             };
-            // S runs up to two tiles ahead of P V, across item boundaries: a
-            // cursor (item, tile) over the same sequence the others walk
-            int64_t sw = w0;                 // item of the next S
+            // S runs up to two key tiles ahead of P V, across item boundaries:
+            // a cursor (item, tile) over the same sequence the others walk
+            int64_t sw = w0;
             Item sit;
-            int sj = 0, sitem = 0;           // tile within it, item count
-            int64_t gs = 0;                  // global index of the next S
+            int sj = 0, sitem = 0;
+            int64_t gs = 0;
             bool s_has = false;
             auto s_next_item = [&]() {
                 s_has = false;
@@ -514,9 +558,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             auto s_issue_one = [&]() -> bool {
                 if (!s_has) return true;
-                if (!issue_s(gs, sj, sit.n_tiles, sitem)) return false;
+                if (!issue_s(sit, sj, gs, sitem)) return false;
                 ++gs;
-                if (++sj == sit.n_tiles) {
+                if (++sj == sit.n_kv) {
                     ++sitem;
                     s_next_item();
                 }
@@ -525,33 +569,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             s_next_item();
             bool ok = s_issue_one() && s_issue_one();
             int64_t g = 0;
+            int64_t gpx[2] = {0, 0};         // P V products issued per group
             for (int64_t w = w0; ok && w < n_items; w += dw) {
                 Item it;
                 if (!item_at(a, w, false, it)) continue;
-                for (int j = 0; j < it.n_tiles; ++j, ++g) {
-                    if (!mbar_wait(bar(kBarPFull), (uint32_t)(g & 1), abort_flag)) {
+                for (int j = 0; j < it.n_kv; ++j, ++g) {
+                    const int st = (int)(g % NST);
+                    if (!mbar_wait(bar(kBarVFull + st), (uint32_t)((g / NST) & 1), abort_flag)) {
                         ok = false;
                         break;
                     }
-                    tc_fence_after();
-                    const int st = (int)(g & 1);
-                    if (!mbar_wait(bar(kBarVFull + st), (uint32_t)((g >> 1) & 1), abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t vst = sV + st * C::KV_BYTES;
+                    const uint64_t dv = dV + (uint64_t)((st * C::KV_BYTES) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < kBN / 16; ++kk) {
-                        const uint32_t poff =
-                            (uint32_t)(kk >> 2) * C::SLAB_P + (uint32_t)(kk & 3) * 32u;
-                        const uint64_t vd = sdesc(vst + (uint32_t)kk * 2048u, C::SLAB_KV, 1024);
-                        umma(tmem + kColO, sdesc(sP + poff, 16, 1024), vd, ID_PV,
-                             (j > 0 || kk > 0));
-                        if constexpr (kSplit)
-                            umma(tmem + kColO, sdesc(sPlo + poff, 16, 1024), vd, ID_PV, 1u);
+                    for (int x = 0; x < 2; ++x) {
+                        if (!ok || j >= it.n[x]) continue;
+                        if (!mbar_wait(bar(kBarPFull + x), (uint32_t)(gpx[x] & 1), abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint64_t dp = dP + (uint64_t)((x * C::P_BYTES) >> 4);
+                        const uint64_t dplo = dPlo + (uint64_t)((x * C::P_BYTES) >> 4);
+#pragma unroll
+                        for (int kk = 0; kk < kBN / 16; ++kk) {
+                            const uint64_t vd = dv + (uint64_t)((kk * 2048) >> 4);
+                            umma(tmem + kColO + x * D, dp + (uint64_t)((kk * 32) >> 4), vd, ID_PV,
+                                 (j > 0 || kk > 0));
+                            if constexpr (kSplit)
+                                umma(tmem + kColO + x * D, dplo + (uint64_t)((kk * 32) >> 4), vd,
+                                     ID_PV, 1u);
+                        }
+                        umma_commit(bar(kBarPvDone + x));
+                        ++gpx[x];
                     }
+                    if (!ok) break;
                     umma_commit(bar(kBarVEmpty + st));
-                    umma_commit(bar(kBarPvDone));
                     if (!s_issue_one()) {
                         ok = false;
                         break;
@@ -565,120 +617,88 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ======================================================= softmax
-        // Warps 2..9.  Warps w and w + 4 share a lane quarter (the rows
-        // 32 (w % 4) .. + 31) and split the keys of each tile: half 0 takes
-        // keys 0..63 (P slab 0) and O's first D/2 columns, half 1 the rest.
-        // The two agree on the running max through tensor memory once per tile.
+        // Warps 2..5: tile A, warps 6..9: tile B; one row per thread (warp w
+        // reaches the lanes 32 (w % 4) .. + 31 of tensor memory).
+        const int x = (warp - 2) >> 2;               // group: tile A (0) or B (1)
         const int q4 = warp & 3;                     // this warp's lane quarter
-        const int half = (warp - 2) >> 2;
-        const int row = q4 * 32 + lane;              // query row of the item = TMEM lane
+        const int row = q4 * 32 + lane;              // row of the tile = TMEM lane
+        const int gtid = (warp - 2 - 4 * x) * 32 + lane;   // 0..127 within the group
         const uint32_t tl = tmem + ((uint32_t)(q4 * 32) << 16);
-        const int stid = tid - 64;                   // 0..255 among the softmax threads
-        const uint32_t xbar = bar(kBarXch + q4);     // the two warps' exchange barrier
-        int xphase = 0;
-        // publish v in this half's slot, wait for the other half, return its value
-        auto exchange = [&](float v, int slot_self, int slot_other, float& other) -> bool {
-            tmem_st1(tl + kColX + (uint32_t)slot_self, v);
-            tc_fence_before();
-            mbar_arrive(xbar);
-            const bool got = mbar_wait(xbar, (uint32_t)(xphase & 1), abort_flag);
-            ++xphase;
-            if (!got) return false;
-            tc_fence_after();
-            other = tmem_ld1(tl + kColX + (uint32_t)slot_other);
-            return true;
-        };
+        const uint32_t tO = tl + kColO + (uint32_t)(x * D);
+        const uint32_t pbase = sP + x * C::P_BYTES, plobase = sPlo + x * C::P_BYTES;
         const float sl2 = a.scale_log2;
         const bool pos_scale = sl2 >= 0.f;
         bool ok = true;
-        int64_t g = 0;
+        int64_t gx = 0;                              // this group's tiles so far
+        int64_t g = 0;                               // key tiles so far (V stage)
         for (int64_t w = w0; ok && w < n_items; w += dw) {
             Item it;
             if (!item_at(a, w, false, it)) continue;
-            const int qpos = it.pos0 + row;          // causal limit of the row
-            float m = -INFINITY, l = 0.f;            // l: this half's share of the row sum
-            for (int j = 0; j < it.n_tiles; ++j, ++g) {
-                const int st = (int)(g & 1);
-                if (!mbar_wait(bar(kBarSFull + st), (uint32_t)((g >> 1) & 1), abort_flag)) {
+            const int nx = x ? it.n[1] : it.n[0];
+            const int pos0 = x ? it.pos0[1] : it.pos0[0];
+            const int rows = x ? it.rows[1] : it.rows[0];
+            // the group that zeroes V rows past the context (only the item's
+            // last key tile has any): the first group whose rows reach that
+            // tile, since its P V is issued before the other's
+            const bool a_last = it.n[0] == it.n_kv;
+            const bool zeroer = x == 0 ? a_last : !a_last;
+            const int qpos = pos0 + row;             // causal limit of the row
+            float m = -INFINITY, l = 0.f;
+            for (int j = 0; j < nx; ++j, ++gx) {
+                const int b = (int)(gx & 1);
+                if (!mbar_wait(bar(kBarSFull + 2 * x + b), (uint32_t)((gx >> 1) & 1), abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t sb = tl + (uint32_t)st * kBN + (uint32_t)half * 64;
-                const int kb = j * kBN + half * 64;      // first key of this half
-                const bool full = kb + 63 <= it.pos0;    // every key visible to every row
-                // row max of this half (scaled scores; masked keys excluded)
+                uint32_t r[64];
+                tmem_ld64(tl + kColS + (uint32_t)(2 * x + b) * kBN, r);
+                const int kb = j * kBN;
+                const bool full = kb + kBN - 1 <= pos0;   // every key visible to every row
                 float mx = -INFINITY;
                 if (full) {
                     float ext = pos_scale ? -INFINITY : INFINITY;
+                    if (pos_scale) {
 #pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        uint32_t r[32];
-                        tmem_ld32(sb + c * 32, r);
-                        if (pos_scale) {
+                        for (int e = 0; e < 64; ++e) ext = fmaxf(ext, __uint_as_float(r[e]));
+                    } else {
 #pragma unroll
-                            for (int e = 0; e < 32; ++e) ext = fmaxf(ext, __uint_as_float(r[e]));
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 32; ++e) ext = fminf(ext, __uint_as_float(r[e]));
-                        }
+                        for (int e = 0; e < 64; ++e) ext = fminf(ext, __uint_as_float(r[e]));
                     }
                     mx = ext * sl2;
                 } else {
 #pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        uint32_t r[32];
-                        tmem_ld32(sb + c * 32, r);
-#pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            if (kb + c * 32 + e <= qpos)
-                                mx = fmaxf(mx, __uint_as_float(r[e]) * sl2);
-                    }
-                }
-                {
-                    // slots alternate with the exchange parity, so a slot is
-                    // rewritten only after the other half has passed the next one
-                    float other;
-                    const int par = xphase & 1;
-                    if (!exchange(mx, half * 2 + par, (half ^ 1) * 2 + par, other)) {
-                        ok = false;
-                        break;
-                    }
-                    mx = fmaxf(mx, other);
+                    for (int e = 0; e < 64; ++e)
+                        if (kb + e <= qpos) mx = fmaxf(mx, __uint_as_float(r[e]) * sl2);
                 }
                 float m_new = m;
                 if (mx > m + kRescaleLog2 || (m == -INFINITY && mx > -INFINITY)) m_new = mx;
                 const bool rescale = j > 0 && m_new != m;
                 const float alpha = rescale ? ex2(m - m_new) : 1.f;
-                // weights of this half, packed to 16 bits (and the bf16 residual)
+                // weights, packed to 16 bits (and the bf16 residual)
                 uint32_t pk[32];
                 uint32_t pr[kSplit ? 32 : 1];
-                float rs = 0.f;
+                float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(sb + c * 32, r);
-#pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        float p0 = ex2(fmaf(__uint_as_float(r[e]), sl2, -m_new));
-                        float p1 = ex2(fmaf(__uint_as_float(r[e + 1]), sl2, -m_new));
-                        if (!full) {
-                            const int k0 = kb + c * 32 + e;
-                            p0 = k0 <= qpos ? p0 : 0.f;
-                            p1 = k0 + 1 <= qpos ? p1 : 0.f;
-                        }
-                        rs += p0 + p1;
-                        uint32_t res;
-                        pk[(c * 32 + e) >> 1] = Pk<T>::pack(p0, p1, res);
-                        if constexpr (kSplit) pr[(c * 32 + e) >> 1] = res;
+                for (int e = 0; e < 64; e += 2) {
+                    float p0 = ex2(fmaf(__uint_as_float(r[e]), sl2, -m_new));
+                    float p1 = ex2(fmaf(__uint_as_float(r[e + 1]), sl2, -m_new));
+                    if (!full) {
+                        p0 = kb + e <= qpos ? p0 : 0.f;
+                        p1 = kb + e + 1 <= qpos ? p1 : 0.f;
                     }
+                    rs0 += p0;
+                    rs1 += p1;
+                    uint32_t res;
+                    pk[e >> 1] = Pk<T>::pack(p0, p1, res);
+                    if constexpr (kSplit) pr[e >> 1] = res;
                 }
-                l = l * alpha + rs;
+                l = l * alpha + (rs0 + rs1);
                 m = m_new;
-                // P's buffer and O are free once the previous P V has completed
-                // (for an item's first tile the previous item's end waited)
+                // P's buffer and O are free once this group's previous P V has
+                // completed (for an item's first tile the previous item's end waited)
                 if (j > 0) {
-                    if (!mbar_wait(bar(kBarPvDone), (uint32_t)((g - 1) & 1), abort_flag)) {
+                    if (!mbar_wait(bar(kBarPvDone + x), (uint32_t)((gx - 1) & 1), abort_flag)) {
                         ok = false;
                         break;
                     }
@@ -686,72 +706,70 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 // V rows past the context (partial last block, blocks never
                 // loaded) are zeroed: their weights are 0, but 0 * NaN would not be
-                const int kbase = j * kBN;
-                if (kbase + kBN > it.ctx) {
-                    if (!mbar_wait(bar(kBarVFull + st), (uint32_t)((g >> 1) & 1), abort_flag)) {
+                const int64_t gk = g + j;
+                if (zeroer && kb + kBN > it.ctx) {
+                    const int st = (int)(gk % NST);
+                    if (!mbar_wait(bar(kBarVFull + st), (uint32_t)((gk / NST) & 1), abort_flag)) {
                         ok = false;
                         break;
                     }
-                    const int z0 = it.ctx - kbase > 0 ? it.ctx - kbase : 0;
+                    const int z0 = it.ctx - kb > 0 ? it.ctx - kb : 0;
                     const int n16 = (kBN - z0) * 8;       // 16-byte chunks per slab
                     unsigned char* vs = gbase + C::V_OFF + st * C::KV_BYTES;
-                    for (int i = stid; i < n16 * C::SLABS; i += kSoftmaxThreads) {
+                    for (int i = gtid; i < n16 * C::SLABS; i += 128) {
                         const int sl = i / n16, wv = i - sl * n16;
                         *reinterpret_cast<uint4*>(vs + sl * C::SLAB_KV + (z0 * 128) + wv * 16) =
                             make_uint4(0u, 0u, 0u, 0u);
                     }
                 }
-                // this half of the P row -> P slab `half` (K-major, 128-byte swizzle)
+                // the P row -> P_X (K-major, 128-byte swizzle)
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch) {
-                    const uint32_t off = (uint32_t)half * C::SLAB_P + (uint32_t)row * 128u +
-                                         ((uint32_t)(ch ^ (row & 7)) << 4);
-                    st_shared_v4(sP + off, pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2],
+                    const uint32_t off = (uint32_t)row * 128u + ((uint32_t)(ch ^ (row & 7)) << 4);
+                    st_shared_v4(pbase + off, pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2],
                                  pk[4 * ch + 3]);
                     if constexpr (kSplit)
-                        st_shared_v4(sPlo + off, pr[4 * ch], pr[4 * ch + 1], pr[4 * ch + 2],
+                        st_shared_v4(plobase + off, pr[4 * ch], pr[4 * ch + 1], pr[4 * ch + 2],
                                      pr[4 * ch + 3]);
                 }
-                // O *= alpha for rows whose running max rose: this half's columns
+                // O *= alpha for rows whose running max rose (warp-wide access)
                 if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-                    for (int c = 0; c < D / 64; ++c) {
-                        const uint32_t ta = tl + kColO + (uint32_t)(half * (D / 2) + c * 32);
-                        uint32_t r[32];
-                        tmem_ld32(ta, r);
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + c * 32, o);
 #pragma unroll
                         for (int e = 0; e < 32; ++e)
-                            r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-                        tmem_st32(ta, r);
+                            o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tmem_st32(tO + c * 32, o);
                     }
                 }
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 tc_fence_before();
-                mbar_arrive(bar(kBarPFull));
+                mbar_arrive(bar(kBarPFull + x));
             }
             if (!ok) break;
-            // the two halves of the row sum, then the item's output rows
-            float other;
-            if (!exchange(l, 4 + half, 4 + (half ^ 1), other) ||
-                !mbar_wait(bar(kBarPvDone), (uint32_t)((g - 1) & 1), abort_flag)) {
+            g += it.n_kv;
+            if (nx == 0) continue;
+            // the item's output rows of this tile
+            if (!mbar_wait(bar(kBarPvDone + x), (uint32_t)((gx - 1) & 1), abort_flag)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            l += other;
             const float inv = l > 0.f ? 1.f / l : 0.f;
             T* orow = static_cast<T*>(a.out) +
-                      ((int64_t)(it.q0 + it.q_begin + row) * a.H + it.h) * D + half * (D / 2);
+                      ((int64_t)(it.q0 + it.q_begin + x * kBM + row) * a.H + it.h) * D;
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c) {
-                uint32_t r[32];
-                tmem_ld32(tl + kColO + (uint32_t)(half * (D / 2) + c * 32), r);
-                if (row < it.rows) {
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                tmem_ld32(tO + c * 32, o);
+                if (row < rows) {
                     uint32_t wv[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
-                        wv[e] = Pk<T>::pack_out(__uint_as_float(r[2 * e]) * inv,
-                                                __uint_as_float(r[2 * e + 1]) * inv);
+                        wv[e] = Pk<T>::pack_out(__uint_as_float(o[2 * e]) * inv,
+                                                __uint_as_float(o[2 * e + 1]) * inv);
                     uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
@@ -802,7 +820,7 @@ bool make_map(CUtensorMap* m, bool bf16, uint32_t rank, const void* gaddr, const
 template <typename T, int D>
 cudaError_t launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                            const PrefillArgs& a, cudaStream_t stream) {
-    const size_t smem = PCfg<D>::smem(Pk<T>::kSplit);
+    const size_t smem = PCfg<D, Pk<T>::kSplit>::SMEM;
     cudaError_t e = cudaFuncSetAttribute(paged_prefill_tc<T, D>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -815,7 +833,7 @@ cudaError_t launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const C
     int dev = 0;
     e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    const int64_t items = (int64_t)a.q_tiles * a.S * a.H;
+    const int64_t items = (int64_t)a.q_items * a.S * a.H;
     const int sms = pkv::sm_count(dev);
     if (sms < 1) return cudaErrorInvalidDevice;
     cfg.gridDim = dim3((unsigned)(items < sms ? items : sms));
@@ -902,7 +920,7 @@ pkv_status pkv_paged_attention_prefill(void* out, const void* q, const void* k_c
     a.max_blocks = max_blocks_per_seq;
     a.max_query_len = max_query_len;
     a.num_tokens = num_query_tokens;
-    a.q_tiles = (max_query_len + kBM - 1) / kBM;
+    a.q_items = (max_query_len + kRows - 1) / kRows;
     a.num_blocks = num_blocks;
     a.err = err;
     cudaError_t e;
