@@ -11,33 +11,34 @@
 //
 // Design.  Persistent CTAs, one per SM, walk the work items longest first;
 // an item is 256 query rows of one (sequence, head): two query tiles A and B
-// of 128 rows, one row per tensor-memory lane, that share every K/V tile.
-// Loads and products run ahead across item boundaries.  Eleven warps:
+// of 128 rows, one row per tensor-memory lane, that share every K/V tile of
+// 64 keys.  Eleven warps:
 //   warps 0, 10 TMA producers: the two query tiles of each item and the K
-//               tiles (warp 0), the V tiles (warp 10), 64 keys per tile, block
-//               by block through the block table (2-D tiled copies with the
-//               128-byte swizzle), each in a ring of 3-4 stages; a K stage is
-//               refilled once its S products are done, a V stage once its
-//               P V products are;
+//               tiles (warp 0), the V tiles (warp 10), block by block through
+//               the block table (2-D tiled copies with the 128-byte swizzle),
+//               each in a ring of four stages;
 //   warp 1      owns the tensor memory and issues the MMAs from one thread:
-//               S_X = Q_X K^T (X = A, B) into double-buffered 128 x 64 fp32
-//               accumulators, O_X += P_X V into 128 x D fp32 accumulators;
+//               S_X = Q_X K^T (X = A, B) into one of two 128 x 64 fp32
+//               buffers per group, and O_X += P_X V with P_X read from tensor
+//               memory, where the softmax wrote it over its S buffer; the S
+//               products run two key tiles ahead of the P V products;
 //   warps 2..5  softmax of tile A, warps 6..9 of tile B, one row per thread:
 //               read S from tensor memory, causal mask (diagonal tiles only),
-//               online softmax in log2 units, write P (16-bit) to shared
-//               memory in the MMA's operand layout, rescale O in tensor
-//               memory when the running max grows.
-// While one group's softmax runs, the tensor cores work on the other group's
-// products.  The running max is only raised when a row's max grows by more
+//               online softmax in log2 units, write P (16-bit, packed in
+//               pairs) back over S, rescale O when the running max grows.
+// The MMAs of one thread complete in issue order: S_X(j) complete means the
+// P V two tiles back is complete, so its buffer (now holding S_X(j)) may take
+// P_X(j).  The running max is only raised when a row's max grows by more
 // than 2^8 (the weights then stay below 256), so most tiles need no O
 // rescale; the result is the same softmax.  For bf16, P = high part +
 // residual (two products), so the weights keep about 16 bits.
 //
-// Operand layouts (shared memory, 1024-byte aligned atoms of 8 rows x 128 B,
-// 16-byte chunk c of row r stored at chunk c ^ (r % 8)):
-//   Q, K: K-major (row = token, 64 elements of the head dimension per slab);
-//   P:    K-major (row = query, the tile's 64 keys);
-//   V:    the same bytes as K, read as an MN-major operand (N = head dimension).
+// Operand layouts: Q, K in shared memory K-major (row = token, 64 elements
+// of the head dimension per 128-byte slab, 1024-byte atoms of 8 rows, 16-byte
+// chunk c of row r at chunk c ^ (r % 8)); V the same bytes read as an
+// MN-major operand (N = head dimension); P in tensor memory, row = lane, keys
+// 2c and 2c + 1 of the tile in column c of the S buffer (bf16 residuals in
+// columns 32 + c).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -56,8 +57,8 @@ constexpr int kBN = 64;             // keys per K/V tile (MMA N of S, K of P V)
 constexpr int kWarps = 11;          // K producer, MMA issuer, 2 x 4 softmax warps, V producer
 constexpr int kThreads = kWarps * 32;
 constexpr uint32_t kTmemCols = 512;
-// tensor-memory columns: S of group X buffer b at kColS + (2X + b) kBN, O of
-// group X at kColO + X D
+// tensor-memory columns: S buffer b of group X (and P over it) at
+// kColS + (2X + b) kBN, O of group X at kColO + X D
 constexpr uint32_t kColS = 0;
 constexpr uint32_t kColO = 4 * kBN;
 constexpr float kRescaleLog2 = 8.f;  // raise the running max only past this growth
@@ -69,18 +70,13 @@ struct PCfg {
     static constexpr int SLABS = D / 64;               // 128-byte slabs per K/Q row
     static constexpr int SLAB_Q = kBM * 128;           // bytes of one Q slab (one tile)
     static constexpr int SLAB_KV = kBN * 128;          // bytes of one K (or V) slab
-    static constexpr int P_BYTES = kBM * kBN * 2;      // one group's P (one slab)
     static constexpr int Q_BYTES = SLABS * SLAB_Q;     // one tile's Q
     static constexpr int KV_BYTES = SLABS * SLAB_KV;
-    // K and V ring depth: as deep as shared memory allows (a K/V tile takes
-    // about as long to arrive as four tiles take to compute)
-    static constexpr int NST = (D == 128 && SPLIT) ? 3 : 4;
+    static constexpr int NST = 4;                      // K and V ring depth
     static constexpr int Q_OFF = 0;                    // Q_A, Q_B
     static constexpr int K_OFF = Q_OFF + 2 * Q_BYTES;
     static constexpr int V_OFF = K_OFF + NST * KV_BYTES;
-    static constexpr int P_OFF = V_OFF + NST * KV_BYTES;  // P_A, P_B
-    static constexpr int PLO_OFF = P_OFF + 2 * P_BYTES;   // bf16 residuals of P_A, P_B
-    static constexpr int BAR_OFF = PLO_OFF + (SPLIT ? 2 * P_BYTES : 0);
+    static constexpr int BAR_OFF = V_OFF + NST * KV_BYTES;
     // dynamic shared memory: 1 KiB of alignment slack, the buffers, 256 B of
     // barriers; never below 116 KiB so that one CTA holds an SM (each CTA
     // allocates 512 tensor-memory columns, the SM's whole tensor memory)
@@ -108,18 +104,30 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
                  : "memory");
 }
 
-// One test of the phase; a thread whose phase is not complete is suspended
-// (up to the hint, 1 ms) until it completes, so waiting threads do not take
-// issue slots from the softmax warps beside them.
+// One test of the phase.  With SUSPEND a thread whose phase is not complete
+// is suspended (up to the hint, 1 ms) until it completes, so waiting threads
+// do not take issue slots from the softmax warps beside them; without it the
+// test returns at once (for the MMA issuer, whose reaction time is on the
+// critical path).
+template <bool SUSPEND>
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
     uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(bar), "r"(parity), "r"(1000000u)
-        : "memory");
+    if (SUSPEND)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(bar), "r"(parity), "r"(1000000u)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(bar), "r"(parity)
+            : "memory");
     return done != 0;
 }
 
@@ -132,10 +140,11 @@ __device__ __forceinline__ uint64_t global_ns() {
 // Wait for the phase of `bar` with the given parity.  Gives up (false) after
 // 1 s, after kWaitLimitIters tests, or once *abort is set (when given; a
 // suspended test notices it after its hint at the latest).
+template <bool SUSPEND>
 __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int* abort) {
     const uint64_t t0 = global_ns();
     for (uint32_t it = 1; it < kWaitLimitIters; ++it) {
-        if (mbar_try(bar, parity)) return true;
+        if (mbar_try<SUSPEND>(bar, parity)) return true;
         if ((it & 31) == 0) {
             if (abort && *abort) return false;
             if (global_ns() - t0 > kWaitLimitNs) return false;
@@ -144,9 +153,10 @@ __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile i
     return false;
 }
 
+template <bool SUSPEND = true>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
-    if (mbar_try(bar, parity)) return true;
-    return wait_slow(bar, parity, abort);
+    if (mbar_try<SUSPEND>(bar, parity)) return true;
+    return wait_slow<SUSPEND>(bar, parity, abort);
 }
 
 // 2-D / 3-D tiled bulk tensor copies global -> shared, completion in bytes on `bar`.
@@ -189,6 +199,18 @@ __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, ui
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a), "l"(b), "r"(id), "r"(accumulate)
+        : "memory");
+}
+
+// The same with A read from tensor memory (M rows = lanes, K packed in pairs
+// along the columns).
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t id,
+                                        uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(id), "r"(accumulate)
         : "memory");
 }
 
@@ -268,13 +290,6 @@ __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
-}
-
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-                 "r"(d)
-                 : "memory");
 }
 
 // ------------------------------------------------------------ element types
@@ -398,7 +413,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t base = (raw + 1023u) & ~1023u;                 // 1024-aligned
     unsigned char* gbase = smem_raw + (base - raw);               // same, generic
     const uint32_t sQ = base + C::Q_OFF, sK = base + C::K_OFF, sV = base + C::V_OFF;
-    const uint32_t sP = base + C::P_OFF, sPlo = base + C::PLO_OFF;
     const uint32_t bars = base + C::BAR_OFF;
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::BAR_OFF + 8 * kBarCount);
@@ -505,7 +519,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             // never carries out of the 14-bit address field (addresses stay
             // below 256 KiB)
             const uint64_t dQ = sdesc(sQ, 16, 1024), dK = sdesc(sK, 16, 1024);
-            const uint64_t dP = sdesc(sP, 16, 1024), dPlo = sdesc(sPlo, 16, 1024);
             const uint64_t dV = sdesc(sV, C::SLAB_KV, 1024);
             // S products of key tile j of an item (global key tile gk): for
             // each group whose rows reach the tile, into its next S buffer
@@ -583,21 +596,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int x = 0; x < 2; ++x) {
                         if (!ok || j >= it.n[x]) continue;
-                        if (!mbar_wait(bar(kBarPFull + x), (uint32_t)(gpx[x] & 1), abort_flag)) {
+                        if (!mbar_wait<false>(bar(kBarPFull + x), (uint32_t)(gpx[x] & 1), abort_flag)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        const uint64_t dp = dP + (uint64_t)((x * C::P_BYTES) >> 4);
-                        const uint64_t dplo = dPlo + (uint64_t)((x * C::P_BYTES) >> 4);
+                        // P_X(j) over the S buffer of the group's tile
+                        const uint32_t pa =
+                            tmem + kColS + (uint32_t)(2 * x + (int)(gpx[x] & 1)) * kBN;
 #pragma unroll
                         for (int kk = 0; kk < kBN / 16; ++kk) {
                             const uint64_t vd = dv + (uint64_t)((kk * 2048) >> 4);
-                            umma(tmem + kColO + x * D, dp + (uint64_t)((kk * 32) >> 4), vd, ID_PV,
-                                 (j > 0 || kk > 0));
+                            umma_ts(tmem + kColO + x * D, pa + (uint32_t)(kk * 8), vd, ID_PV,
+                                    (j > 0 || kk > 0));
                             if constexpr (kSplit)
-                                umma(tmem + kColO + x * D, dplo + (uint64_t)((kk * 32) >> 4), vd,
-                                     ID_PV, 1u);
+                                umma_ts(tmem + kColO + x * D, pa + (uint32_t)(32 + kk * 8), vd,
+                                        ID_PV, 1u);
                         }
                         umma_commit(bar(kBarPvDone + x));
                         ++gpx[x];
@@ -625,7 +639,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int gtid = (warp - 2 - 4 * x) * 32 + lane;   // 0..127 within the group
         const uint32_t tl = tmem + ((uint32_t)(q4 * 32) << 16);
         const uint32_t tO = tl + kColO + (uint32_t)(x * D);
-        const uint32_t pbase = sP + x * C::P_BYTES, plobase = sPlo + x * C::P_BYTES;
         const float sl2 = a.scale_log2;
         const bool pos_scale = sl2 >= 0.f;
         bool ok = true;
@@ -651,8 +664,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
+                const uint32_t tS = tl + kColS + (uint32_t)(2 * x + b) * kBN;
                 uint32_t r[64];
-                tmem_ld64(tl + kColS + (uint32_t)(2 * x + b) * kBN, r);
+                tmem_ld64(tS, r);
                 const int kb = j * kBN;
                 const bool full = kb + kBN - 1 <= pos0;   // every key visible to every row
                 float mx = -INFINITY;
@@ -695,14 +709,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 l = l * alpha + (rs0 + rs1);
                 m = m_new;
-                // P's buffer and O are free once this group's previous P V has
-                // completed (for an item's first tile the previous item's end waited)
+                // P over this tile's S buffer (its scores are in registers)
+                tmem_st32(tS, pk);
+                if constexpr (kSplit) tmem_st32(tS + 32, pr);
+                // The previous P V must be complete before O is rescaled, and
+                // before this tile's P is announced: the MMA issuer has then
+                // taken the previous announcement, so the barrier never runs two
+                // phases ahead of it (a phase parity would then be ambiguous).
+                // S_X(j) complete already implies the P V before that one.
                 if (j > 0) {
                     if (!mbar_wait(bar(kBarPvDone + x), (uint32_t)((gx - 1) & 1), abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
+                }
+                // O_X *= alpha for rows whose running max rose (warp-wide access)
+                if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + c * 32, o);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tmem_st32(tO + c * 32, o);
+                    }
                 }
                 // V rows past the context (partial last block, blocks never
                 // loaded) are zeroed: their weights are 0, but 0 * NaN would not be
@@ -721,37 +753,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         *reinterpret_cast<uint4*>(vs + sl * C::SLAB_KV + (z0 * 128) + wv * 16) =
                             make_uint4(0u, 0u, 0u, 0u);
                     }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 }
-                // the P row -> P_X (K-major, 128-byte swizzle)
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    const uint32_t off = (uint32_t)row * 128u + ((uint32_t)(ch ^ (row & 7)) << 4);
-                    st_shared_v4(pbase + off, pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2],
-                                 pk[4 * ch + 3]);
-                    if constexpr (kSplit)
-                        st_shared_v4(plobase + off, pr[4 * ch], pr[4 * ch + 1], pr[4 * ch + 2],
-                                     pr[4 * ch + 3]);
-                }
-                // O *= alpha for rows whose running max rose (warp-wide access)
-                if (__any_sync(0xffffffffu, rescale)) {
-#pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t o[32];
-                        tmem_ld32(tO + c * 32, o);
-#pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                        tmem_st32(tO + c * 32, o);
-                    }
-                }
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 tc_fence_before();
                 mbar_arrive(bar(kBarPFull + x));
             }
             if (!ok) break;
             g += it.n_kv;
             if (nx == 0) continue;
-            // the item's output rows of this tile
+            // the item's output rows of this tile, once its last P V is done
             if (!mbar_wait(bar(kBarPvDone + x), (uint32_t)((gx - 1) & 1), abort_flag)) {
                 ok = false;
                 break;
