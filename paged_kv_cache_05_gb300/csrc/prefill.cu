@@ -12,33 +12,33 @@
 // Design.  Persistent CTAs, one per SM, walk the work items longest first;
 // an item is 256 query rows of one (sequence, head): two query tiles A and B
 // of 128 rows, one row per tensor-memory lane, that share every K/V tile of
-// 64 keys.  Eleven warps:
+// 128 keys.  Eleven warps:
 //   warps 0, 10 TMA producers: the two query tiles of each item and the K
 //               tiles (warp 0), the V tiles (warp 10), block by block through
 //               the block table (2-D tiled copies with the 128-byte swizzle),
-//               each in a ring of four stages;
+//               each in a ring of 2-4 stages;
 //   warp 1      owns the tensor memory and issues the MMAs from one thread:
-//               S_X = Q_X K^T (X = A, B) into one of two 128 x 64 fp32
-//               buffers per group, and O_X += P_X V with P_X read from tensor
-//               memory, where the softmax wrote it over its S buffer; the S
-//               products run two key tiles ahead of the P V products;
+//               S_X = Q_X K^T (X = A, B; 128 x 128 fp32 in tensor memory) and
+//               O_X += P_X V with P_X read from tensor memory, where the
+//               softmax wrote it over S_X;
 //   warps 2..5  softmax of tile A, warps 6..9 of tile B, one row per thread:
 //               read S from tensor memory, causal mask (diagonal tiles only),
 //               online softmax in log2 units, write P (16-bit, packed in
 //               pairs) back over S, rescale O when the running max grows.
-// The MMAs of one thread complete in issue order: S_X(j) complete means the
-// P V two tiles back is complete, so its buffer (now holding S_X(j)) may take
-// P_X(j).  The running max is only raised when a row's max grows by more
-// than 2^8 (the weights then stay below 256), so most tiles need no O
-// rescale; the result is the same softmax.  For bf16, P = high part +
-// residual (two products), so the weights keep about 16 bits.
+// The two groups ping-pong: while one group's softmax runs, the tensor cores
+// compute the other group's products.  The MMAs of one thread complete in
+// issue order, so S_X(j+1) (issued after O_X += P_X(j) V) finding its
+// barrier complete means that P V has completed too.  The running max is
+// only raised when a row's max grows by more than 2^8 (the weights then stay
+// below 256), so most tiles need no O rescale; the result is the same
+// softmax.  For bf16, P = high part + residual (two products), so the
+// weights keep about 16 bits.
 //
 // Operand layouts: Q, K in shared memory K-major (row = token, 64 elements
 // of the head dimension per 128-byte slab, 1024-byte atoms of 8 rows, 16-byte
 // chunk c of row r at chunk c ^ (r % 8)); V the same bytes read as an
 // MN-major operand (N = head dimension); P in tensor memory, row = lane, keys
-// 2c and 2c + 1 of the tile in column c of the S buffer (bf16 residuals in
-// columns 32 + c).
+// 64 h + 2c and 64 h + 2c + 1 in column 64 h + c.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -53,14 +53,14 @@ namespace {
 
 constexpr int kBM = 128;            // query rows per tile (MMA M, tensor-memory lanes)
 constexpr int kRows = 2 * kBM;      // query rows per work item (tiles A and B)
-constexpr int kBN = 64;             // keys per K/V tile (MMA N of S, K of P V)
+constexpr int kBN = 128;            // keys per K/V tile (MMA N of S, K of P V)
 constexpr int kWarps = 11;          // K producer, MMA issuer, 2 x 4 softmax warps, V producer
 constexpr int kThreads = kWarps * 32;
 constexpr uint32_t kTmemCols = 512;
-// tensor-memory columns: S buffer b of group X (and P over it) at
-// kColS + (2X + b) kBN, O of group X at kColO + X D
-constexpr uint32_t kColS = 0;
-constexpr uint32_t kColO = 4 * kBN;
+// tensor-memory columns: S_X (and P_X over it) at X kBN, O_X at kColO + X D;
+// P_X: keys 64 h .. + 63 packed in pairs in the columns 64 h .. + 31 of S_X,
+// their bf16 residuals in 64 h + 32 .. + 63
+constexpr uint32_t kColO = 2 * kBN;
 constexpr float kRescaleLog2 = 8.f;  // raise the running max only past this growth
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr uint32_t kWaitLimitIters = 1u << 26;
@@ -72,7 +72,8 @@ struct PCfg {
     static constexpr int SLAB_KV = kBN * 128;          // bytes of one K (or V) slab
     static constexpr int Q_BYTES = SLABS * SLAB_Q;     // one tile's Q
     static constexpr int KV_BYTES = SLABS * SLAB_KV;
-    static constexpr int NST = 4;                      // K and V ring depth
+    // K and V ring depth: as deep as shared memory allows
+    static constexpr int NST = D == 128 ? 2 : 4;
     static constexpr int Q_OFF = 0;                    // Q_A, Q_B
     static constexpr int K_OFF = Q_OFF + 2 * Q_BYTES;
     static constexpr int V_OFF = K_OFF + NST * KV_BYTES;
@@ -347,11 +348,11 @@ enum : int {
     kBarKEmpty = 6,   // + stage
     kBarVFull = 10,   // + stage
     kBarVEmpty = 14,  // + stage
-    kBarSFull = 18,   // + 2 group + buffer
-    kBarPFull = 22,   // + group
-    kBarPvDone = 24,  // + group
-    kBarMmaDone = 26,
-    kBarCount = 27
+    kBarSFull = 18,   // + group: S_X computed (and every earlier product)
+    kBarPFull = 20,   // + group: P_X written, O_X rescaled
+    kBarPvDone = 22,  // + group: an item's last O_X += P_X V completed
+    kBarMmaDone = 24,
+    kBarCount = 25
 };
 
 // One work item: 256 query rows (tiles A and B) of one (sequence, head).
@@ -448,11 +449,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0 || warp == kWarps - 1) {
         // ============================================ TMA producers
-        // warp 0: the query tiles and the K tiles; the last warp: the V tiles.
-        // Both walk the same items and the same global key-tile sequence g;
-        // tile g uses stage g % NST of its ring.
-        const bool kq = warp == 0;
+        // warp 0: the query tiles and the K tiles; the last warp: the V tiles
+        // (separate warps: a lane waiting on a barrier would hold up the
+        // other's issue).  Both walk the same items and the same global
+        // key-tile sequence g; tile g uses stage g % NST of its ring.
         if (lane == 0) {
+            const bool kq = warp == 0;
             const CUtensorMap* map = kq ? &tm_k : &tm_v;
             const uint32_t ring = kq ? sK : sV;
             const int full0 = kq ? kBarKFull : kBarVFull, empty0 = kq ? kBarKEmpty : kBarVEmpty;
@@ -520,109 +522,99 @@ __global__ void __launch_bounds__(kThreads, 1)
             // below 256 KiB)
             const uint64_t dQ = sdesc(sQ, 16, 1024), dK = sdesc(sK, 16, 1024);
             const uint64_t dV = sdesc(sV, C::SLAB_KV, 1024);
-            // S products of key tile j of an item (global key tile gk): for
-            // each group whose rows reach the tile, into its next S buffer
-            int64_t gsx[2] = {0, 0};         // S products issued per group
-            auto issue_s = [&](const Item& it, int j, int64_t gk, int item) -> bool {
-                if (j == 0 && !mbar_wait(bar(kBarQFull), (uint32_t)(item & 1), abort_flag))
-                    return false;
-                const int st = (int)(gk % NST);
-                if (!mbar_wait(bar(kBarKFull + st), (uint32_t)((gk / NST) & 1), abort_flag))
-                    return false;
-                tc_fence_after();
-                const uint64_t dk = dK + (uint64_t)((st * C::KV_BYTES) >> 4);
-#pragma unroll
-                for (int x = 0; x < 2; ++x) {
-                    if (j >= it.n[x]) continue;
-                    const int b = (int)(gsx[x] & 1);
-                    const uint32_t d = tmem + kColS + (uint32_t)(2 * x + b) * kBN;
-                    const uint64_t dq = dQ + (uint64_t)((x * C::Q_BYTES) >> 4);
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t qo = ((kk >> 2) * C::SLAB_Q + (kk & 3) * 32) >> 4;
-                        const uint32_t ko = ((kk >> 2) * C::SLAB_KV + (kk & 3) * 32) >> 4;
-                        umma(d, dq + qo, dk + ko, ID_S, kk > 0);
-                    }
-                    umma_commit(bar(kBarSFull + 2 * x + b));
-                    ++gsx[x];
-                }
-                umma_commit(bar(kBarKEmpty + st));
-                if (j == it.n_kv - 1) umma_commit(bar(kBarQEmpty));
-                return true;
-            };
-            // S runs up to two key tiles ahead of P V, across item boundaries:
-            // a cursor (item, tile) over the same sequence the others walk
-            int64_t sw = w0;
-            Item sit;
-            int sj = 0, sitem = 0;
-            int64_t gs = 0;
-            bool s_has = false;
-            auto s_next_item = [&]() {
-                s_has = false;
-                while (sw < n_items) {
-                    const bool v = item_at(a, sw, true, sit);
-                    sw += dw;
-                    if (v) {
-                        s_has = true;
-                        sj = 0;
-                        return;
-                    }
-                }
-            };
-            auto s_issue_one = [&]() -> bool {
-                if (!s_has) return true;
-                if (!issue_s(sit, sj, gs, sitem)) return false;
-                ++gs;
-                if (++sj == sit.n_kv) {
-                    ++sitem;
-                    s_next_item();
-                }
-                return true;
-            };
-            s_next_item();
-            bool ok = s_issue_one() && s_issue_one();
-            int64_t g = 0;
+            int64_t gkf = 0;                 // K tiles waited for so far
             int64_t gpx[2] = {0, 0};         // P V products issued per group
+            int items = 0;
+            // S_X = Q_X K^T for the key tile in stage st into S_X's columns
+            auto s_mma = [&](int x, int st) {
+                const uint64_t dk = dK + (uint64_t)((st * C::KV_BYTES) >> 4);
+                const uint64_t dq = dQ + (uint64_t)((x * C::Q_BYTES) >> 4);
+                const uint32_t d = tmem + (uint32_t)(x * kBN);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t qo = ((kk >> 2) * C::SLAB_Q + (kk & 3) * 32) >> 4;
+                    const uint32_t ko = ((kk >> 2) * C::SLAB_KV + (kk & 3) * 32) >> 4;
+                    umma(d, dq + qo, dk + ko, ID_S, kk > 0);
+                }
+                umma_commit(bar(kBarSFull + x));
+            };
+            bool ok = true;
+            int64_t g = 0;
             for (int64_t w = w0; ok && w < n_items; w += dw) {
                 Item it;
-                if (!item_at(a, w, false, it)) continue;
-                for (int j = 0; j < it.n_kv; ++j, ++g) {
+                if (!item_at(a, w, true, it)) continue;
+                // the last group whose S reads a key tile (B, unless B has no rows)
+                const int xl = it.n[1] > 0 ? 1 : 0;
+                if (!mbar_wait(bar(kBarQFull), (uint32_t)(items & 1), abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                // S of key tile 0
+                {
+                    const int st = (int)(g % NST);
+                    if (!mbar_wait(bar(kBarKFull + st), (uint32_t)((g / NST) & 1), abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    ++gkf;
+                    tc_fence_after();
+                    for (int x = 0; x < 2; ++x)
+                        if (it.n[x] > 0) s_mma(x, st);
+                    umma_commit(bar(kBarKEmpty + st));
+                    if (it.n_kv == 1) umma_commit(bar(kBarQEmpty));
+                }
+                for (int j = 0; ok && j < it.n_kv; ++j, ++g) {
                     const int st = (int)(g % NST);
                     if (!mbar_wait(bar(kBarVFull + st), (uint32_t)((g / NST) & 1), abort_flag)) {
                         ok = false;
                         break;
                     }
                     const uint64_t dv = dV + (uint64_t)((st * C::KV_BYTES) >> 4);
-#pragma unroll
+                    const int stn = (int)((g + 1) % NST);
+                    bool k_next = false;             // next key tile's K waited for
                     for (int x = 0; x < 2; ++x) {
-                        if (!ok || j >= it.n[x]) continue;
+                        if (j >= it.n[x]) continue;
+                        // O_X += P_X(j) V_j, P_X from tensor memory
                         if (!mbar_wait<false>(bar(kBarPFull + x), (uint32_t)(gpx[x] & 1), abort_flag)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        // P_X(j) over the S buffer of the group's tile
-                        const uint32_t pa =
-                            tmem + kColS + (uint32_t)(2 * x + (int)(gpx[x] & 1)) * kBN;
+                        const uint32_t pa = tmem + (uint32_t)(x * kBN);
 #pragma unroll
                         for (int kk = 0; kk < kBN / 16; ++kk) {
+                            // keys 16 kk .. + 15: half kk / 4, 8 columns per step
+                            const uint32_t pc = (uint32_t)((kk >> 2) * 64 + (kk & 3) * 8);
                             const uint64_t vd = dv + (uint64_t)((kk * 2048) >> 4);
-                            umma_ts(tmem + kColO + x * D, pa + (uint32_t)(kk * 8), vd, ID_PV,
-                                    (j > 0 || kk > 0));
+                            umma_ts(tmem + kColO + x * D, pa + pc, vd, ID_PV, (j > 0 || kk > 0));
                             if constexpr (kSplit)
-                                umma_ts(tmem + kColO + x * D, pa + (uint32_t)(32 + kk * 8), vd,
-                                        ID_PV, 1u);
+                                umma_ts(tmem + kColO + x * D, pa + pc + 32, vd, ID_PV, 1u);
                         }
-                        umma_commit(bar(kBarPvDone + x));
                         ++gpx[x];
+                        if (j == it.n[x] - 1) umma_commit(bar(kBarPvDone + x));
+                        // then S_X of the next key tile over P_X (in issue order)
+                        if (j + 1 < it.n[x]) {
+                            if (!k_next) {
+                                if (!mbar_wait(bar(kBarKFull + stn), (uint32_t)(((g + 1) / NST) & 1),
+                                               abort_flag)) {
+                                    ok = false;
+                                    break;
+                                }
+                                ++gkf;
+                                k_next = true;
+                                tc_fence_after();
+                            }
+                            s_mma(x, stn);
+                            if (x == xl || j + 1 >= it.n[1]) {
+                                umma_commit(bar(kBarKEmpty + stn));
+                                if (j + 1 == it.n_kv - 1) umma_commit(bar(kBarQEmpty));
+                            }
+                        }
                     }
                     if (!ok) break;
                     umma_commit(bar(kBarVEmpty + st));
-                    if (!s_issue_one()) {
-                        ok = false;
-                        break;
-                    }
                 }
+                ++items;
             }
             if (!ok) fail();
             // every MMA issued has completed before the CTA moves on
@@ -638,12 +630,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = q4 * 32 + lane;              // row of the tile = TMEM lane
         const int gtid = (warp - 2 - 4 * x) * 32 + lane;   // 0..127 within the group
         const uint32_t tl = tmem + ((uint32_t)(q4 * 32) << 16);
+        const uint32_t tS = tl + (uint32_t)(x * kBN);      // S_X, then P_X over it
         const uint32_t tO = tl + kColO + (uint32_t)(x * D);
         const float sl2 = a.scale_log2;
         const bool pos_scale = sl2 >= 0.f;
         bool ok = true;
         int64_t gx = 0;                              // this group's tiles so far
         int64_t g = 0;                               // key tiles so far (V stage)
+        int items = 0;
         for (int64_t w = w0; ok && w < n_items; w += dw) {
             Item it;
             if (!item_at(a, w, false, it)) continue;
@@ -658,72 +652,75 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int qpos = pos0 + row;             // causal limit of the row
             float m = -INFINITY, l = 0.f;
             for (int j = 0; j < nx; ++j, ++gx) {
-                const int b = (int)(gx & 1);
-                if (!mbar_wait(bar(kBarSFull + 2 * x + b), (uint32_t)((gx >> 1) & 1), abort_flag)) {
+                // S_X(j) complete (and with it the previous O_X += P_X V)
+                if (!mbar_wait(bar(kBarSFull + x), (uint32_t)(gx & 1), abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t tS = tl + kColS + (uint32_t)(2 * x + b) * kBN;
-                uint32_t r[64];
-                tmem_ld64(tS, r);
                 const int kb = j * kBN;
                 const bool full = kb + kBN - 1 <= pos0;   // every key visible to every row
+                // row max of the masked, scaled scores (two halves of 64 keys)
                 float mx = -INFINITY;
-                if (full) {
-                    float ext = pos_scale ? -INFINITY : INFINITY;
-                    if (pos_scale) {
 #pragma unroll
-                        for (int e = 0; e < 64; ++e) ext = fmaxf(ext, __uint_as_float(r[e]));
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t r[64];
+                    tmem_ld64(tS + (uint32_t)(hh * 64), r);
+                    if (full) {
+                        float e0 = pos_scale ? -INFINITY : INFINITY, e1 = e0;
+                        if (pos_scale) {
+#pragma unroll
+                            for (int e = 0; e < 64; e += 2) {
+                                e0 = fmaxf(e0, __uint_as_float(r[e]));
+                                e1 = fmaxf(e1, __uint_as_float(r[e + 1]));
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 64; e += 2) {
+                                e0 = fminf(e0, __uint_as_float(r[e]));
+                                e1 = fminf(e1, __uint_as_float(r[e + 1]));
+                            }
+                        }
+                        mx = fmaxf(mx, (pos_scale ? fmaxf(e0, e1) : fminf(e0, e1)) * sl2);
                     } else {
 #pragma unroll
-                        for (int e = 0; e < 64; ++e) ext = fminf(ext, __uint_as_float(r[e]));
+                        for (int e = 0; e < 64; ++e)
+                            if (kb + hh * 64 + e <= qpos) mx = fmaxf(mx, __uint_as_float(r[e]) * sl2);
                     }
-                    mx = ext * sl2;
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 64; ++e)
-                        if (kb + e <= qpos) mx = fmaxf(mx, __uint_as_float(r[e]) * sl2);
                 }
                 float m_new = m;
                 if (mx > m + kRescaleLog2 || (m == -INFINITY && mx > -INFINITY)) m_new = mx;
                 const bool rescale = j > 0 && m_new != m;
                 const float alpha = rescale ? ex2(m - m_new) : 1.f;
-                // weights, packed to 16 bits (and the bf16 residual)
-                uint32_t pk[32];
-                uint32_t pr[kSplit ? 32 : 1];
+                // weights, packed in pairs over S: half hh (keys 64 hh ..) goes to
+                // the columns 64 hh .. + 31 (high parts) and + 32 .. + 63 (bf16
+                // residuals), which held that half's scores, read again here
                 float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
-                for (int e = 0; e < 64; e += 2) {
-                    float p0 = ex2(fmaf(__uint_as_float(r[e]), sl2, -m_new));
-                    float p1 = ex2(fmaf(__uint_as_float(r[e + 1]), sl2, -m_new));
-                    if (!full) {
-                        p0 = kb + e <= qpos ? p0 : 0.f;
-                        p1 = kb + e + 1 <= qpos ? p1 : 0.f;
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t r[64];
+                    tmem_ld64(tS + (uint32_t)(hh * 64), r);
+                    uint32_t pk[32];
+                    uint32_t pr[kSplit ? 32 : 1];
+#pragma unroll
+                    for (int e = 0; e < 64; e += 2) {
+                        float p0 = ex2(fmaf(__uint_as_float(r[e]), sl2, -m_new));
+                        float p1 = ex2(fmaf(__uint_as_float(r[e + 1]), sl2, -m_new));
+                        if (!full) {
+                            p0 = kb + hh * 64 + e <= qpos ? p0 : 0.f;
+                            p1 = kb + hh * 64 + e + 1 <= qpos ? p1 : 0.f;
+                        }
+                        rs0 += p0;
+                        rs1 += p1;
+                        uint32_t res;
+                        pk[e >> 1] = Pk<T>::pack(p0, p1, res);
+                        if constexpr (kSplit) pr[e >> 1] = res;
                     }
-                    rs0 += p0;
-                    rs1 += p1;
-                    uint32_t res;
-                    pk[e >> 1] = Pk<T>::pack(p0, p1, res);
-                    if constexpr (kSplit) pr[e >> 1] = res;
+                    tmem_st32(tS + (uint32_t)(hh * 64), pk);
+                    if constexpr (kSplit) tmem_st32(tS + (uint32_t)(hh * 64 + 32), pr);
                 }
                 l = l * alpha + (rs0 + rs1);
                 m = m_new;
-                // P over this tile's S buffer (its scores are in registers)
-                tmem_st32(tS, pk);
-                if constexpr (kSplit) tmem_st32(tS + 32, pr);
-                // The previous P V must be complete before O is rescaled, and
-                // before this tile's P is announced: the MMA issuer has then
-                // taken the previous announcement, so the barrier never runs two
-                // phases ahead of it (a phase parity would then be ambiguous).
-                // S_X(j) complete already implies the P V before that one.
-                if (j > 0) {
-                    if (!mbar_wait(bar(kBarPvDone + x), (uint32_t)((gx - 1) & 1), abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                }
                 // O_X *= alpha for rows whose running max rose (warp-wide access)
                 if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
@@ -762,10 +759,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             g += it.n_kv;
             if (nx == 0) continue;
             // the item's output rows of this tile, once its last P V is done
-            if (!mbar_wait(bar(kBarPvDone + x), (uint32_t)((gx - 1) & 1), abort_flag)) {
+            if (!mbar_wait(bar(kBarPvDone + x), (uint32_t)(items & 1), abort_flag)) {
                 ok = false;
                 break;
             }
+            ++items;
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
             T* orow = static_cast<T*>(a.out) +
@@ -786,6 +784,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         dst[e] = make_uint4(wv[4 * e], wv[4 * e + 1], wv[4 * e + 2], wv[4 * e + 3]);
                 }
             }
+            tc_fence_before();
         }
         if (!ok) fail();
         tc_fence_before();
