@@ -287,6 +287,39 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         : "memory");
 }
 
+// Pairs of fp32 values in one 64-bit register, and the packed fp32 FMA and
+// add that work on both halves at once.
+__device__ __forceinline__ uint64_t f2(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t v, float& a, float& b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// max / min of three values in one instruction
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+__device__ __forceinline__ float min3(float a, float b, float c) {
+    float d;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -670,15 +703,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         float e0 = pos_scale ? -INFINITY : INFINITY, e1 = e0;
                         if (pos_scale) {
 #pragma unroll
-                            for (int e = 0; e < 64; e += 2) {
-                                e0 = fmaxf(e0, __uint_as_float(r[e]));
-                                e1 = fmaxf(e1, __uint_as_float(r[e + 1]));
+                            for (int e = 0; e < 64; e += 4) {
+                                e0 = max3(e0, __uint_as_float(r[e]), __uint_as_float(r[e + 1]));
+                                e1 = max3(e1, __uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]));
                             }
                         } else {
 #pragma unroll
-                            for (int e = 0; e < 64; e += 2) {
-                                e0 = fminf(e0, __uint_as_float(r[e]));
-                                e1 = fminf(e1, __uint_as_float(r[e + 1]));
+                            for (int e = 0; e < 64; e += 4) {
+                                e0 = min3(e0, __uint_as_float(r[e]), __uint_as_float(r[e + 1]));
+                                e1 = min3(e1, __uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]));
                             }
                         }
                         mx = fmaxf(mx, (pos_scale ? fmaxf(e0, e1) : fminf(e0, e1)) * sl2);
@@ -695,23 +728,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // weights, packed in pairs over S: half hh (keys 64 hh ..) goes to
                 // the columns 64 hh .. + 31 (high parts) and + 32 .. + 63 (bf16
                 // residuals), which held that half's scores, read again here
-                float rs0 = 0.f, rs1 = 0.f;
+                uint64_t rs2 = f2(0.f, 0.f);
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     uint32_t r[64];
                     tmem_ld64(tS + (uint32_t)(hh * 64), r);
                     uint32_t pk[32];
                     uint32_t pr[kSplit ? 32 : 1];
+                    const uint64_t sc2 = f2(sl2, sl2), nm2 = f2(-m_new, -m_new);
 #pragma unroll
                     for (int e = 0; e < 64; e += 2) {
-                        float p0 = ex2(fmaf(__uint_as_float(r[e]), sl2, -m_new));
-                        float p1 = ex2(fmaf(__uint_as_float(r[e + 1]), sl2, -m_new));
+                        const uint64_t x2 =
+                            fma2(f2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), sc2, nm2);
+                        float p0, p1;
+                        f2_split(x2, p0, p1);
+                        p0 = ex2(p0);
+                        p1 = ex2(p1);
                         if (!full) {
                             p0 = kb + hh * 64 + e <= qpos ? p0 : 0.f;
                             p1 = kb + hh * 64 + e + 1 <= qpos ? p1 : 0.f;
                         }
-                        rs0 += p0;
-                        rs1 += p1;
+                        rs2 = add2(rs2, f2(p0, p1));
                         uint32_t res;
                         pk[e >> 1] = Pk<T>::pack(p0, p1, res);
                         if constexpr (kSplit) pr[e >> 1] = res;
@@ -719,6 +756,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_st32(tS + (uint32_t)(hh * 64), pk);
                     if constexpr (kSplit) tmem_st32(tS + (uint32_t)(hh * 64 + 32), pr);
                 }
+                float rs0, rs1;
+                f2_split(rs2, rs0, rs1);
                 l = l * alpha + (rs0 + rs1);
                 m = m_new;
                 // O_X *= alpha for rows whose running max rose (warp-wide access)
