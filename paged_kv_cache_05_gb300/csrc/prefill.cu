@@ -38,7 +38,7 @@
 // of the head dimension per 128-byte slab, 1024-byte atoms of 8 rows, 16-byte
 // chunk c of row r at chunk c ^ (r % 8)); V the same bytes read as an
 // MN-major operand (N = head dimension); P in tensor memory, row = lane, keys
-// 64 h + 2c and 64 h + 2c + 1 in column 64 h + c.
+// 32 q + 2c and 32 q + 2c + 1 in column 32 q + c (bf16 residuals 16 further).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -58,8 +58,8 @@ constexpr int kWarps = 11;          // K producer, MMA issuer, 2 x 4 softmax war
 constexpr int kThreads = kWarps * 32;
 constexpr uint32_t kTmemCols = 512;
 // tensor-memory columns: S_X (and P_X over it) at X kBN, O_X at kColO + X D;
-// P_X: keys 64 h .. + 63 packed in pairs in the columns 64 h .. + 31 of S_X,
-// their bf16 residuals in 64 h + 32 .. + 63
+// P_X: keys 32 q .. + 31 packed in pairs in the columns 32 q .. + 15 of S_X,
+// their bf16 residuals in 32 q + 16 .. + 31
 constexpr uint32_t kColO = 2 * kBN;
 constexpr float kRescaleLog2 = 8.f;  // raise the running max only past this growth
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
@@ -269,6 +269,18 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
           "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]),
           "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
         : "r"(taddr)
+        : "memory");
+}
+
+// Store 16 columns of this warp's lanes and wait for the store to complete.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, "
+        "%10, %11, %12, %13, %14, %15, %16};\n\t"
+        "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15])
         : "memory");
 }
 
@@ -616,12 +628,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t pa = tmem + (uint32_t)(x * kBN);
 #pragma unroll
                         for (int kk = 0; kk < kBN / 16; ++kk) {
-                            // keys 16 kk .. + 15: half kk / 4, 8 columns per step
-                            const uint32_t pc = (uint32_t)((kk >> 2) * 64 + (kk & 3) * 8);
+                            // keys 16 kk .. + 15: quarter kk / 2, 8 columns per step
+                            const uint32_t pc = (uint32_t)((kk >> 1) * 32 + (kk & 1) * 8);
                             const uint64_t vd = dv + (uint64_t)((kk * 2048) >> 4);
                             umma_ts(tmem + kColO + x * D, pa + pc, vd, ID_PV, (j > 0 || kk > 0));
                             if constexpr (kSplit)
-                                umma_ts(tmem + kColO + x * D, pa + pc + 32, vd, ID_PV, 1u);
+                                umma_ts(tmem + kColO + x * D, pa + pc + 16, vd, ID_PV, 1u);
                         }
                         ++gpx[x];
                         if (j == it.n[x] - 1) umma_commit(bar(kBarPvDone + x));
@@ -725,19 +737,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (mx > m + kRescaleLog2 || (m == -INFINITY && mx > -INFINITY)) m_new = mx;
                 const bool rescale = j > 0 && m_new != m;
                 const float alpha = rescale ? ex2(m - m_new) : 1.f;
-                // weights, packed in pairs over S: half hh (keys 64 hh ..) goes to
-                // the columns 64 hh .. + 31 (high parts) and + 32 .. + 63 (bf16
-                // residuals), which held that half's scores, read again here
+                // weights, packed in pairs over S, a quarter of 32 keys at a
+                // time: keys 32 q .. + 31 go to the columns 32 q .. + 15 (high
+                // parts) and + 16 .. + 31 (bf16 residuals), which held that
+                // quarter's scores, read again here
                 uint64_t rs2 = f2(0.f, 0.f);
+                const uint64_t sc2 = f2(sl2, sl2), nm2 = f2(-m_new, -m_new);
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    uint32_t r[64];
-                    tmem_ld64(tS + (uint32_t)(hh * 64), r);
-                    uint32_t pk[32];
-                    uint32_t pr[kSplit ? 32 : 1];
-                    const uint64_t sc2 = f2(sl2, sl2), nm2 = f2(-m_new, -m_new);
+                for (int q = 0; q < kBN / 32; ++q) {
+                    uint32_t r[32];
+                    tmem_ld32(tS + (uint32_t)(q * 32), r);
+                    uint32_t pk[16];
+                    uint32_t pr[kSplit ? 16 : 1];
 #pragma unroll
-                    for (int e = 0; e < 64; e += 2) {
+                    for (int e = 0; e < 32; e += 2) {
                         const uint64_t x2 =
                             fma2(f2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), sc2, nm2);
                         float p0, p1;
@@ -745,16 +758,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         p0 = ex2(p0);
                         p1 = ex2(p1);
                         if (!full) {
-                            p0 = kb + hh * 64 + e <= qpos ? p0 : 0.f;
-                            p1 = kb + hh * 64 + e + 1 <= qpos ? p1 : 0.f;
+                            p0 = kb + q * 32 + e <= qpos ? p0 : 0.f;
+                            p1 = kb + q * 32 + e + 1 <= qpos ? p1 : 0.f;
                         }
                         rs2 = add2(rs2, f2(p0, p1));
                         uint32_t res;
                         pk[e >> 1] = Pk<T>::pack(p0, p1, res);
                         if constexpr (kSplit) pr[e >> 1] = res;
                     }
-                    tmem_st32(tS + (uint32_t)(hh * 64), pk);
-                    if constexpr (kSplit) tmem_st32(tS + (uint32_t)(hh * 64 + 32), pr);
+                    tmem_st16(tS + (uint32_t)(q * 32), pk);
+                    if constexpr (kSplit) tmem_st16(tS + (uint32_t)(q * 32 + 16), pr);
                 }
                 float rs0, rs1;
                 f2_split(rs2, rs0, rs1);
