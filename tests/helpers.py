@@ -108,3 +108,35 @@ def spread(ctx, n):
     order = np.argsort(ctx, kind="stable")
     pick = np.unique(np.linspace(0, len(ctx) - 1, n).round().astype(int))
     return sorted(int(order[i]) for i in pick)
+
+
+def prefill_oracle_threaded(q, kc, vc, bt, ctx, qs, scale, dtype: str, threads: int = 8):
+    """The prompt-phase oracle, one sequence per call, calls spread over host
+    threads (the C routine runs without the GIL).  Each call is the unchanged
+    oracle on that sequence alone: its table row, context and query rows."""
+    import threading
+    T = int(qs[-1])
+    H, D = kc.shape[1], kc.shape[3]
+    out = np.zeros((T, H, D), np.float64)
+    todo = sorted((s for s in range(len(ctx)) if qs[s + 1] > qs[s]),
+                  key=lambda s: -(int(qs[s + 1] - qs[s]) * int(ctx[s])))
+    errs = []
+
+    def worker(i):
+        try:
+            for s in todo[i::threads]:
+                a, b = int(qs[s]), int(qs[s + 1])
+                out[a:b] = oracle.paged_attention_prefill(
+                    q[a:b], kc, vc, bt[s:s + 1], np.array([ctx[s]], np.int32),
+                    np.array([0, b - a], np.int32), scale, ORC_DTYPE[dtype])
+        except Exception as e:  # surfaced below
+            errs.append(e)
+
+    ts = [threading.Thread(target=worker, args=(i,)) for i in range(max(1, threads))]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    if errs:
+        raise errs[0]
+    return out

@@ -7,7 +7,8 @@ import numpy as np
 import pytest
 
 import oracle
-from helpers import ORC_DTYPE, attn_check, random_case, to_dev, words
+from helpers import (ORC_DTYPE, attn_check, prefill_oracle_threaded, random_case, to_dev,
+                     words)
 from paged_kv_cache_05_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -28,8 +29,8 @@ def run_case(pkv, rs, ctx, qlen, H, D, B, dtype):
     T = int(qs[-1])
     q = words((max(T, 1), H, D), dtype, rs)[:T]
     scale = float(np.float32(1 / math.sqrt(D)))
-    ref = oracle.paged_attention_prefill(q, case["kc"], case["vc"], case["bt"], case["ctx"], qs,
-                                         scale, ORC_DTYPE[dtype])
+    ref = prefill_oracle_threaded(q, case["kc"], case["vc"], case["bt"], case["ctx"], qs, scale,
+                                  dtype)
     dq = to_dev(q, dtype) if T else torch.empty((0, H, D), dtype=torch.float16, device="cuda")
     out = torch.full_like(dq, float("nan"))
     pkv.paged_attention_prefill(out, dq, to_dev(case["kc"], dtype), to_dev(case["vc"], dtype),
@@ -126,3 +127,81 @@ def test_prefill_unwritten_slots_never_matter(pkv, dtype, B):
     ref = oracle.paged_attention_prefill(q, case["kc"], case["vc"], case["bt"], case["ctx"], qs,
                                          0.088, ORC_DTYPE[dtype])
     attn_check(a, ref, "prefill dtype=%s B=%d" % (dtype, B))
+
+
+
+@pytest.mark.parametrize("dtype,D", [("f16", 128), ("bf16", 128), ("f16", 64)])
+def test_prefill_many_items_per_cta(pkv, dtype, D):
+    """About 480 (sequence, head, 256-row) work items for 152 persistent CTAs,
+    so each CTA takes several in turn and the loads and products that run ahead
+    across item boundaries are exercised: prompts of two items, items with both
+    128-row tiles, many short continued prompts (one tile, partly filled), and
+    empty queries, in random order."""
+    rs = np.random.default_rng(950 + D + (dtype == "bf16"))
+    pairs = []
+    for _ in range(4):                       # whole prompts past 256 rows
+        c = int(rs.integers(260, 331))
+        pairs.append((c, c))
+    for _ in range(8):                       # both tiles of one item
+        c = int(rs.integers(140, 301))
+        pairs.append((c, int(rs.integers(129, min(c, 256) + 1))))
+    for i in range(44):                      # short continuations
+        c = int(rs.integers(1, 201))
+        pairs.append((c, 0 if i % 15 == 7 else int(rs.integers(1, min(c, 40) + 1))))
+    rs.shuffle(pairs)
+    ctx = [c for c, _ in pairs]
+    qlen = [n for _, n in pairs]
+    H = 8
+    assert sum(-(-n // 256) for n in qlen) * H > 2 * 152
+    run_case(pkv, rs, ctx, qlen, H, D, 16, dtype)
+
+
+def test_prefill_workload_full_size_sampled(pkv):
+    """The prompt-phase workload at its full size (16 prompts of 543..1729
+    tokens, 40 heads x 128, fp16, B 16), set up as the benchmark does (block
+    manager slots, every prompt token written by reshape_and_cache), checked on
+    sampled query rows of every prompt: the rows on each side of the 128-row
+    tile and 256-row item edges, the last row and random rows.  Causal row p of
+    a prompt is the same attention as a one-token query at context p + 1, so
+    each sampled row goes to the oracle as its own one-row sequence."""
+    import torch
+    spec = W.SPECS["prefill"]
+    ctx = W.context_lens(spec)
+    S, H, D, B = spec.num_seqs, spec.num_heads, spec.head_dim, spec.block_size
+    nb = W.pool_blocks(spec, ctx)
+    bm = pkv.BlockManager(nb, B, spec.seed)
+    slots = np.concatenate([bm.add_sequence(s, int(ctx[s])) for s in range(S)])
+    maxb = max(-(-int(c) // B) for c in ctx)
+    tables, _ = bm.export(list(range(S)), maxb)
+    T = int(ctx.sum())
+    kc = torch.zeros((nb, H, B, D), dtype=torch.float16, device="cuda")
+    vc = torch.zeros_like(kc)
+    k = W.device_normal((T, H, D), "f16", spec.seed + 1)
+    v = W.device_normal((T, H, D), "f16", spec.seed + 2)
+    q = W.device_normal((T, H, D), "f16", spec.seed + 3)
+    qs = np.concatenate([[0], np.cumsum(ctx)]).astype(np.int32)
+    pkv.reshape_and_cache(k, v, kc, vc, torch.from_numpy(slots).cuda())
+    out = torch.full_like(q, float("nan"))
+    pkv.paged_attention_prefill(out, q, kc, vc, torch.from_numpy(tables).cuda(),
+                                torch.from_numpy(ctx).cuda(), torch.from_numpy(qs).cuda(),
+                                spec.scale, int(ctx.max()))
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == 0
+    rs = np.random.default_rng(951)
+    seq, rows = [], []
+    for s in range(S):
+        n = int(ctx[s])
+        pick = {0, 1, n - 1} | {e + d for e in range(128, n, 128) for d in (-1, 0)}
+        pick |= {int(x) for x in rs.integers(0, n, size=3)}
+        for p in sorted(x for x in pick if 0 <= x < n):
+            seq.append(s)
+            rows.append(p)
+    seq, rows = np.array(seq), np.array(rows)
+    grow = qs[seq] + rows                            # row index into q / out
+    qh = W.torch_to_words(q[torch.from_numpy(grow).cuda()])
+    kh, vh = W.torch_to_words(kc), W.torch_to_words(vc)
+    n = len(rows)
+    ref = prefill_oracle_threaded(qh, kh, vh, tables[seq], (rows + 1).astype(np.int32),
+                                  np.arange(n + 1, dtype=np.int32), spec.scale, "f16")
+    attn_check(out[torch.from_numpy(grow).cuda()], ref,
+               "prefill workload, %d sampled rows x %d heads" % (n, H))
