@@ -46,6 +46,7 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "pkv_internal.h"
 
@@ -743,32 +744,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // quarter's scores, read again here
                 uint64_t rs2 = f2(0.f, 0.f);
                 const uint64_t sc2 = f2(sl2, sl2), nm2 = f2(-m_new, -m_new);
+                // the full-tile loop carries no mask code; the diagonal one
+                // compares each key with the row's last visible key
+                auto weights = [&](auto masked) {
+                    constexpr bool kMask = decltype(masked)::value;
+                    const int lim = qpos - kb;       // last visible key of the tile
 #pragma unroll
-                for (int q = 0; q < kBN / 32; ++q) {
-                    uint32_t r[32];
-                    tmem_ld32(tS + (uint32_t)(q * 32), r);
-                    uint32_t pk[16];
-                    uint32_t pr[kSplit ? 16 : 1];
+                    for (int q = 0; q < kBN / 32; ++q) {
+                        uint32_t r[32];
+                        tmem_ld32(tS + (uint32_t)(q * 32), r);
+                        uint32_t pk[16];
+                        uint32_t pr[kSplit ? 16 : 1];
 #pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        const uint64_t x2 =
-                            fma2(f2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), sc2, nm2);
-                        float p0, p1;
-                        f2_split(x2, p0, p1);
-                        p0 = ex2(p0);
-                        p1 = ex2(p1);
-                        if (!full) {
-                            p0 = kb + q * 32 + e <= qpos ? p0 : 0.f;
-                            p1 = kb + q * 32 + e + 1 <= qpos ? p1 : 0.f;
+                        for (int e = 0; e < 32; e += 2) {
+                            const uint64_t x2 = fma2(
+                                f2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), sc2, nm2);
+                            float p0, p1;
+                            f2_split(x2, p0, p1);
+                            p0 = ex2(p0);
+                            p1 = ex2(p1);
+                            if constexpr (kMask) {
+                                p0 = q * 32 + e <= lim ? p0 : 0.f;
+                                p1 = q * 32 + e + 1 <= lim ? p1 : 0.f;
+                            }
+                            rs2 = add2(rs2, f2(p0, p1));
+                            uint32_t res;
+                            pk[e >> 1] = Pk<T>::pack(p0, p1, res);
+                            if constexpr (kSplit) pr[e >> 1] = res;
                         }
-                        rs2 = add2(rs2, f2(p0, p1));
-                        uint32_t res;
-                        pk[e >> 1] = Pk<T>::pack(p0, p1, res);
-                        if constexpr (kSplit) pr[e >> 1] = res;
+                        tmem_st16(tS + (uint32_t)(q * 32), pk);
+                        if constexpr (kSplit) tmem_st16(tS + (uint32_t)(q * 32 + 16), pr);
                     }
-                    tmem_st16(tS + (uint32_t)(q * 32), pk);
-                    if constexpr (kSplit) tmem_st16(tS + (uint32_t)(q * 32 + 16), pr);
-                }
+                };
+                if (full)
+                    weights(std::false_type{});
+                else
+                    weights(std::true_type{});
                 float rs0, rs1;
                 f2_split(rs2, rs0, rs1);
                 l = l * alpha + (rs0 + rs1);
