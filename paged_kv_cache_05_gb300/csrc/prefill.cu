@@ -321,6 +321,13 @@ __device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
     return d;
 }
 
+// 32 bytes to global memory in one instruction (32-byte aligned address)
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t* w) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]),
+                 "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
 // max / min of three values in one instruction
 __device__ __forceinline__ float max3(float a, float b, float c) {
     float d;
@@ -376,6 +383,7 @@ struct Pk<__nv_bfloat16> {
 
 struct PrefillArgs {
     void* out;
+    int out_v8;                  // out is 32-byte aligned: 32-byte stores
     const int32_t* block_tables;
     const int32_t* context_lens;
     const int32_t* query_start;
@@ -841,10 +849,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int e = 0; e < 16; ++e)
                         wv[e] = Pk<T>::pack_out(__uint_as_float(o[2 * e]) * inv,
                                                 __uint_as_float(o[2 * e + 1]) * inv);
-                    uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+                    if (a.out_v8) {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        dst[e] = make_uint4(wv[4 * e], wv[4 * e + 1], wv[4 * e + 2], wv[4 * e + 3]);
+                        for (int e = 0; e < 2; ++e)
+                            st_global_v8(orow + c * 32 + e * 16, wv + 8 * e);
+                    } else {
+                        uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            dst[e] =
+                                make_uint4(wv[4 * e], wv[4 * e + 1], wv[4 * e + 2], wv[4 * e + 3]);
+                    }
                 }
             }
             tc_fence_before();
@@ -982,6 +997,7 @@ pkv_status pkv_paged_attention_prefill(void* out, const void* q, const void* k_c
     }
     PrefillArgs a;
     a.out = out;
+    a.out_v8 = aligned(out, 32) ? 1 : 0;
     a.block_tables = block_tables;
     a.context_lens = context_lens;
     a.query_start = query_start;
