@@ -205,3 +205,29 @@ def test_prefill_workload_full_size_sampled(pkv):
                                   np.arange(n + 1, dtype=np.int32), spec.scale, "f16")
     attn_check(out[torch.from_numpy(grow).cuda()], ref,
                "prefill workload, %d sampled rows x %d heads" % (n, H))
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_prefill_output_16_byte_aligned(pkv, dtype):
+    """An output that is 16- but not 32-byte aligned takes the 16-byte stores:
+    the same bits as a 32-byte aligned output."""
+    import torch
+    rs = np.random.default_rng(960 + (dtype == "bf16"))
+    ctx, qlen, H, D, B = [300, 129, 64], [300, 60, 64], 4, 128, 16
+    case = random_case(rs, len(ctx), H, D, B, ctx, dtype)
+    qs = np.concatenate([[0], np.cumsum(qlen)]).astype(np.int32)
+    T = int(qs[-1])
+    q = to_dev(words((T, H, D), dtype, rs), dtype)
+    args = (q, to_dev(case["kc"], dtype), to_dev(case["vc"], dtype),
+            torch.from_numpy(case["bt"]).cuda(), torch.from_numpy(case["ctx"]).cuda(),
+            torch.from_numpy(qs).cuda(), 0.088, max(qlen))
+    a32 = torch.full_like(q, float("nan"))
+    pkv.paged_attention_prefill(a32, *args)
+    buf = torch.full((T * H * D + 8,), float("nan"), dtype=q.dtype, device="cuda")
+    a16 = buf[8:].view(T, H, D)                      # 16 bytes past a 256-byte boundary
+    assert a16.data_ptr() % 32 == 16
+    pkv.paged_attention_prefill(a16, *args)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == 0
+    assert torch.equal(a32.view(torch.int16), a16.view(torch.int16))
+    assert not torch.isnan(a32).any()
