@@ -530,8 +530,13 @@ def main():
                        "unit": "GB/s", "h2d_bytes_per_step": e2e["h2d"],
                        "d2h_bytes_per_step": e2e["d2h"], "steps": e2e["steps"],
                        "us_per_step": round(1e6 * e2e["seconds"] / e2e["steps"], 2),
-                       "how": "CUDA-graph replay per step: one pinned H2D copy of the step's "
-                              "inputs, the step's kernels, D2H of out, stream sync"}
+                       "serial_us_per_step": round(e2e["serial_us_per_step"], 2),
+                       "how": "CUDA-graph replay per step, pipelined over two input buffers: "
+                              "step i's kernels run while a copy stream brings step i+1's "
+                              "inputs from pinned host memory; step i's output is copied to "
+                              "pinned host memory and read by the host one step later; one "
+                              "H2D and one D2H per step in the timed region (serial_us_per_step: "
+                              "copy in, kernels, copy out, full sync, step by step)"}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl)
         line["cpu_baseline_single_thread"] = cpu_baseline(wl, single_thread=True)
@@ -542,12 +547,23 @@ def main():
 
 
 def measure_e2e(wl: Workload, steps: int, device, dist):
-    """End to end through the public API with host buffers, every step: the
-    step's inputs (q, new K/V, slot mapping, block tables, context lengths,
-    copy pairs) copied from pinned host memory in one transfer, the step's
-    kernels, the output copied back to pinned host memory, and a stream
-    synchronise.  Each layer's step is captured once in a CUDA graph (copies
-    and kernels); the timed loop replays the graphs."""
+    """End to end through the public API with host buffers.  Every step copies
+    its inputs (q, new K/V, slot mapping, block tables, context lengths, copy
+    pairs) from pinned host memory in one transfer, runs the step's kernels and
+    copies the output back to pinned host memory, where the host reads it.
+
+    Pipelined (the value reported): two device input buffers and two device
+    output buffers; step i's graph runs its kernels on input buffer i % 2 into
+    output buffer i % 2 while a copy stream fills the other input buffer with
+    step i + 1's inputs and copies step i - 1's output to pinned host memory;
+    the host reads step i - 1's output once step i's graph is done, and step
+    K - 1's output is copied after the loop, inside the timed region.  The
+    first step's inputs are copied before the timed region and the last
+    step's copy of the next inputs stands in for it; the first graph's output
+    copy (of no step) is an extra one, so the timed region holds one input
+    copy per step and one output copy per step plus one; the host reads every
+    step's output.  Serial (reported beside it): one graph per step, copy in,
+    kernels, copy out, then a full stream synchronise before the next step."""
     import torch
     parts = [("q", wl.q), ("k_new", wl.k_new), ("v_new", wl.v_new), ("slots", wl.slots),
              ("tables", wl.tables), ("ctx", wl.ctx), ("pairs", wl.pairs)]
@@ -557,49 +573,106 @@ def measure_e2e(wl: Workload, steps: int, device, dist):
         offs.append(o)
         o += (n + 255) // 256 * 256
     host = torch.empty(o, dtype=torch.uint8).pin_memory()
-    dev = torch.empty(o, dtype=torch.uint8, device=device)
-    views = {}
+    devs = [torch.empty(o, dtype=torch.uint8, device=device) for _ in range(2)]
+    views = [{}, {}]
     for (name, t), off, n in zip(parts, offs, sizes):
         host[off:off + n].copy_(t.detach().cpu().contiguous().view(-1).view(torch.uint8))
-        views[name] = dev[off:off + n].view(t.dtype).view(t.shape)
-    out_host = torch.empty(wl.out.shape, dtype=wl.out.dtype).pin_memory()
+        for b in range(2):
+            views[b][name] = devs[b][off:off + n].view(t.dtype).view(t.shape)
+    out_hosts = [torch.empty(wl.out.shape, dtype=wl.out.dtype).pin_memory() for _ in range(2)]
+    outs = [wl.out, torch.empty_like(wl.out)]
     h2d = sum(sizes)
-    d2h = out_host.numel() * out_host.element_size()
+    d2h = out_hosts[0].numel() * out_hosts[0].element_size()
     pkv = wl.pkv
+    layers = max(1, min(wl.layers, steps))
 
-    def body(layer):
-        dev.copy_(host, non_blocking=True)
+    def kernels(layer, v, out):
         kc, vc = wl.kc[layer], wl.vc[layer]
         if len(wl.pairs_host):
-            pkv.copy_blocks(kc, vc, views["pairs"])
-        pkv.reshape_and_cache(views["k_new"], views["v_new"], kc, vc, views["slots"])
-        pkv.paged_attention_decode(wl.out, views["q"], kc, vc, views["tables"], views["ctx"],
+            pkv.copy_blocks(kc, vc, v["pairs"])
+        pkv.reshape_and_cache(v["k_new"], v["v_new"], kc, vc, v["slots"])
+        pkv.paged_attention_decode(out, v["q"], kc, vc, v["tables"], v["ctx"],
                                    wl.scale, wl.partition, wl.ws)
-        out_host.copy_(wl.out, non_blocking=True)
 
-    layers = min(wl.layers, steps)
-    for layer in range(layers):           # first calls outside capture
-        body(layer)
-    torch.cuda.synchronize()
-    graphs = []
     side = torch.cuda.Stream(device=device)
+    cps = torch.cuda.Stream(device=device)
+
+    def body_pipelined(layer, p):
+        cur = torch.cuda.current_stream()
+        start = torch.cuda.Event()
+        start.record(cur)
+        cps.wait_event(start)
+        with torch.cuda.stream(cps):
+            devs[1 - p].copy_(host, non_blocking=True)       # the next step's inputs
+            out_hosts[1 - p].copy_(outs[1 - p], non_blocking=True)   # the previous step's output
+        copied = torch.cuda.Event()
+        copied.record(cps)
+        kernels(layer, views[p], outs[p])
+        cur.wait_event(copied)
+
+    def body_serial(layer):
+        devs[0].copy_(host, non_blocking=True)
+        kernels(layer, views[0], outs[0])
+        out_hosts[0].copy_(outs[0], non_blocking=True)
+
+    # first calls outside capture, then one graph per (layer, buffer parity)
+    # the timed loop meets, and one per layer for the serial form
+    keys = sorted({(i % layers, i % 2) for i in range(steps + 3)})
+    for layer, p in keys:
+        body_pipelined(layer, p)
+    for layer in range(layers):
+        body_serial(layer)
+    torch.cuda.synchronize()
+    pg, sg = {}, []
+    for key in keys:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            body_pipelined(*key)
+        pg[key] = g
     for layer in range(layers):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=side):
-            body(layer)
-        graphs.append(g)
+            body_serial(layer)
+        sg.append(g)
     torch.cuda.synchronize()
-    for i in range(3):
-        graphs[i % layers].replay()
+    evs = [torch.cuda.Event(), torch.cuda.Event()]
+    seen = 0.0
+
+    def run_pipelined(n):
+        nonlocal seen
+        devs[0].copy_(host)                                   # step 0's inputs
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(n):
+            pg[(i % layers, i % 2)].replay()
+            evs[i % 2].record()
+            if i > 1:
+                # graph i - 1 is done: step i - 2's output is on the host
+                evs[(i - 1) % 2].synchronize()
+                seen += float(out_hosts[i % 2].view(-1)[0])
+        last = (n - 1) % 2
+        out_hosts[last].copy_(outs[last], non_blocking=True)   # step n - 1's output
         torch.cuda.current_stream().synchronize()
+        seen += float(out_hosts[last].view(-1)[0])
+        if n > 1:
+            seen += float(out_hosts[1 - last].view(-1)[0])        # step n - 2's
+        return time.perf_counter() - t0
+
+    run_pipelined(3)
     if dist is not None:
         dist.barrier()
+    sec = run_pipelined(steps)
+    for i in range(3):
+        sg[i % layers].replay()
+        torch.cuda.current_stream().synchronize()
     t0 = time.perf_counter()
     for i in range(steps):
-        graphs[i % layers].replay()
+        sg[i % layers].replay()
         torch.cuda.current_stream().synchronize()
-    sec = time.perf_counter() - t0
-    return {"seconds": sec, "steps": steps, "h2d": h2d, "d2h": d2h}
+        seen += float(out_hosts[0].view(-1)[0])
+    sec_serial = time.perf_counter() - t0
+    return {"seconds": sec, "steps": steps, "h2d": h2d, "d2h": d2h,
+            "serial_us_per_step": 1e6 * sec_serial / steps}
 
 
 def measure_parts(wl: Workload, device, warmup: int) -> dict:
