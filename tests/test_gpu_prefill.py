@@ -231,3 +231,36 @@ def test_prefill_output_16_byte_aligned(pkv, dtype):
     assert pkv.get_device_error() == 0
     assert torch.equal(a32.view(torch.int16), a16.view(torch.int16))
     assert not torch.isnan(a32).any()
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_prefill_running_max_rises(pkv, dtype):
+    """Keys from position 128 on are 8x larger, so every row's running max
+    jumps by far more than the lazy-rescale margin at the second key tile (and
+    the output rescale and, where a row is redone, the recomputed weights are
+    exercised), on whole and continued prompts."""
+    import torch
+    rs = np.random.default_rng(970 + (dtype == "bf16"))
+    ctx, qlen, H, D, B = [600, 420], [600, 200], 2, 64, 16
+    case = random_case(rs, len(ctx), H, D, B, ctx, dtype)
+    kc = case["kc"].copy()
+    fl = (lambda w: w.view(np.float16).astype(np.float32)) if dtype == "f16" else \
+        (lambda w: (w.astype(np.uint32) << 16).view(np.float32))
+    to_w = (lambda f: f.astype(np.float16).view(np.uint16)) if dtype == "f16" else \
+        (lambda f: (f.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16))
+    for s, n in enumerate(ctx):
+        for t in range(128, n):
+            b = case["bt"][s, t // B]
+            kc[b, :, t % B, :] = to_w(fl(kc[b, :, t % B, :]) * 8.0)
+    qs = np.concatenate([[0], np.cumsum(qlen)]).astype(np.int32)
+    T = int(qs[-1])
+    q = words((T, H, D), dtype, rs)
+    scale = float(np.float32(1 / math.sqrt(D)))
+    ref = prefill_oracle_threaded(q, kc, case["vc"], case["bt"], case["ctx"], qs, scale, dtype)
+    out = torch.full((T, H, D), float("nan"), dtype=W.torch_dtype(dtype), device="cuda")
+    pkv.paged_attention_prefill(out, to_dev(q, dtype), to_dev(kc, dtype), to_dev(case["vc"], dtype),
+                                torch.from_numpy(case["bt"]).cuda(),
+                                torch.from_numpy(case["ctx"]).cuda(), torch.from_numpy(qs).cuda(),
+                                scale, max(qlen))
+    assert pkv.get_device_error() == 0
+    attn_check(out, ref, "prefill rising max dtype=%s" % dtype)
