@@ -55,19 +55,23 @@ def read_peaks():
         return FALLBACK_HBM_GBS, FALLBACK_NOTE
 
 
-def kernel_source_digest() -> str:
+def kernel_source_digest(files=("decode_kernel.cuh", "decode_api.cu", "pkv_internal.h")) -> str:
     import hashlib
     h = hashlib.sha256()
-    for f in ("decode_kernel.cuh", "decode_api.cu", "pkv_internal.h"):
+    for f in files:
         with open(os.path.join(ROOT, "paged_kv_cache_05_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
-    """DRAM bytes per decode launch from the committed ncu summary, if it was
-    taken on the current kernel source (else None)."""
-    p = os.path.join(ROOT, "profiles", "paged_decode_main_%s.md" % workload)
+PREFILL_SOURCES = ("prefill.cu", "pkv_internal.h")
+
+
+def profiled_traffic(workload: str, profile: str = None, sources=None):
+    """DRAM bytes per launch from the committed ncu summary (the decode
+    kernel's for the workload, or the named profile), if it was taken on the
+    current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", profile or ("paged_decode_main_%s.md" % workload))
     if not os.path.exists(p):
         return None
     kv = {}
@@ -75,7 +79,8 @@ def profiled_traffic(workload: str):
         if ":" in line and line.strip().startswith("- "):
             k, v = line.strip()[2:].split(":", 1)
             kv[k.strip()] = v.strip().strip("`")
-    if kv.get("kernel_source_sha256_16") != kernel_source_digest():
+    digest = kernel_source_digest(sources) if sources else kernel_source_digest()
+    if kv.get("kernel_source_sha256_16") != digest:
         return None
     try:
         return float(kv["dram_bytes_per_launch_full_size"])
@@ -861,6 +866,9 @@ def bench_prefill(args):
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
+    sampler = ClockSampler(0)
+    sampler.start()
+    time.sleep(0.3)                       # let the sampler start before the timed region
     K = max(10, args.steps // 20)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record()
@@ -875,6 +883,7 @@ def bench_prefill(args):
     b.record()
     torch.cuda.synchronize()
     t_attn = a.elapsed_time(b) / K * 1e-3
+    clocks = sampler.stop()
     if pkv.get_device_error() != 0:
         raise SystemExit("bench.py --op prefill: device error bits")
     flops = float(sum(4.0 * D * H * (c * (c + 1) / 2.0) for c in ctx))
@@ -894,8 +903,11 @@ def bench_prefill(args):
                    "flops_per_call": flops},
         "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(tf / peak, 4), "peak_source": src,
+                     "traffic": profiled_traffic("prefill", "paged_prefill_tc_prefill.md",
+                                                 PREFILL_SOURCES),
                      "note": "tcgen05.mma kind::f16 from shared-memory descriptors, S and O in "
                              "tensor memory, TMA tiled copies through the block table"},
+        "clocks": clocks,
     }), flush=True)
 
 
