@@ -110,24 +110,32 @@ def spread(ctx, n):
     return sorted(int(order[i]) for i in pick)
 
 
-def prefill_oracle_threaded(q, kc, vc, bt, ctx, qs, scale, dtype: str, threads: int = 8):
-    """The prompt-phase oracle, one sequence per call, calls spread over host
-    threads (the C routine runs without the GIL).  Each call is the unchanged
-    oracle on that sequence alone: its table row, context and query rows."""
+def prefill_oracle_threaded(q, kc, vc, bt, ctx, qs, scale, dtype: str, threads: int = 8,
+                            rows_per_call: int = 32):
+    """The prompt-phase oracle on pieces of at most rows_per_call query rows,
+    spread over host threads (the C routine runs without the GIL).  Each piece
+    is the unchanged oracle on one sequence: rows a .. b-1 of a sequence with
+    context n and qlen new tokens are the new tokens of the same sequence cut
+    at context n - qlen + b (the rows attend positions up to their own)."""
     import threading
     T = int(qs[-1])
     H, D = kc.shape[1], kc.shape[3]
     out = np.zeros((T, H, D), np.float64)
-    todo = sorted((s for s in range(len(ctx)) if qs[s + 1] > qs[s]),
-                  key=lambda s: -(int(qs[s + 1] - qs[s]) * int(ctx[s])))
+    pieces = []
+    for s in range(len(ctx)):
+        q0, q1 = int(qs[s]), int(qs[s + 1])
+        n, ql = int(ctx[s]), q1 - q0
+        for a in range(0, ql, rows_per_call):
+            b = min(a + rows_per_call, ql)
+            pieces.append((s, q0 + a, q0 + b, n - ql + b))
+    pieces.sort(key=lambda p: -(p[2] - p[1]) * p[3])
     errs = []
 
     def worker(i):
         try:
-            for s in todo[i::threads]:
-                a, b = int(qs[s]), int(qs[s + 1])
+            for s, a, b, n_cut in pieces[i::threads]:
                 out[a:b] = oracle.paged_attention_prefill(
-                    q[a:b], kc, vc, bt[s:s + 1], np.array([ctx[s]], np.int32),
+                    q[a:b], kc, vc, bt[s:s + 1], np.array([n_cut], np.int32),
                     np.array([0, b - a], np.int32), scale, ORC_DTYPE[dtype])
         except Exception as e:  # surfaced below
             errs.append(e)

@@ -45,7 +45,7 @@ def run_case(pkv, rs, ctx, qlen, H, D, B, dtype):
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("D", [64, 128])
-@pytest.mark.parametrize("B", [8, 16, 64])
+@pytest.mark.parametrize("B", [8, 16, 32, 64])
 def test_prefill_parity(pkv, dtype, D, B):
     rs = np.random.default_rng(600 + D + B + (dtype == "bf16"))
     # (context, new tokens): whole prompts, continued prompts, one-token rows
@@ -264,3 +264,12 @@ def test_prefill_running_max_rises(pkv, dtype):
                                 scale, max(qlen))
     assert pkv.get_device_error() == 0
     attn_check(out, ref, "prefill rising max dtype=%s" % dtype)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_prefill_long_context_continued(pkv, dtype):
+    """300 new tokens after a 5,700-token cached prefix (about 47 key tiles per
+    item), next to a short whole prompt: the long key loop, its running max and
+    rescales, and the last partial block."""
+    rs = np.random.default_rng(980 + (dtype == "bf16"))
+    run_case(pkv, rs, [6000, 90], [300, 90], 2, 128, 16, dtype)
