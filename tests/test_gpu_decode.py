@@ -252,3 +252,50 @@ def test_dynamic_tail_repeated_calls_and_graph_replay(pkv):
         torch.cuda.synchronize()
         assert pkv.get_device_error() == 0
         attn_check(out, ref, "replay %d" % i)
+
+
+@pytest.mark.parametrize("partition", [0, 512])
+def test_large_batch(pkv, partition):
+    """4,000 short sequences (about 32 KiB of per-sequence lengths and step
+    offsets in each CTA's shared memory, so fewer CTAs fit an SM), ragged
+    lengths with empty rows, balanced and fixed splits."""
+    rs = np.random.default_rng(1200 + partition)
+    S = 4000
+    ctx = [int(c) for c in rs.integers(0, 70, size=S)]
+    case = random_case(rs, S, 2, 64, 16, ctx, "f16")
+    scale = float(np.float32(1 / math.sqrt(64)))
+    ref = oracle.paged_attention_decode_threaded(
+        case["q"], case["kc"], case["vc"], case["bt"], case["ctx"], scale, ORC_DTYPE["f16"],
+        threads=8)
+    out = run_gpu(pkv, case, scale, partition)
+    attn_check(out, ref, "large batch partition=%d" % partition)
+    zero = [s for s in range(S) if ctx[s] == 0]
+    assert zero and (out[zero] == 0).all()
+
+
+def test_batch_size_limit(pkv):
+    """The largest batch the ABI takes (16,384 sequences, whose per-sequence
+    arrays fill most of a CTA's shared memory, one CTA per SM) matches the
+    oracle; one more sequence is refused on the host, nothing launched."""
+    import torch
+    rs = np.random.default_rng(1300)
+    S = 16384
+    ctx = [int(c) for c in rs.integers(0, 40, size=S)]
+    case = random_case(rs, S, 1, 64, 16, ctx, "f16")
+    scale = 0.125
+    ref = oracle.paged_attention_decode_threaded(
+        case["q"], case["kc"], case["vc"], case["bt"], case["ctx"], scale, ORC_DTYPE["f16"],
+        threads=8)
+    out = run_gpu(pkv, case, scale)
+    attn_check(out, ref, "16384 sequences")
+    S1 = S + 1
+    q = torch.zeros((S1, 1, 64), dtype=torch.float16, device="cuda")
+    kc = torch.zeros((S1, 1, 16, 64), dtype=torch.float16, device="cuda")
+    bt = torch.arange(S1, dtype=torch.int32, device="cuda").view(S1, 1)
+    cl = torch.ones(S1, dtype=torch.int32, device="cuda")
+    o1 = torch.full_like(q, float("nan"))
+    with pytest.raises(pkv.PagedKVError) as ei:
+        pkv.paged_attention_decode(o1, q, kc, kc, bt, cl, scale)
+    assert ei.value.status == 1 and "num_seqs" in str(ei.value)
+    torch.cuda.synchronize()
+    assert torch.isnan(o1).all() and pkv.get_device_error() == 0
