@@ -379,6 +379,8 @@ def main():
                     help="step: the decode layer-step (default); swap: block swap GPU<->CPU; "
                          "sharing: memory saved by block sharing (host only)")
     ap.add_argument("--workload", default="opt13b", choices=sorted(W.SPECS))
+    ap.add_argument("--dtype", choices=["f16", "bf16"], default="f16",
+                    help="storage type of q and the caches for --op prefill")
     ap.add_argument("--partition", type=int, default=None,
                     help="split length in tokens (0 = balanced); default: the workload's")
     ap.add_argument("--block-size", type=int, default=None)
@@ -844,11 +846,12 @@ def bench_prefill(args):
     maxb = max(-(-int(c) // B) for c in ctx)
     tables, _ = bm.export(list(range(S)), maxb)
     T = int(ctx.sum())
-    kc = torch.zeros((nb, H, B, D), dtype=torch.float16, device=dev)
+    dt = getattr(args, "dtype", "f16")
+    kc = torch.zeros((nb, H, B, D), dtype=W.torch_dtype(dt), device=dev)
     vc = torch.zeros_like(kc)
-    k = W.device_normal((T, H, D), "f16", spec.seed + 1, dev)
-    v = W.device_normal((T, H, D), "f16", spec.seed + 2, dev)
-    q = W.device_normal((T, H, D), "f16", spec.seed + 3, dev)
+    k = W.device_normal((T, H, D), dt, spec.seed + 1, dev)
+    v = W.device_normal((T, H, D), dt, spec.seed + 2, dev)
+    q = W.device_normal((T, H, D), dt, spec.seed + 3, dev)
     out = torch.empty_like(q)
     qs = torch.from_numpy(np.concatenate([[0], np.cumsum(ctx)]).astype(np.int32)).to(dev)
     bt = torch.from_numpy(tables).to(dev)
@@ -897,14 +900,15 @@ def bench_prefill(args):
         "op": "prefill", "metric": "prompt-phase paged attention TFLOP/s", "unit": "TFLOP/s",
         "value": round(tf, 1), "us_per_call": round(t_attn * 1e6, 1),
         "us_per_step_with_cache_write": round(t_step * 1e6, 1),
-        "tokens_per_s": round(T / t_step, 1), "dtype": "f16 in, f32 accumulate",
+        "tokens_per_s": round(T / t_step, 1), "dtype": "%s in, f32 accumulate" % dt,
         "config": {"workload": "prefill: %d prompts, lengths %d..%d (sum %d), 40 heads x 128, "
-                               "B=16, fp16" % (S, int(ctx.min()), int(ctx.max()), T),
+                               "B=16, %s" % (S, int(ctx.min()), int(ctx.max()), T,
+                                                                {"f16": "fp16", "bf16": "bf16"}[dt]),
                    "flops_per_call": flops},
         "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(tf / peak, 4), "peak_source": src,
                      "traffic": profiled_traffic("prefill", "paged_prefill_tc_prefill.md",
-                                                 PREFILL_SOURCES),
+                                                 PREFILL_SOURCES) if dt == "f16" else None,
                      "note": "tcgen05.mma kind::f16 from shared-memory descriptors, S and O in "
                              "tensor memory, TMA tiled copies through the block table"},
         "clocks": clocks,
