@@ -37,6 +37,27 @@ def test_reshape_and_cache_bit_exact(pkv, dtype, D, B):
     assert np.array_equal(W.torch_to_words(dv), vc)
 
 
+@pytest.mark.parametrize("D,T", [(64, 20011), (128, 10007)])
+def test_reshape_and_cache_many_rows(pkv, D, T):
+    """Enough (token, head) rows that every CTA of the one-wave grid strides
+    over them several times, the last pass partial."""
+    import torch
+    rs = np.random.default_rng(D + T)
+    H, B = 8, 16
+    nb = -(-T // B) + 3
+    kc, vc = words((nb, H, B, D), "f16", rs), words((nb, H, B, D), "f16", rs)
+    k, v = words((T, H, D), "f16", rs), words((T, H, D), "f16", rs)
+    slots = rs.permutation(nb * B)[:T].astype(np.int64)
+    slots[rs.random(T) < 0.05] = -1
+    dk, dv = to_dev(kc, "f16"), to_dev(vc, "f16")
+    pkv.reshape_and_cache(to_dev(k, "f16"), to_dev(v, "f16"), dk, dv,
+                          torch.from_numpy(slots).cuda())
+    assert pkv.get_device_error() == 0
+    oracle.reshape_and_cache(k, v, kc, vc, slots)
+    assert np.array_equal(W.torch_to_words(dk), kc)
+    assert np.array_equal(W.torch_to_words(dv), vc)
+
+
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("H,D,B", [(8, 64, 16), (40, 128, 16), (3, 128, 64), (2, 64, 8)])
 def test_copy_blocks_bit_exact(pkv, dtype, H, D, B):
