@@ -481,7 +481,12 @@ def main():
 
     peak, peak_note = read_peaks()
     achieved = wl.attn_bytes / (attn_avg * 1e-3) / 1e9
-    traffic = profiled_traffic(args.workload)
+    # the committed capture is of the workload as specified (its block size,
+    # the balanced split, scattered blocks)
+    traffic = (profiled_traffic(args.workload)
+               if args.block_size in (None, W.SPECS[args.workload].block_size)
+               and args.partition in (None, W.SPECS[args.workload].partition_size)
+               and args.placement == "scattered" else None)
     line = {
         "metric": "paged-attn decode: achieved HBM GB/s (% of GB300 peak), us/layer-step at OPT-13B",
         "value": round(value, 1),
