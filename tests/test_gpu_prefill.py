@@ -234,13 +234,17 @@ def test_prefill_output_16_byte_aligned(pkv, dtype):
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-def test_prefill_running_max_rises(pkv, dtype):
-    """Keys from position 128 on are 8x larger, so every row's running max
-    jumps by far more than the lazy-rescale margin at the second key tile (and
-    the output rescale and, where a row is redone, the recomputed weights are
-    exercised), on whole and continued prompts."""
+@pytest.mark.parametrize("jumps", [((128, 8.0),), ((48, 8.0),), ((40, 4.0), (200, 16.0))],
+                         ids=["tile-start", "mid-tile", "two-rises"])
+def test_prefill_running_max_rises(pkv, dtype, jumps):
+    """Keys from a position on are several times larger, so a row's running
+    max jumps by far more than the lazy-rescale margin: at the start of the
+    second key tile, inside the first (a quarter of 32 keys after others of the
+    same tile), or twice (inside the first tile and inside the second).  The
+    output rescale, the row-sum rescale and any rescale of weights already
+    written for the tile are exercised, on whole and continued prompts."""
     import torch
-    rs = np.random.default_rng(970 + (dtype == "bf16"))
+    rs = np.random.default_rng(970 + (dtype == "bf16") + 7 * len(jumps) + jumps[0][0])
     ctx, qlen, H, D, B = [600, 420], [600, 200], 2, 64, 16
     case = random_case(rs, len(ctx), H, D, B, ctx, dtype)
     kc = case["kc"].copy()
@@ -248,10 +252,11 @@ def test_prefill_running_max_rises(pkv, dtype):
         (lambda w: (w.astype(np.uint32) << 16).view(np.float32))
     to_w = (lambda f: f.astype(np.float16).view(np.uint16)) if dtype == "f16" else \
         (lambda f: (f.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16))
-    for s, n in enumerate(ctx):
-        for t in range(128, n):
-            b = case["bt"][s, t // B]
-            kc[b, :, t % B, :] = to_w(fl(kc[b, :, t % B, :]) * 8.0)
+    for start, factor in jumps:
+        for s, n in enumerate(ctx):
+            for t in range(start, n):
+                b = case["bt"][s, t // B]
+                kc[b, :, t % B, :] = to_w(fl(kc[b, :, t % B, :]) * factor)
     qs = np.concatenate([[0], np.cumsum(qlen)]).astype(np.int32)
     T = int(qs[-1])
     q = words((T, H, D), dtype, rs)
@@ -263,7 +268,7 @@ def test_prefill_running_max_rises(pkv, dtype):
                                 torch.from_numpy(case["ctx"]).cuda(), torch.from_numpy(qs).cuda(),
                                 scale, max(qlen))
     assert pkv.get_device_error() == 0
-    attn_check(out, ref, "prefill rising max dtype=%s" % dtype)
+    attn_check(out, ref, "prefill rising max %s dtype=%s" % (jumps, dtype))
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
