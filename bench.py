@@ -40,6 +40,7 @@ sys.path.insert(0, ROOT)
 
 from paged_kv_cache_05_gb300 import workloads as W  # noqa: E402
 
+METRIC = "paged-attn decode: achieved HBM GB/s (% of GB300 peak), us/layer-step at OPT-13B"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_NOTE = "fallback (MEASURED_PEAKS.json absent): one earlier GB300 copy measurement"
 
@@ -248,7 +249,8 @@ class Workload:
         self.ws = pkv.alloc_workspace(S, H, D, B, self.max_blocks, self.partition, dev)
         self.scale = spec.scale
         e = 2
-        self.attn_bytes = (int(ctx.astype(np.int64).sum()) * H * D * 2 * e + 2 * S * H * D * e
+        self.kv_bytes = int(ctx.astype(np.int64).sum()) * H * D * 2 * e
+        self.attn_bytes = (self.kv_bytes + 2 * S * H * D * e
                            + sum(-(-int(c) // B) for c in ctx) * 4 + 4 * S)
         self.reshape_bytes = 2 * (2 * S * H * D * e)
         self.copy_bytes = len(pairs) * 2 * 2 * H * B * D * e
@@ -288,57 +290,94 @@ class Workload:
 
 
 # ------------------------------------------------------------------ oracle leg
-def oracle_sample(wl: Workload, seqs=None):
-    """Host copies of the blocks a subset of the workload's sequences use (all
-    heads, layer 0), for the CPU oracle; default: every sequence."""
-    import torch
-    pick = list(range(wl.S)) if seqs is None else sorted(seqs)
-    B = wl.B
-    used = sorted(set(int(b) for s in pick
-                      for b in wl.tables_host[s, :-(-int(wl.ctx_host[s]) // B)]))
+def host_case(name: str, block_size=None):
+    """The workload's block tables and context lengths built on the host
+    only, by the oracle's own model of the block manager (the same seeded
+    policy and the same sequence of operations as the device workload: every
+    sequence holds ctx - 1 tokens, then one decode step appends its newest;
+    shared prefixes are forked and their suffixes appended round-robin).  No
+    product library is loaded."""
+    from oracle.block_manager import BlockManagerModel
+    spec = W.SPECS[name]
+    B = block_size or spec.block_size
+    ctx = W.context_lens(spec)
+    m = BlockManagerModel(W.pool_blocks(spec, ctx, B), B, spec.seed)
+    S = spec.num_seqs
+    if name == "shared_prefix":
+        p_len, s_len = W.prompt_and_suffix_lens(spec)
+        g = spec.extra["per_group"]
+        for gi in range(len(p_len)):
+            m.add_sequence(gi * g, int(p_len[gi]))
+            for c in range(1, g):
+                m.fork(gi * g, gi * g + c)
+        for t in range(int(s_len.max())):
+            for s_ in range(S):
+                if t < s_len[s_]:
+                    m.append_slot(s_)
+    else:
+        for s_ in range(S):
+            m.add_sequence(s_, int(ctx[s_]) - 1)
+        for s_ in range(S):
+            m.append_slot(s_)
+    tables = [m.block_table(s_) for s_ in range(S)]
+    assert [m.context_len(s_) for s_ in range(S)] == [int(c) for c in ctx]
+    return dict(spec=spec, B=B, ctx=ctx, tables=tables)
+
+
+def oracle_sample(hc: dict, seqs=None, tile_blocks: int = 256):
+    """Oracle inputs for a subset of a host case's sequences (all heads):
+    their tables renumbered over the blocks they use, and pools of seeded
+    host values (tile_blocks random blocks repeated over the blocks in use:
+    the oracle's cost does not depend on the values)."""
+    spec, B, ctx = hc["spec"], hc["B"], hc["ctx"]
+    pick = list(range(spec.num_seqs)) if seqs is None else sorted(seqs)
+    used = sorted(set(int(b) for s in pick for b in hc["tables"][s]))
     remap = {b: i for i, b in enumerate(used)}
-    idx = torch.tensor(used, dtype=torch.long, device=wl.kc[0].device)
-    kc = W.torch_to_words(wl.kc[0].index_select(0, idx))
-    vc = W.torch_to_words(wl.vc[0].index_select(0, idx))
-    q = W.torch_to_words(wl.q[torch.tensor(pick, device=wl.q.device)])
-    mb = max(1, max(-(-int(wl.ctx_host[s]) // B) for s in pick))
+    H, D = spec.num_heads, spec.head_dim
+    n = len(used)
+    kc, vc = (np.resize(W.normal_words((min(n, tile_blocks), H, B, D), spec.dtype, spec.seed,
+                                       40 + k), (n, H, B, D)) for k in range(2))
+    q = W.normal_words((len(pick), H, D), spec.dtype, spec.seed, 42)
+    mb = max(1, max(len(hc["tables"][s]) for s in pick))
     bt = np.full((len(pick), mb), -1, np.int32)
     for i, s in enumerate(pick):
-        n = -(-int(wl.ctx_host[s]) // B)
-        bt[i, :n] = [remap[int(b)] for b in wl.tables_host[s, :n]]
-    cl = wl.ctx_host[pick].astype(np.int32)
-    H, D, e = wl.H, wl.D, 2
+        bt[i, :len(hc["tables"][s])] = [remap[int(b)] for b in hc["tables"][s]]
+    cl = ctx[pick].astype(np.int32)
+    e = 2
     nbytes = (int(cl.astype(np.int64).sum()) * H * D * 2 * e + 2 * len(pick) * H * D * e
               + sum(-(-int(c) // B) for c in cl) * 4 + 4 * len(pick))
-    return dict(q=q, kc=kc, vc=vc, bt=bt, cl=cl, bytes=nbytes, seqs=len(pick), heads=H)
+    return dict(q=q, kc=kc, vc=vc, bt=bt, cl=cl, bytes=nbytes, seqs=len(pick), heads=H,
+                scale=spec.scale, dtype=spec.dtype)
 
 
-def run_oracle(sample, scale, dtype, threads):
+def run_oracle(sample, threads):
     import oracle
-    dt = oracle.F16 if dtype == "f16" else oracle.BF16
+    dt = oracle.F16 if sample["dtype"] == "f16" else oracle.BF16
     t0 = time.perf_counter()
     oracle.paged_attention_decode_threaded(sample["q"], sample["kc"], sample["vc"], sample["bt"],
-                                           sample["cl"], float(np.float32(scale)), dt,
+                                           sample["cl"], float(np.float32(sample["scale"])), dt,
                                            threads=threads)
     return time.perf_counter() - t0
 
 
-def sized_sample(wl: Workload, budget_s: float, threads: int):
+def sized_sample(hc: dict, budget_s: float, threads: int):
     """The largest length-spread subset of sequences whose oracle pass is
     expected to fit in budget_s (calibrated on a small subset), at least one."""
-    order = [int(i) for i in np.argsort(wl.ctx_host, kind="stable")]
-    probe = sorted(order[::max(1, wl.S // 8)])
-    p = oracle_sample(wl, probe)
-    t = run_oracle(p, wl.scale, wl.dtype, threads)
-    per_byte = t / p["bytes"] * max(1, min(threads, len(probe))) / max(1, min(threads, wl.S))
+    ctx, S = hc["ctx"], hc["spec"].num_seqs
+    order = [int(i) for i in np.argsort(ctx, kind="stable")]
+    probe = sorted(order[::max(1, S // 8)])
+    p = oracle_sample(hc, probe)
+    t = run_oracle(p, threads)
+    per_byte = t / p["bytes"] * max(1, min(threads, len(probe))) / max(1, min(threads, S))
     allowed = budget_s / max(per_byte, 1e-15)
-    take, acc = [], 0
-    for k in range(1, wl.S + 1):
-        sel = sorted(order[::max(1, wl.S // k)])[:k]
-        b = sum(int(wl.ctx_host[s]) for s in sel) * wl.H * wl.D * 4
+    take = []
+    spec = hc["spec"]
+    for k in range(1, S + 1):
+        sel = sorted(order[::max(1, S // k)])[:k]
+        b = sum(int(ctx[s]) for s in sel) * spec.num_heads * spec.head_dim * 4
         if b > allowed and take:
             break
-        take, acc = sel, b
+        take = sel
     return take
 
 def max_over_ranks(x: float, dist) -> float:
@@ -390,6 +429,12 @@ def main():
                          "or every sequence's blocks consecutive (contiguous baseline)")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--roofline-seconds", type=float, default=0.5,
+                    help="length of the roofline region (back-to-back attention calls; at "
+                         "least --steps calls)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other workloads' block (long, short, shared prefix, prompt "
+                         "phase)")
     args = ap.parse_args()
 
     import torch
@@ -428,17 +473,18 @@ def main():
                   args.placement)
     stream = torch.cuda.current_stream()
 
+    K = args.steps
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(device.index if device.index is not None else 0)
+    sampler.start()
+    time.sleep(0.3)                       # let the sampler start before the GPU work
+    # the W warm-up steps run right before the timed region, so that the GPU
+    # is not left idle (clocks ramping down) between them
     for i in range(args.warmup):
         wl.step(i)
     torch.cuda.synchronize()
     if wl.pkv.get_device_error() != 0:
         raise SystemExit("bench.py: device error bits after warm-up")
-
-    K = args.steps
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(device.index if device.index is not None else 0)
-    sampler.start()
-    time.sleep(0.3)                       # let the sampler start before the timed region
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
@@ -449,11 +495,14 @@ def main():
         wl.step(args.warmup + i)
     t_end.record(stream)
     torch.cuda.synchronize()
-    # timed region 2: K launches of the dominant operation alone, bracketed
-    # by events on the launching stream: its average duration per launch
+    # timed region 2: back-to-back launches of the dominant operation alone
+    # (at least K, and at least --roofline-seconds of them, so that the
+    # clock record covers it), bracketed by events on the launching stream:
+    # its average duration per launch
+    n_attn = attention_calls(wl, K, args.roofline_seconds, stream)
     a_start, a_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a_start.record(stream)
-    for i in range(K):
+    for i in range(n_attn):
         wl.attention(args.warmup + i)
     a_end.record(stream)
     torch.cuda.synchronize()
@@ -461,7 +510,7 @@ def main():
         dist.barrier()
     clocks = sampler.stop()
     ms_total = max_over_ranks(t_start.elapsed_time(t_end), dist)
-    attn_avg = a_start.elapsed_time(a_end) / K
+    attn_avg = a_start.elapsed_time(a_end) / n_attn
     ms_step = ms_total / K
     value = whole_job_rate(wl.step_bytes, ms_step * 1e-3, world)
 
@@ -471,8 +520,10 @@ def main():
     parts = measure_parts(wl, device, args.warmup)
 
     # ---- end to end: host (pinned) inputs -> C ABI -> host output, every step
-    e2e = None
+    e2e = api = None
     if args.e2e_steps > 0:
+        api = measure_e2e_api(wl, args.e2e_steps, device, dist)
+        api["seconds"] = max_over_ranks(api["seconds"], dist)
         e2e = measure_e2e(wl, args.e2e_steps, device, dist)
         e2e["seconds"] = max_over_ranks(e2e["seconds"], dist)
 
@@ -488,7 +539,7 @@ def main():
                and args.partition in (None, W.SPECS[args.workload].partition_size)
                and args.placement == "scattered" else None)
     line = {
-        "metric": "paged-attn decode: achieved HBM GB/s (% of GB300 peak), us/layer-step at OPT-13B",
+        "metric": METRIC,
         "value": round(value, 1),
         "unit": "GB/s",
         "n_gpus": world,
@@ -530,32 +581,322 @@ def main():
                              "launches (2 kernels each) for the roofline" % (
                                  wl.launches_per_step,
                                  "copy_blocks, " * bool(len(wl.pairs_host))
-                                 + "reshape_and_cache, paged_decode_main, paged_decode_merge", K),
+                                 + "reshape_and_cache, paged_decode_main, paged_decode_merge",
+                                 n_attn),
+        "roofline_region": {"calls": n_attn, "ms": round(attn_avg * n_attn, 2)},
         "clocks": clocks,
         "parts": parts,
     }
     if wl.unique_kv_bytes is not None:
         line["config"]["unique_kv_bytes"] = wl.unique_kv_bytes
     if e2e is not None:
-        line["e2e"] = {"value": round(whole_job_rate(wl.step_bytes, e2e["seconds"] / e2e["steps"],
+        api_us = 1e6 * api["seconds"] / api["steps"]
+        line["api_us_per_step"] = round(api_us, 2)
+        line["e2e"] = {"value": round(whole_job_rate(wl.step_bytes, api["seconds"] / api["steps"],
                                                     world), 1),
-                       "unit": "GB/s", "h2d_bytes_per_step": e2e["h2d"],
-                       "d2h_bytes_per_step": e2e["d2h"], "steps": e2e["steps"],
-                       "us_per_step": round(1e6 * e2e["seconds"] / e2e["steps"], 2),
+                       "unit": "GB/s", "h2d_bytes_per_step": api["h2d"],
+                       "d2h_bytes_per_step": api["d2h"], "steps": api["steps"],
+                       "us_per_step": round(api_us, 2),
+                       "host_issue_us_per_step": round(api["host_issue_us_per_step"], 2),
+                       "graph_us_per_step": round(1e6 * e2e["seconds"] / e2e["steps"], 2),
+                       "graph_value": round(whole_job_rate(
+                           wl.step_bytes, e2e["seconds"] / e2e["steps"], world), 1),
                        "serial_us_per_step": round(e2e["serial_us_per_step"], 2),
-                       "how": "CUDA-graph replay per step, pipelined over two input buffers: "
-                              "step i's kernels run while a copy stream brings step i+1's "
-                              "inputs from pinned host memory; step i's output is copied to "
-                              "pinned host memory and read by the host one step later; one "
-                              "H2D and one D2H per step in the timed region (serial_us_per_step: "
-                              "copy in, kernels, copy out, full sync, step by step)"}
+                       "how": "every step issued from the host through the public API (the "
+                              "Python binding of the C ABI: copy_blocks, reshape_and_cache, "
+                              "paged_attention_decode), pipelined over two input and two "
+                              "output buffers: a copy stream brings step i+1's inputs from "
+                              "pinned host memory and copies step i-1's output to pinned host "
+                              "memory while step i's kernels run; the host reads every byte of "
+                              "each step's output (a checksum) two steps later; wall clock "
+                              "over all steps.  graph_us_per_step: the same pipeline with each "
+                              "step's calls captured once in a CUDA graph and replayed; "
+                              "serial_us_per_step: copy in, kernels, copy out, full sync, step "
+                              "by step (graphs)"}
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(wl)
-        line["cpu_baseline_single_thread"] = cpu_baseline(wl, single_thread=True)
+        line["cpu_baseline"] = cpu_baseline(args.workload)
+        line["cpu_baseline_single_thread"] = cpu_baseline(args.workload, single_thread=True)
+    if not args.no_configs and args.placement == "scattered" and args.workload == "opt13b" \
+            and args.block_size is None and args.partition is None:
+        del wl
+        import gc
+        gc.collect()
+        torch.cuda.empty_cache()
+        line["configs"] = measure_configs(device, args.roofline_seconds, args.warmup, dist,
+                                          attn_avg * 1e3)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def attention_calls(wl: Workload, at_least: int, seconds: float, stream) -> int:
+    """How many back-to-back attention calls fill `seconds` (from a short
+    timed probe), at least `at_least`."""
+    import torch
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(20):
+        wl.attention(i)
+    b.record(stream)
+    torch.cuda.synchronize()
+    per = a.elapsed_time(b) / 20 * 1e-3
+    return max(at_least, int(math.ceil(seconds / max(per, 1e-7))))
+
+
+def timed_attention(wl: Workload, seconds: float, warmup: int, device, partition=None,
+                    ws=None) -> dict:
+    """Back-to-back attention calls (about `seconds` of them) between two events
+    on the launching stream, with nvidia-smi clock samples over the region."""
+    import torch
+    stream = torch.cuda.current_stream()
+
+    def call(i):
+        layer = i % wl.layers
+        wl.pkv.paged_attention_decode(wl.out, wl.q, wl.kc[layer], wl.vc[layer], wl.tables, wl.ctx,
+                                      wl.scale, wl.partition if partition is None else partition,
+                                      wl.ws if ws is None else ws)
+
+    for i in range(max(3, warmup)):
+        call(i)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(20):
+        call(i)
+    b.record(stream)
+    torch.cuda.synchronize()
+    n = max(20, int(math.ceil(seconds / max(a.elapsed_time(b) / 20 * 1e-3, 1e-7))))
+    sampler = ClockSampler(device.index if device.index is not None else 0)
+    sampler.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for i in range(n):
+        call(i)
+    b.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if wl.pkv.get_device_error() != 0:
+        raise SystemExit("bench.py: device error bits in the configs block")
+    us = a.elapsed_time(b) / n * 1e3
+    return {"calls": n, "us": us, "clocks": clocks}
+
+
+def timed_contiguous(name: str, device, seconds: float, warmup: int) -> dict:
+    """The decode attention over a contiguous [S][H][T][D] K/V layout (T = the
+    batch's longest context; no block table) for the workload's batch, split
+    and dtype, timed like the paged call.  Algorithmic bytes: the paged
+    call's without the table entries."""
+    import torch
+    import paged_kv_cache_05_gb300 as pkv
+    spec = W.SPECS[name]
+    ctx = W.context_lens(spec)
+    S, H, D = spec.num_seqs, spec.num_heads, spec.head_dim
+    T = int(ctx.max())
+    q = W.device_normal((S, H, D), spec.dtype, spec.seed * 1000 + 900, device)
+    k = W.device_normal((S, H, T, D), spec.dtype, spec.seed * 1000 + 903, device)
+    v = W.device_normal((S, H, T, D), spec.dtype, spec.seed * 1000 + 904, device)
+    cl = torch.from_numpy(ctx).to(device)
+    part = spec.partition_size
+    ws = torch.empty(pkv.contiguous_workspace_size(S, H, D, T, part), dtype=torch.uint8,
+                     device=device)
+    out = torch.empty_like(q)
+    stream = torch.cuda.current_stream()
+
+    def call():
+        pkv.contiguous_attention_decode(out, q, k, v, cl, spec.scale, part, ws)
+
+    for _ in range(max(3, warmup)):
+        call()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(20):
+        call()
+    b.record(stream)
+    torch.cuda.synchronize()
+    n = max(20, int(math.ceil(seconds / max(a.elapsed_time(b) / 20 * 1e-3, 1e-7))))
+    sampler = ClockSampler(device.index if device.index is not None else 0)
+    sampler.start()
+    time.sleep(0.3)
+    a.record(stream)
+    for _ in range(n):
+        call()
+    b.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if pkv.get_device_error() != 0:
+        raise SystemExit("bench.py: device error bits (contiguous layout)")
+    us = a.elapsed_time(b) / n * 1e3
+    nbytes = int(ctx.astype(np.int64).sum()) * H * D * 2 * 2 + 2 * S * H * D * 2 + 4 * S
+    peak, _ = read_peaks()
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"workload": "%s batch, contiguous [S][H][T][D] layout (T = %d), %s, split %s" % (
+                name, T, spec.dtype, "balanced" if part == 0 else "%d tokens" % part),
+            "attention_us_per_call": round(us, 2), "attention_bytes_per_call": nbytes,
+            "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4), "calls": n, "clocks": clocks}
+
+
+def measure_configs(device, seconds: float, warmup: int, dist, headline_attn_us: float) -> dict:
+    """The other workloads of the decode path, each on its own: the attention
+    call (main + merge) timed back to back for about `seconds`, its
+    algorithmic GB/s and fraction of the measured copy peak, with the clock
+    record of its region; and the prompt phase.  Long context: split length
+    512 (the workload's) and the balanced split; short: bf16, B = 16;
+    shared prefix: GB/s of the metric's logical bytes and of the unique
+    blocks' bytes."""
+    import torch
+    peak, _ = read_peaks()
+    out = {}
+
+    def entry(wl, t, extra=None):
+        gbs = wl.attn_bytes / (t["us"] * 1e-6) / 1e9
+        e = {"workload": wl.describe(), "attention_us_per_call": round(t["us"], 2),
+             "attention_bytes_per_call": wl.attn_bytes, "GB/s": round(gbs, 1),
+             "frac": round(gbs / peak, 4), "calls": t["calls"], "clocks": t["clocks"]}
+        if extra:
+            e.update(extra)
+        return e
+
+    for name, parts in (("long", (512, 0)), ("short", (None,)), ("shared_prefix", (None,))):
+        wl = Workload(name, device)
+        for part in parts:
+            ws = None
+            if part is not None and part != wl.partition:
+                ws = wl.pkv.alloc_workspace(wl.S, wl.H, wl.D, wl.B, wl.max_blocks, part, device)
+            t = timed_attention(wl, seconds, warmup, device, part, ws)
+            key = name if part is None else "%s_split_%s" % (
+                name, "balanced" if part == 0 else str(part))
+            extra = None
+            if wl.unique_kv_bytes is not None:
+                ub = wl.unique_kv_bytes + (wl.attn_bytes - wl.kv_bytes)
+                extra = {"unique_bytes_per_call": ub,
+                         "unique_GB/s": round(ub / (t["us"] * 1e-6) / 1e9, 1),
+                         "unique_frac": round(ub / (t["us"] * 1e-6) / 1e9 / peak, 4)}
+            out[key] = entry(wl, t, extra)
+            p_ = wl.partition if part is None else part
+            out[key]["split"] = "balanced" if p_ == 0 else "%d tokens" % p_
+            del ws
+        del wl
+        torch.cuda.empty_cache()
+    # the contiguous-layout kernel on the same batches (paging's cost)
+    for name, paged_key in (("opt13b", None), ("short", "short"), ("long", "long_split_512")):
+        c = timed_contiguous(name, device, seconds, warmup)
+        ref_us = headline_attn_us if paged_key is None else out[paged_key]["attention_us_per_call"]
+        c["paged_attention_us_per_call"] = round(ref_us, 2)
+        c["paged_over_contiguous"] = round(ref_us / c["attention_us_per_call"], 4)
+        out[name + "_contiguous"] = c
+        torch.cuda.empty_cache()
+    out["prefill"] = measure_prefill("f16", max(3, warmup), seconds)
+    out["note"] = ("each workload alone, after the headline runs; attention = paged_decode_main "
+                   "+ paged_decode_merge back to back; frac of the measured copy peak "
+                   "(%s GB/s); *_contiguous: the same kernel over a contiguous layout with no "
+                   "block table, paged_over_contiguous = paged / contiguous call time; "
+                   "prefill: tensor-core TFLOP/s of the prompt phase" % peak)
+    return out
+
+
+def measure_e2e_api(wl: Workload, steps: int, device, dist):
+    """End to end through the public API with host buffers, every step issued
+    by the host: the step's inputs (q, new K/V, slot mapping, block tables,
+    context lengths, copy pairs) are copied from pinned host memory in one
+    transfer, the step's three calls run on the compute stream, and its
+    output is copied to pinned host memory and read, every byte, by the host.
+
+    Pipelined over two device input buffers and two output buffers: while
+    step i's kernels run, a copy stream copies step i-1's output out and
+    then brings step i+1's inputs into the other input buffer (both after
+    step i-1's kernels are done with that buffer); before issuing step i+1
+    the host reads step i-1's output.  The first step's inputs are copied
+    before the timed region (the copy of step K's inputs, made in the timed
+    region and not used, stands in for it) and the last output is copied and
+    read after the loop, inside the timed region.  Returns the wall-clock
+    seconds and the host's own issue time per step."""
+    import torch
+    parts = [("q", wl.q), ("k_new", wl.k_new), ("v_new", wl.v_new), ("slots", wl.slots),
+             ("tables", wl.tables), ("ctx", wl.ctx), ("pairs", wl.pairs)]
+    sizes = [t.numel() * t.element_size() for _, t in parts]
+    offs, o = [], 0
+    for n in sizes:
+        offs.append(o)
+        o += (n + 255) // 256 * 256
+    host = torch.empty(o, dtype=torch.uint8).pin_memory()
+    devs = [torch.empty(o, dtype=torch.uint8, device=device) for _ in range(2)]
+    views = [{}, {}]
+    for (name, t), off, n in zip(parts, offs, sizes):
+        host[off:off + n].copy_(t.detach().cpu().contiguous().view(-1).view(torch.uint8))
+        for b in range(2):
+            views[b][name] = devs[b][off:off + n].view(t.dtype).view(t.shape)
+    out_hosts = [torch.empty(wl.out.shape, dtype=wl.out.dtype).pin_memory() for _ in range(2)]
+    out_words = [h.view(-1).view(torch.uint8).numpy().view(np.uint64) for h in out_hosts]
+    outs = [torch.empty_like(wl.out), torch.empty_like(wl.out)]
+    h2d = sum(sizes)
+    d2h = out_hosts[0].numel() * out_hosts[0].element_size()
+    pkv = wl.pkv
+    comp = torch.cuda.current_stream()
+    cps = torch.cuda.Stream(device=device)
+    in_ready = [torch.cuda.Event(), torch.cuda.Event()]
+    done = [torch.cuda.Event(), torch.cuda.Event()]
+    out_ready = [torch.cuda.Event(), torch.cuda.Event()]
+    check = [0]
+
+    def issue(i):
+        p, layer = i % 2, i % wl.layers
+        v = views[p]
+        kc, vc = wl.kc[layer], wl.vc[layer]
+        comp.wait_event(in_ready[p])
+        if len(wl.pairs_host):
+            pkv.copy_blocks(kc, vc, v["pairs"], stream=comp)
+        pkv.reshape_and_cache(v["k_new"], v["v_new"], kc, vc, v["slots"], stream=comp)
+        pkv.paged_attention_decode(outs[p], v["q"], kc, vc, v["tables"], v["ctx"], wl.scale,
+                                   wl.partition, wl.ws, stream=comp)
+        done[p].record(comp)
+        # the copy stream: step i-1's output out, then step i+1's inputs in
+        # (step i-1's kernels are done with input buffer 1-p)
+        cps.wait_event(done[1 - p])
+        with torch.cuda.stream(cps):
+            if i > 0:
+                out_hosts[1 - p].copy_(outs[1 - p], non_blocking=True)
+                out_ready[1 - p].record(cps)
+            devs[1 - p].copy_(host, non_blocking=True)
+            in_ready[1 - p].record(cps)
+
+    def read(j):
+        out_ready[j % 2].synchronize()
+        check[0] ^= int(np.bitwise_xor.reduce(out_words[j % 2]))
+
+    def run(n):
+        torch.cuda.synchronize()
+        with torch.cuda.stream(cps):
+            devs[0].copy_(host, non_blocking=True)
+            in_ready[0].record(cps)
+        done[1].record(comp)
+        torch.cuda.synchronize()
+        host_s = 0.0
+        t0 = time.perf_counter()
+        for i in range(n):
+            h0 = time.perf_counter()
+            issue(i)
+            host_s += time.perf_counter() - h0
+            if i >= 2:
+                read(i - 2)                    # copied out while step i-1 ran
+        last = (n - 1) % 2
+        cps.wait_event(done[last])
+        with torch.cuda.stream(cps):
+            out_hosts[last].copy_(outs[last], non_blocking=True)
+            out_ready[last].record(cps)
+        for j in range(max(0, n - 2), n):
+            read(j)
+        torch.cuda.synchronize()
+        return time.perf_counter() - t0, host_s
+
+    run(3)
+    if dist is not None:
+        dist.barrier()
+    sec, host_s = run(steps)
+    if pkv.get_device_error() != 0:
+        raise SystemExit("bench.py: device error bits in the end-to-end leg")
+    return {"seconds": sec, "steps": steps, "h2d": h2d, "d2h": d2h,
+            "host_issue_us_per_step": 1e6 * host_s / steps, "checksum": check[0]}
 
 
 def measure_e2e(wl: Workload, steps: int, device, dist):
@@ -738,31 +1079,35 @@ def measure_parts(wl: Workload, device, warmup: int) -> dict:
     return out
 
 
-def cpu_baseline(wl: Workload, single_thread: bool = False) -> dict:
-    """The oracle, as it stands, on the host cores over the whole layer-0 batch,
-    repeated until about 10 s of CPU work has been done; single_thread: one
-    thread over the first sequences (about an eighth of the batch's bytes)."""
-    threads = 1 if single_thread else min(host_cores(), wl.S)
+def cpu_baseline(name: str, single_thread: bool = False) -> dict:
+    """The oracle, as it stands, on the host cores over the whole batch of the
+    workload (inputs built on the host: host_case), repeated until about 10 s
+    of CPU work has been done; single_thread: one thread over the longest
+    sequences holding about an eighth of the batch's bytes."""
+    hc = host_case(name)
+    ctx, S = hc["ctx"], hc["spec"].num_seqs
+    threads = 1 if single_thread else min(host_cores(), S)
     seqs = None
     if single_thread:
-        order = np.argsort(wl.ctx_host)
-        budget, seqs, acc = int(wl.ctx_host.sum()) // 8, [], 0
+        order = np.argsort(ctx)
+        budget, seqs, acc = int(ctx.sum()) // 8, [], 0
         for s_ in order[::-1]:
             if acc >= budget and seqs:
                 break
             seqs.append(int(s_))
-            acc += int(wl.ctx_host[s_])
-    sample = oracle_sample(wl, seqs)
-    first = run_oracle(sample, wl.scale, wl.dtype, threads)
+            acc += int(ctx[s_])
+    sample = oracle_sample(hc, seqs)
+    first = run_oracle(sample, threads)
     reps = max(1, min(30, int(10.0 / max(first, 1e-3))))
     total, done = first, 1
     while done < reps and total < 10.0:
-        total += run_oracle(sample, wl.scale, wl.dtype, threads)
+        total += run_oracle(sample, threads)
         done += 1
     return {"value": round(sample["bytes"] * done / total / 1e9, 4), "unit": "GB/s",
             "cores": threads, "kind": "oracle",
-            "sample": "%d of %d sequences x %d heads of layer 0, %d pass(es), %.1f s" % (
-                wl.S if seqs is None else len(seqs), wl.S, wl.H, done, total)}
+            "sample": "%d of %d sequences x %d heads, %d pass(es), %.1f s; tables from the "
+                      "oracle's block-manager model, values from the seeded host generator" % (
+                          S if seqs is None else len(seqs), S, hc["spec"].num_heads, done, total)}
 
 
 def bench_swap(args):
@@ -832,15 +1177,24 @@ def bench_swap(args):
 
 
 def bench_prefill(args):
+    """--op prefill: the prompt phase on its own (measure_prefill)."""
+    from paged_kv_cache_05_gb300 import build
+    build.build()
+    r = measure_prefill(getattr(args, "dtype", "f16"), max(3, args.warmup),
+                        args.roofline_seconds, min_calls=max(10, args.steps // 20))
+    print(json.dumps(dict({"op": "prefill", "metric": "prompt-phase paged attention TFLOP/s",
+                           "unit": "TFLOP/s"}, **r)), flush=True)
+
+
+def measure_prefill(dt: str, warmup: int, seconds: float, min_calls: int = 10) -> dict:
     """The prompt phase at the OPT-13B shape: every prompt's K/V written into
     the pool (reshape_and_cache), then causal paged attention of all prompt
     tokens (tensor cores).  FLOPs = sum over query rows of 4 * D * H * (p + 1)
     (Q K^T and P V, causal); peak = the measured dense bf16 tensor rate
-    (fp16 runs at the same nominal rate)."""
+    (fp16 runs at the same nominal rate).  The whole step and the attention
+    alone are each timed back to back for about `seconds`."""
     import torch
     import paged_kv_cache_05_gb300 as pkv
-    from paged_kv_cache_05_gb300 import build
-    build.build()
     dev = torch.device("cuda", 0)
     spec = W.SPECS["prefill"]
     ctx = W.context_lens(spec)
@@ -851,7 +1205,6 @@ def bench_prefill(args):
     maxb = max(-(-int(c) // B) for c in ctx)
     tables, _ = bm.export(list(range(S)), maxb)
     T = int(ctx.sum())
-    dt = getattr(args, "dtype", "f16")
     kc = torch.zeros((nb, H, B, D), dtype=W.torch_dtype(dt), device=dev)
     vc = torch.zeros_like(kc)
     k = W.device_normal((T, H, D), dt, spec.seed + 1, dev)
@@ -871,14 +1224,18 @@ def bench_prefill(args):
     def attn():
         pkv.paged_attention_prefill(out, q, kc, vc, bt, cl, qs, spec.scale, maxq)
 
-    for _ in range(max(3, args.warmup)):
+    for _ in range(max(3, warmup)):
         step()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(5):
+        step()
+    b.record()
     torch.cuda.synchronize()
+    K = max(min_calls, int(math.ceil(seconds / (a.elapsed_time(b) / 5 * 1e-3))))
     sampler = ClockSampler(0)
     sampler.start()
     time.sleep(0.3)                       # let the sampler start before the timed region
-    K = max(10, args.steps // 20)
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record()
     for _ in range(K):
         step()
@@ -893,7 +1250,7 @@ def bench_prefill(args):
     t_attn = a.elapsed_time(b) / K * 1e-3
     clocks = sampler.stop()
     if pkv.get_device_error() != 0:
-        raise SystemExit("bench.py --op prefill: device error bits")
+        raise SystemExit("bench.py prefill: device error bits")
     flops = float(sum(4.0 * D * H * (c * (c + 1) / 2.0) for c in ctx))
     try:
         peak = float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["bf16_tflops"])
@@ -901,14 +1258,13 @@ def bench_prefill(args):
     except Exception:
         peak, src = 1900.0, "fallback"
     tf = flops / t_attn / 1e12
-    print(json.dumps({
-        "op": "prefill", "metric": "prompt-phase paged attention TFLOP/s", "unit": "TFLOP/s",
-        "value": round(tf, 1), "us_per_call": round(t_attn * 1e6, 1),
+    return {
+        "value": round(tf, 1), "us_per_call": round(t_attn * 1e6, 1), "calls": K,
         "us_per_step_with_cache_write": round(t_step * 1e6, 1),
         "tokens_per_s": round(T / t_step, 1), "dtype": "%s in, f32 accumulate" % dt,
         "config": {"workload": "prefill: %d prompts, lengths %d..%d (sum %d), 40 heads x 128, "
                                "B=16, %s" % (S, int(ctx.min()), int(ctx.max()), T,
-                                                                {"f16": "fp16", "bf16": "bf16"}[dt]),
+                                             {"f16": "fp16", "bf16": "bf16"}[dt]),
                    "flops_per_call": flops},
         "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(tf / peak, 4), "peak_source": src,
@@ -917,7 +1273,7 @@ def bench_prefill(args):
                      "note": "tcgen05.mma kind::f16 from shared-memory descriptors, S and O in "
                              "tensor memory, TMA tiled copies through the block table"},
         "clocks": clocks,
-    }), flush=True)
+    }
 
 
 def sharing_savings(seed: int = 2024, block_size: int = 16):
@@ -991,37 +1347,38 @@ def sharing_savings(seed: int = 2024, block_size: int = 16):
 def reference_arm(args, world, rank, dist):
     """The CPU fp64 oracle as the reference arm, on the host cores: W warm-up
     and K timed steps, each over a length-spread subset of the workload sized
-    so that the whole run takes about a minute."""
-    import torch
+    so that the whole run takes about a minute.  Its inputs are built on the
+    host (host_case: the oracle's block-manager model and the seeded host
+    generator), so the product library is never loaded."""
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
         return
-    if not torch.cuda.is_available():
-        raise SystemExit("bench.py --impl reference: the workload generator needs the GPU")
-    device = torch.device("cuda", 0)
-    from paged_kv_cache_05_gb300 import build
-    build.build()
-    wl = Workload(args.workload, device, args.partition, args.block_size, layers=1)
+    hc = host_case(args.workload, args.block_size)
+    spec = hc["spec"]
     threads = host_cores()
     K, Wu = max(1, args.steps), max(0, args.warmup)
-    seqs = sized_sample(wl, 60.0 / (K + Wu), threads)
-    sample = oracle_sample(wl, seqs)
+    seqs = sized_sample(hc, 60.0 / (K + Wu), threads)
+    sample = oracle_sample(hc, seqs)
     threads = min(threads, len(seqs))
     for _ in range(Wu):
-        run_oracle(sample, wl.scale, wl.dtype, threads)
-    times = [run_oracle(sample, wl.scale, wl.dtype, threads) for _ in range(K)]
+        run_oracle(sample, threads)
+    times = [run_oracle(sample, threads) for _ in range(K)]
     sec = statistics.mean(times)
     v = sample["bytes"] / sec / 1e9
-    desc = "%d of %d sequences (length-spread), all %d heads, layer 0, per step" % (
-        len(seqs), wl.S, wl.H)
+    desc = "%d of %d sequences (length-spread), all %d heads, per step" % (
+        len(seqs), spec.num_seqs, spec.num_heads)
+    c = hc["ctx"]
     line = {
         "impl": "reference",
-        "metric": "paged-attn decode: achieved HBM GB/s (% of GB300 peak), us/layer-step at OPT-13B",
+        "metric": METRIC,
         "value": round(v, 4), "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": Wu,
         "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-        "config": {"workload": wl.describe(), "sample": desc},
+        "config": {"workload": "%s: %d seqs x %d heads x %d, %s K/V, B=%d, ctx %d..%d (sum %d)"
+                               % (args.workload, spec.num_seqs, spec.num_heads, spec.head_dim,
+                                  spec.dtype, hc["B"], int(c.min()), int(c.max()), int(c.sum())),
+                   "sample": desc},
         "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": threads,
                          "kind": "oracle", "sample": desc},
         "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,

@@ -134,6 +134,51 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* k_ca
                                       size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * The same decode attention over a CONTIGUOUS K/V layout, for measuring what
+ * paging costs: the baseline the pages compare PagedAttention with keeps each
+ * sequence's KV cache in one contiguous region reserved for its maximum
+ * length (wywy.jp notes, "existing systems" in the WHAT section; the
+ * zhaifeiyue.github.io detail page, "Kernel 开销 (§7.1)": the paged kernel is
+ * 20-26% slower than FasterTransformer's contiguous attention kernel, Fig. 18a).
+ *   k, v  [num_seqs][num_heads][max_context_len][head_dim], device; token t of
+ *         sequence s, head h at ((s * num_heads + h) * max_context_len + t) * head_dim.
+ *   out[s][h] = sum_{t < context_lens[s]} softmax_t(scale q[s][h] . k[s][h][t]) v[s][h][t]
+ * No block table.  The kernel is the paged one with the table lookup replaced
+ * by that address (same persistent split, copy ring, online softmax and merge),
+ * so the two differ only in the indirection.  context_lens[s] above
+ * max_context_len is clamped and sets PKV_DEVERR_BAD_CONTEXT.  The workspace
+ * (pkv_contiguous_workspace_size) and every other rule are those of
+ * pkv_paged_attention_decode.
+ */
+pkv_status pkv_contiguous_workspace_size(int num_seqs, int num_heads, int head_dim,
+                                         int max_context_len, int partition_size,
+                                         size_t* bytes);
+pkv_status pkv_contiguous_attention_decode(void* out, const void* q, const void* k,
+                                           const void* v, const int32_t* context_lens,
+                                           float scale, int num_seqs, int num_heads,
+                                           int head_dim, int max_context_len, pkv_dtype dtype,
+                                           int partition_size, void* workspace,
+                                           size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Bound, in nanoseconds, of the decode kernels' pipeline waits (a consumer
+ * warp waiting for a ring stage's copy, the producer waiting for a free stage
+ * or for a claimed chunk's query slice, the consumer warps meeting at the end
+ * of a piece), for every later launch of pkv_paged_attention_decode and
+ * pkv_paged_attention_decode_noalloc from any host thread.  Default 1 s; at
+ * most 10 s (larger values: PKV_ERR_INVALID, nothing changed).  A wait that
+ * runs out sets PKV_DEVERR_TIMEOUT; the CTA then stops issuing copies, its
+ * other waits give up at once, its results for the call are not valid, and it
+ * returns after every copy it issued has landed (those waits always keep the
+ * 1 s bound, so no copy lands in a CTA that has ended).  The next call starts
+ * afresh.  A short limit exists to exercise that path (tests); 0 gives up on
+ * the first check that finds a phase incomplete.  *previous (may be NULL)
+ * receives the limit it replaces.  Host only; touches no GPU.
+ * (Failure handling of the kernels; the pages have no counterpart.)
+ */
+pkv_status pkv_set_decode_wait_limit(uint64_t ns, uint64_t* previous);
+
+/*
  * The same decode attention for callers that cannot allocate device memory
  * (the paper has no counterpart; this is an interface convenience).  Some
  * callers can neither allocate nor be handed a workspace -- a serving loop
@@ -149,11 +194,14 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* k_ca
  * with PKV_ERR_INVALID and nothing is launched.
  *
  * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture.  All calls on a device share the array, which
- * keeps the last call's contents (nothing in it needs to start at zero):
- * calls whose work overlaps on the GPU (other streams, other host threads)
- * race on it and must be serialised by the caller.
+ * (cudaGetSymbolAddress) with that device current and keeps it for the life
+ * of the process; make that first call before any stream capture.  The kept
+ * address belongs to the device's primary context: do not use this entry
+ * point after cudaDeviceReset on that device or from another context (the
+ * library's device error word is kept the same way).  All calls on a device
+ * share the array, which keeps the last call's contents (nothing in it needs
+ * to start at zero): calls whose work overlaps on the GPU (other streams,
+ * other host threads) race on it and must be serialised by the caller.
  */
 #define PKV_NOALLOC_SCRATCH_BYTES (16u << 20)
 

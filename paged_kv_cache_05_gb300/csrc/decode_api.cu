@@ -26,6 +26,11 @@ struct OccEntry {
 std::mutex g_mu;
 OccEntry g_occ[kMaxDevices][8] = {};
 
+// Bound of the decode kernels' pipeline waits, in ns (pkv_set_decode_wait_limit).
+constexpr uint64_t kDefaultWaitNs = 1000000000ull;
+constexpr uint64_t kMaxWaitNs = 10000000000ull;
+std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
+
 // A 40-bit tag per call.  The call's first CTA stamps the workspace's claim
 // word with it, and a claimant starts claiming only once it sees the tag, so
 // a word left by an earlier call, or never written, is not taken for this
@@ -88,6 +93,76 @@ int64_t max_chunks(int S, int H, int D, int B, int max_blocks, int partition_siz
     return (steps + L - 1) / L;
 }
 
+// The checks and launch shared by the paged and the contiguous entry points.
+// `a` arrives with the layout's fields set (tables, ctx_cap, kv_stride,
+// num_blocks); B and max_blocks are the layout's step geometry.
+pkv_status launch_decode(const char* fn, const pkv::DecodeKernel* k, pkv::DecodeArgs a,
+                         void* out, const void* q, const void* k_cache, const void* v_cache,
+                         const int32_t* context_lens, float scale, int num_seqs, int num_heads,
+                         int head_dim, int block_size, int max_blocks, int partition_size,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (!out || !q || !k_cache || !v_cache || !context_lens || !workspace)
+        return pkv::fail(PKV_ERR_INVALID, "%s: NULL pointer", fn);
+    if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+        return pkv::fail(PKV_ERR_INVALID, "%s: out, q and the caches must be 16-byte aligned", fn);
+    if (!aligned(context_lens, 4))
+        return pkv::fail(PKV_ERR_INVALID, "%s: int32 arrays must be 4-byte aligned", fn);
+    if (!aligned(workspace, 256))
+        return pkv::fail(PKV_ERR_INVALID, "%s: workspace must be 256-byte aligned", fn);
+    const int64_t mc = max_chunks(num_seqs, num_heads, head_dim, block_size, max_blocks,
+                                  partition_size);
+    const pkv::WsLayout wl = pkv::ws_layout(num_seqs, num_heads, head_dim, mc);
+    if (workspace_bytes < wl.total)
+        return pkv::fail(PKV_ERR_INVALID, "%s: workspace too small (%zu < %zu bytes)", fn,
+                         workspace_bytes, wl.total);
+
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return pkv::cuda_fail(e, fn);
+    if (dev < 0 || dev >= kMaxDevices) return pkv::fail(PKV_ERR_INVALID, "%s: device id", fn);
+    const size_t smem = k->smem_bytes(num_seqs);
+    int per_sm = 0;
+    e = ctas_per_sm(k, dev, smem, &per_sm);
+    if (e != cudaSuccess) return pkv::cuda_fail(e, "decode: occupancy");
+    if (per_sm < 1)
+        return pkv::fail(PKV_ERR_INVALID, "%s: %d sequences need %zu bytes of shared memory", fn,
+                         num_seqs, smem);
+    int grid = pkv::sm_count(dev) * per_sm * PKV_DECODE_WAVES;
+    if (grid < 1) return pkv::fail(PKV_ERR_CUDA, "%s: no multiprocessors", fn);
+    if (grid > PKV_MAX_GRID) grid = PKV_MAX_GRID;
+    {
+        // small batches: no more CTAs than balanced chunks of the minimum length
+        // the batch could fill (the bound uses the table width, not the
+        // device-side lengths)
+        const int64_t steps_bound = (int64_t)num_seqs * num_heads *
+                                    pkv::max_steps_per_seq(head_dim, block_size, max_blocks);
+        const int64_t useful = (steps_bound + kMinChunkSteps - 1) / kMinChunkSteps;
+        if (useful < grid) grid = (int)(useful > 0 ? useful : 1);
+    }
+    int32_t* err = pkv::device_error_word();
+    if (!err) return pkv::fail(PKV_ERR_CUDA, "%s: no device error word", fn);
+
+    a.out = out;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.context_lens = context_lens;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.S = num_seqs;
+    a.H = num_heads;
+    a.L_steps = partition_size > 0 ? partition_size / pkv::step_tokens(head_dim) : 0;
+    a.min_chunk_steps = kMinChunkSteps;
+    a.main_grid = grid;
+    a.epoch = next_epoch();
+    a.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+    a.ws = static_cast<char*>(workspace);
+    a.ws_l = wl;
+    a.err = err;
+    e = k->launch(a, grid, stream);
+    if (e != cudaSuccess) return pkv::cuda_fail(e, fn);
+    return PKV_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -121,72 +196,75 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* k_ca
         return pkv::fail(PKV_ERR_INVALID, "%s: unknown dtype", fn);
     if (!std::isfinite(scale)) return pkv::fail(PKV_ERR_INVALID, "%s: scale is not finite", fn);
     if (num_seqs == 0) return PKV_OK;
-    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !workspace)
-        return pkv::fail(PKV_ERR_INVALID, "%s: NULL pointer", fn);
-    if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
-        return pkv::fail(PKV_ERR_INVALID, "%s: out, q and the caches must be 16-byte aligned", fn);
-    if (!aligned(block_tables, 4) || !aligned(context_lens, 4))
+    if (!block_tables) return pkv::fail(PKV_ERR_INVALID, "%s: NULL pointer", fn);
+    if (!aligned(block_tables, 4))
         return pkv::fail(PKV_ERR_INVALID, "%s: int32 arrays must be 4-byte aligned", fn);
-    if (!aligned(workspace, 256))
-        return pkv::fail(PKV_ERR_INVALID, "%s: workspace must be 256-byte aligned", fn);
-    const int64_t mc = max_chunks(num_seqs, num_heads, head_dim, block_size, max_blocks_per_seq,
-                                  partition_size);
-    const pkv::WsLayout wl = pkv::ws_layout(num_seqs, num_heads, head_dim, mc);
-    if (workspace_bytes < wl.total)
-        return pkv::fail(PKV_ERR_INVALID, "%s: workspace too small (%zu < %zu bytes)", fn,
-                         workspace_bytes, wl.total);
-
     const pkv::DecodeKernel* k = dtype == PKV_F16 ? pkv::decode_kernel_f16(head_dim, block_size)
                                                   : pkv::decode_kernel_bf16(head_dim, block_size);
     if (!k) return pkv::fail(PKV_ERR_INVALID, "%s: unsupported head_dim/block_size", fn);
-
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return pkv::cuda_fail(e, fn);
-    if (dev < 0 || dev >= kMaxDevices) return pkv::fail(PKV_ERR_INVALID, "%s: device id", fn);
-    const size_t smem = k->smem_bytes(num_seqs);
-    int per_sm = 0;
-    e = ctas_per_sm(k, dev, smem, &per_sm);
-    if (e != cudaSuccess) return pkv::cuda_fail(e, "pkv_paged_attention_decode: occupancy");
-    if (per_sm < 1)
-        return pkv::fail(PKV_ERR_INVALID, "%s: %d sequences need %zu bytes of shared memory", fn,
-                         num_seqs, smem);
-    int grid = pkv::sm_count(dev) * per_sm * PKV_DECODE_WAVES;
-    if (grid < 1) return pkv::fail(PKV_ERR_CUDA, "%s: no multiprocessors", fn);
-    if (grid > PKV_MAX_GRID) grid = PKV_MAX_GRID;
-    {
-        // small batches: no more CTAs than balanced chunks of the minimum length
-        // the batch could fill (the bound uses max_blocks_per_seq, not the
-        // device-side lengths)
-        const int64_t steps_bound = (int64_t)num_seqs * num_heads *
-                                    pkv::max_steps_per_seq(head_dim, block_size, max_blocks_per_seq);
-        const int64_t useful = (steps_bound + kMinChunkSteps - 1) / kMinChunkSteps;
-        if (useful < grid) grid = (int)(useful > 0 ? useful : 1);
-    }
-    int32_t* err = pkv::device_error_word();
-    if (!err) return pkv::fail(PKV_ERR_CUDA, "%s: no device error word", fn);
-
-    pkv::DecodeArgs a;
-    a.out = out;
-    a.q = q;
-    a.k_cache = k_cache;
-    a.v_cache = v_cache;
+    pkv::DecodeArgs a = {};
     a.block_tables = block_tables;
-    a.context_lens = context_lens;
-    a.scale_log2 = scale * 1.4426950408889634f;
-    a.S = num_seqs;
-    a.H = num_heads;
     a.max_blocks = max_blocks_per_seq;
+    a.ctx_cap = max_blocks_per_seq * block_size;
+    a.kv_stride = 0;
     a.num_blocks = num_blocks;
-    a.L_steps = partition_size > 0 ? partition_size / pkv::step_tokens(head_dim) : 0;
-    a.min_chunk_steps = kMinChunkSteps;
-    a.main_grid = grid;
-    a.epoch = next_epoch();
-    a.ws = static_cast<char*>(workspace);
-    a.ws_l = wl;
-    a.err = err;
-    e = k->launch(a, grid, stream);
-    if (e != cudaSuccess) return pkv::cuda_fail(e, fn);
+    return launch_decode(fn, k, a, out, q, k_cache, v_cache, context_lens, scale, num_seqs,
+                         num_heads, head_dim, block_size, max_blocks_per_seq, partition_size,
+                         workspace, workspace_bytes, stream);
+}
+
+pkv_status pkv_contiguous_workspace_size(int num_seqs, int num_heads, int head_dim,
+                                         int max_context_len, int partition_size,
+                                         size_t* bytes) {
+    const char* fn = "pkv_contiguous_workspace_size";
+    if (head_dim != 64 && head_dim != 128)
+        return pkv::fail(PKV_ERR_INVALID, "%s: head_dim must be 64 or 128", fn);
+    if (max_context_len < 1)
+        return pkv::fail(PKV_ERR_INVALID, "%s: max_context_len must be >= 1", fn);
+    const int sub = pkv::step_tokens(head_dim);
+    return pkv_decode_workspace_size(num_seqs, num_heads, head_dim, sub,
+                                     (max_context_len + sub - 1) / sub, partition_size, bytes);
+}
+
+pkv_status pkv_contiguous_attention_decode(void* out, const void* q, const void* k,
+                                           const void* v, const int32_t* context_lens,
+                                           float scale, int num_seqs, int num_heads,
+                                           int head_dim, int max_context_len, pkv_dtype dtype,
+                                           int partition_size, void* workspace,
+                                           size_t workspace_bytes, cudaStream_t stream) {
+    const char* fn = "pkv_contiguous_attention_decode";
+    if (head_dim != 64 && head_dim != 128)
+        return pkv::fail(PKV_ERR_INVALID, "%s: head_dim must be 64 or 128", fn);
+    if (max_context_len < 1)
+        return pkv::fail(PKV_ERR_INVALID, "%s: max_context_len must be >= 1", fn);
+    const int sub = pkv::step_tokens(head_dim);
+    const int mb = (max_context_len + sub - 1) / sub;
+    pkv_status st = check_shape(num_seqs, num_heads, head_dim, sub, mb, partition_size, fn);
+    if (st != PKV_OK) return st;
+    if (dtype != PKV_F16 && dtype != PKV_BF16)
+        return pkv::fail(PKV_ERR_INVALID, "%s: unknown dtype", fn);
+    if (!std::isfinite(scale)) return pkv::fail(PKV_ERR_INVALID, "%s: scale is not finite", fn);
+    if (num_seqs == 0) return PKV_OK;
+    const pkv::DecodeKernel* kern = dtype == PKV_F16 ? pkv::decode_kernel_contig_f16(head_dim)
+                                                     : pkv::decode_kernel_contig_bf16(head_dim);
+    if (!kern) return pkv::fail(PKV_ERR_INVALID, "%s: unsupported head_dim", fn);
+    pkv::DecodeArgs a = {};
+    a.block_tables = nullptr;
+    a.max_blocks = mb;
+    a.ctx_cap = max_context_len;
+    a.kv_stride = max_context_len;
+    a.num_blocks = 1;
+    return launch_decode(fn, kern, a, out, q, k, v, context_lens, scale, num_seqs, num_heads,
+                         head_dim, sub, mb, partition_size, workspace, workspace_bytes, stream);
+}
+
+pkv_status pkv_set_decode_wait_limit(uint64_t ns, uint64_t* previous) {
+    if (ns > kMaxWaitNs)
+        return pkv::fail(PKV_ERR_INVALID,
+                         "pkv_set_decode_wait_limit: %llu ns is above the %llu ns maximum",
+                         (unsigned long long)ns, (unsigned long long)kMaxWaitNs);
+    const uint64_t old = g_wait_ns.exchange(ns);
+    if (previous) *previous = old;
     return PKV_OK;
 }
 

@@ -43,8 +43,16 @@
 //     slots of each split (s, h) with the log-sum-exp rule.
 //   * CUDA cores, not tensor cores: decode attention is a matrix-vector
 //     product, about 0.5 flop per byte of K/V, bound by HBM bandwidth.
-//   * Every wait is bounded (1 s); a wait that runs out sets a device error
-//     bit and the CTA winds down (after draining its copies in flight).
+//   * Every wait is bounded.  The pipeline waits (ring stages, claimed-chunk
+//     queue, the consumer warps' meeting at a piece end) give up after the
+//     launch's limit (1 s unless the caller shortened it): the warp sets the
+//     timeout bit of the device error word and a CTA abort flag, after which
+//     every wait of the CTA gives up at once and the warps run out their
+//     remaining work without computing it.  A consumer releases a ring stage
+//     only once it has seen the stage's copy land, so the producer never
+//     re-arms a stage whose copy is in flight, and before the producer warp
+//     exits it waits (1 s bound, always) for every copy it issued, so no copy
+//     lands in a CTA that has ended.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -117,10 +125,6 @@ __device__ __forceinline__ uint64_t global_ns() {
     return t;
 }
 
-__device__ __forceinline__ void named_bar_sync(int id, int threads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-
 __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
     uint4 r;
     asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -130,16 +134,18 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
 }
 
 // Wait for the phase of `bar` with the given parity to complete.  Gives up
-// (returns false) after kWaitLimitNs, after kWaitLimitIters polls, or, when
-// `abort` is given, once *abort becomes nonzero.
-static __device__ __noinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort) {
+// (returns false) once more than limit_ns have passed (checked every 32
+// polls), after kWaitLimitIters polls, or, when `abort` is given, once *abort
+// becomes nonzero.
+static __device__ __noinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                                 uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     for (uint32_t it = 1; it < kWaitLimitIters; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 31) == 0) {
             if (abort && *abort) return false;
-            if (global_ns() - t0 > kWaitLimitNs) return false;
+            if (global_ns() - t0 > limit_ns) return false;
         }
     }
     return false;
@@ -147,9 +153,17 @@ static __device__ __noinline__ bool wait_bounded(uint64_t* bar, uint32_t parity,
 
 // Common case inline (the phase has already completed); the bounded loop only
 // when it has not.
-__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort) {
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                           uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
-    return wait_bounded(bar, parity, abort);
+    return wait_bounded(bar, parity, abort, limit_ns);
+}
+
+// A wait of a pipeline role gave up: record the timeout (unless another warp
+// already aborted the CTA, which is the reason this one gave up) and abort.
+__device__ __forceinline__ void note_timeout(volatile int* abort, int32_t* err) {
+    if (!*abort) atomicOr(err, PKV_DEVERR_TIMEOUT);
+    *abort = 1;
 }
 
 // Programmatic dependent launch: wait for the preceding kernel in the stream
@@ -234,8 +248,8 @@ struct Cfg {
     static constexpr int RS = LOG_LPT - LOG_NL;
     static constexpr int MROW = D + 4;                  // merge row: acc[D], m, l, pad
     static constexpr size_t RING = (size_t)NSTAGE * STAGE;
-    static constexpr size_t BAR_OFF = RING;
-    static constexpr size_t MERGE_OFF = BAR_OFF + 16 * (size_t)NSTAGE;
+    static constexpr size_t BAR_OFF = RING;     // full[NSTAGE], empty[NSTAGE], pair[2]
+    static constexpr size_t MERGE_OFF = BAR_OFF + 16 * (size_t)NSTAGE + 16;
     static constexpr size_t MISC_OFF = MERGE_OFF + 4 * (size_t)(2 * NW * MROW);
     // misc: the abort flag (16 B), then one scan partial per warp
     static constexpr size_t MISC_BYTES = (16 + 4 * (NW + 1) + 15) / 16 * 16;
@@ -443,7 +457,7 @@ __device__ __forceinline__ int64_t claim_chunk(unsigned long long* word, uint64_
 }
 
 // ------------------------------------------------------------ the main kernel
-template <typename T, int D, int B>
+template <typename T, int D, int B, bool CONTIG>
 __global__ void __launch_bounds__(Cfg<D, B>::THREADS, PKV_DECODE_MIN_CTAS)
     paged_decode_main(const DecodeArgs a) {
     using C = Cfg<D, B>;
@@ -451,6 +465,7 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, PKV_DECODE_MIN_CTAS)
     unsigned char* ring = smem;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
     uint64_t* empty = full + C::NSTAGE;
+    uint64_t* pair = empty + C::NSTAGE;        // the consumer warps' meeting, per merge buffer
     float* merge = reinterpret_cast<float*>(smem + C::MERGE_OFF);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF);
     int* scratch = reinterpret_cast<int*>(smem + C::MISC_OFF) + 4;   // NW + 1 ints
@@ -462,7 +477,7 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, PKV_DECODE_MIN_CTAS)
 
     // 1. context lengths (validated and clamped) and the step prefix
     grid_dependency_wait();
-    const int cap = a.max_blocks * B;
+    const int cap = a.ctx_cap;
     for (int s = tid; s < S; s += C::THREADS) {
         int c = a.context_lens[s];
         if (c < 0 || c > cap) {
@@ -480,6 +495,8 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, PKV_DECODE_MIN_CTAS)
             mbar_init(&empty[i], 1);
         }
         for (int i = 0; i < C::QN; ++i) mbar_init(&qfull[i], 1);
+        mbar_init(&pair[0], C::NW);
+        mbar_init(&pair[1], C::NW);
         fence_mbar_init();
         *abort_flag = 0;
     }
@@ -548,13 +565,15 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, PKV_DECODE_MIN_CTAS)
                 const int ns = s_base[p.s + 1] - s_base[p.s];
                 const int64_t left = re - x;
                 const int run = (int64_t)(ns - p.j) < left ? ns - p.j : (int)left;
-                const int nblk = (s_ctx[p.s] + B - 1) / B;
-                const int32_t* row = a.block_tables + (int64_t)p.s * a.max_blocks;
                 for (int i = 0; i < run; ++i) {
                     const int j = p.j + i;
                     // first logical block of the step, and the step's token offset in it
                     const int jb = C::BPS > 1 ? j * C::BPS : j / C::SPB;
                     const int sub = C::BPS > 1 ? 0 : j - jb * C::SPB;
+                    int phys_raw[C::BPS];
+                    if constexpr (!CONTIG) {
+                    const int nblk = (s_ctx[p.s] + B - 1) / B;
+                    const int32_t* row = a.block_tables + (int64_t)p.s * a.max_blocks;
                     const int win = jb & ~31;
                     if (p.s != tc_s || win != tc_win) {
                         if (p.s == tc_s && win == tc_win + 32 && tn_ok) {
@@ -580,13 +599,17 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, PKV_DECODE_MIN_CTAS)
                         tn_ok = win + 32 < nblk;
                         if (tn_ok) tn_val = (win + 32 + lane < nblk) ? __ldg(row + win + 32 + lane) : 0;
                     }
-                    int phys_raw[C::BPS];
 #pragma unroll
                     for (int b = 0; b < C::BPS; ++b)
                         phys_raw[b] = __shfl_sync(kFull, tc_val, jb + b - win);
+                    }  // !CONTIG
                     int ok = 1;
                     if (lane == 0) {
-                        ok = wait_phase(&empty[stage], phase ^ 1u, abort_flag) ? 1 : 0;
+                        // an aborted CTA issues nothing more
+                        ok = (!*abort_flag &&
+                              wait_phase(&empty[stage], phase ^ 1u, abort_flag, a.wait_ns))
+                                 ? 1
+                                 : 0;
                         if (ok) {
                             // only the step's valid tokens move (the last step of a
                             // row is usually partial); the rest of the stage keeps
@@ -606,13 +629,20 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, PKV_DECODE_MIN_CTAS)
 #pragma unroll
                             for (int b = 0; b < C::BPS; ++b) {
                                 if (bytes[b] == 0) continue;
-                                int64_t phys = phys_raw[b];
-                                if (phys < 0 || phys >= a.num_blocks) {
-                                    atomicOr(a.err, PKV_DEVERR_BAD_BLOCK);
-                                    phys = 0;
+                                int64_t off;
+                                if constexpr (CONTIG) {
+                                    // [seq][head][token][D]: the step's tokens are one run
+                                    off = (((int64_t)p.s * H + p.h) * a.kv_stride + tok0) *
+                                          (int64_t)D * 2;
+                                } else {
+                                    int64_t phys = phys_raw[b];
+                                    if (phys < 0 || phys >= a.num_blocks) {
+                                        atomicOr(a.err, PKV_DEVERR_BAD_BLOCK);
+                                        phys = 0;
+                                    }
+                                    off = ((phys * H + p.h) * B + (int64_t)sub * C::SUB) *
+                                          (int64_t)D * 2;
                                 }
-                                const int64_t off =
-                                    ((phys * H + p.h) * B + (int64_t)sub * C::SUB) * (int64_t)D * 2;
                                 const uint32_t doff = (uint32_t)(b * C::TPC * D * 2);
                                 bulk_g2s(dst + doff, kpool + off, bytes[b], &full[stage]);
                                 bulk_g2s(dst + C::CHUNK + doff, vpool + off, bytes[b], &full[stage]);
@@ -621,10 +651,7 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, PKV_DECODE_MIN_CTAS)
                     }
                     ok = __shfl_sync(kFull, ok, 0);
                     if (!ok) {
-                        if (lane == 0) {
-                            if (!*abort_flag) atomicOr(a.err, PKV_DEVERR_TIMEOUT);
-                            *abort_flag = 1;
-                        }
+                        if (lane == 0) note_timeout(abort_flag, a.err);
                         stop = true;
                         break;
                     }
@@ -678,15 +705,17 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, PKV_DECODE_MIN_CTAS)
             issue_range(rb, rb + sp.Ld < total ? rb + sp.Ld : total);
         }
         __syncwarp();
-        if (*abort_flag && lane == 0) {
-            // the query slices still in flight
+        if (lane == 0) {
+            // the query slices this warp copied (the latest use of each queue
+            // entry): landed before the CTA may end, whatever the consumers did
             for (int e = published > C::QN ? published - C::QN : 0; e < published; ++e)
-                wait_bounded(&qfull[e % C::QN], (uint32_t)(e / C::QN) & 1u, nullptr);
+                wait_bounded(&qfull[e % C::QN], (uint32_t)(e / C::QN) & 1u, nullptr, kWaitLimitNs);
         }
 #endif
         __syncwarp();
-        if (*abort_flag && lane == 0) {
-            // wind down: let the copies still in flight land before exiting
+        if (lane == 0) {
+            // the same for the ring: the latest copy into each stage (earlier
+            // ones landed before their stage was released for reuse)
             const int n = issued < C::NSTAGE ? issued : C::NSTAGE;
             int st = stage;
             uint32_t ph = phase;
@@ -695,7 +724,7 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, PKV_DECODE_MIN_CTAS)
                     st = C::NSTAGE - 1;
                     ph ^= 1u;
                 }
-                wait_bounded(&full[st], ph, nullptr);
+                wait_bounded(&full[st], ph, nullptr, kWaitLimitNs);
             }
         }
         return;
@@ -713,6 +742,7 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, PKV_DECODE_MIN_CTAS)
 
     uint32_t g0 = 0;
     int pbuf = 0;
+    uint32_t npiece = 0;                        // pieces met so far (pair barrier phases)
     // the static range, then the claimed chunks the producer publishes; one
     // copy of the loop serves both.  q_first is the query slice of a range's
     // first row; the next piece's slice is loaded one piece ahead, and the
@@ -733,11 +763,10 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, PKV_DECODE_MIN_CTAS)
 #else
             if (sp.fixed || sp.Kd == 0 || *abort_flag) break;
             const int slot = qe % C::QN;
-            if (!wait_phase(&qfull[slot], (uint32_t)(qe / C::QN) & 1u, abort_flag)) {
-                if (lane == 0) {
-                    if (!*abort_flag) atomicOr(a.err, PKV_DEVERR_TIMEOUT);
-                    *abort_flag = 1;
-                }
+            const bool got = wait_phase(&qfull[slot], (uint32_t)(qe / C::QN) & 1u, abort_flag,
+                                        a.wait_ns);
+            if (!__all_sync(kFull, got)) {
+                if (lane == 0) note_timeout(abort_flag, a.err);
                 break;
             }
             ++qe;
@@ -789,15 +818,12 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, PKV_DECODE_MIN_CTAS)
                 const uint32_t g = g0 + (uint32_t)i;
                 const int stage = (int)(g % C::NSTAGE);
                 const uint32_t par = (g / C::NSTAGE) & 1u;
-                if (!*abort_flag) {
-                    if (!wait_phase(&full[stage], par, abort_flag)) {
-                        if (lane == 0) {
-                            if (!*abort_flag) atomicOr(a.err, PKV_DEVERR_TIMEOUT);
-                            *abort_flag = 1;
-                        }
-                    }
-                }
-                __syncwarp();
+                // `have`: every lane saw the stage's copy land.  Only then is
+                // the stage released; after an abort the warp runs through
+                // its steps without waiting (and its results are not used).
+                const bool got = !*abort_flag && wait_phase(&full[stage], par, abort_flag, a.wait_ns);
+                const bool have = __all_sync(kFull, got);
+                if (!have && lane == 0) note_timeout(abort_flag, a.err);
                 const uint4* Ks = reinterpret_cast<const uint4*>(ring + (size_t)stage * C::STAGE);
                 const uint4* Vs = Ks + C::CHUNK / 16;
                 const int nvalid = ctx - (p.j + i) * C::SUB;   // >= 1
@@ -834,7 +860,7 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, PKV_DECODE_MIN_CTAS)
                 }
                 m = m_new;
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[stage]);
+                if (lane == 0 && have) mbar_arrive(&empty[stage]);
             }
     
             // fold the token groups of the warp, then merge the warps
@@ -853,8 +879,16 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, PKV_DECODE_MIN_CTAS)
                 mrow[D] = m;
                 mrow[D + 1] = l;
             }
-            named_bar_sync(1, C::NW * 32);
-            if (!*abort_flag) {
+            // meet the other consumer warps (bounded: an aborted CTA's warps
+            // may no longer agree on their pieces)
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&pair[pbuf]);
+            const bool met_l = !*abort_flag &&
+                               wait_phase(&pair[pbuf], (npiece >> 1) & 1u, abort_flag, a.wait_ns);
+            const bool met = __all_sync(kFull, met_l);
+            if (!met && lane == 0) note_timeout(abort_flag, a.err);
+            ++npiece;
+            if (met) {
                 const float* mb = merge + pbuf * C::NW * C::MROW;
                 float M = -INFINITY;
     #pragma unroll
@@ -899,7 +933,7 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, PKV_DECODE_MIN_CTAS)
 //   M = max_k m_k,  out = sum_k 2^(m_k - M) acc_k / sum_k 2^(m_k - M) l_k.
 constexpr int kMergeBatch = 8;
 
-template <typename T, int D, int B>
+template <typename T, int D, int B, bool CONTIG>
 __global__ void __launch_bounds__(128) paged_decode_merge(const DecodeArgs a) {
     using C = Cfg<D, B>;
     extern __shared__ int msm[];            // base[S + 1], then 8 scan partials
@@ -910,7 +944,7 @@ __global__ void __launch_bounds__(128) paged_decode_merge(const DecodeArgs a) {
 
     // the step prefix, as the main kernel forms it (same clamping)
     {
-        const int cap = a.max_blocks * B;
+        const int cap = a.ctx_cap;
         const int per = (S + 127) / 128;
         const int b = min(tid * per, S), e = min(b + per, S);
         int local = 0;
@@ -1012,7 +1046,7 @@ __global__ void __launch_bounds__(128) paged_decode_merge(const DecodeArgs a) {
 // ------------------------------------------------------------ host glue
 constexpr int kLimitDevices = 64;
 
-template <typename T, int D, int B>
+template <typename T, int D, int B, bool CONTIG = false>
 struct Launcher {
     using C = Cfg<D, B>;
     static size_t smem_bytes(int S) { return C::smem(S); }
@@ -1053,9 +1087,9 @@ struct Launcher {
         }
         Limits& L = limits();
         std::lock_guard<std::mutex> lk(L.mu);
-        e = set_limit(&L.main[dev], (const void*)paged_decode_main<T, D, B>, smem);
+        e = set_limit(&L.main[dev], (const void*)paged_decode_main<T, D, B, CONTIG>, smem);
         if (e != cudaSuccess) return e;
-        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, paged_decode_main<T, D, B>,
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, paged_decode_main<T, D, B, CONTIG>,
                                                              C::THREADS, smem);
     }
     // Both kernels are launched as programmatic dependents of their
@@ -1080,17 +1114,17 @@ struct Launcher {
         cfg.numAttrs = 1;
         Limits& L = limits();
         std::lock_guard<std::mutex> lk(L.mu);
-        e = set_limit(&L.main[dev], (const void*)paged_decode_main<T, D, B>, cfg.dynamicSmemBytes);
+        e = set_limit(&L.main[dev], (const void*)paged_decode_main<T, D, B, CONTIG>, cfg.dynamicSmemBytes);
         if (e != cudaSuccess) return e;
-        e = cudaLaunchKernelEx(&cfg, paged_decode_main<T, D, B>, a);
+        e = cudaLaunchKernelEx(&cfg, paged_decode_main<T, D, B, CONTIG>, a);
         if (e != cudaSuccess) return e;
         const int64_t warps = (int64_t)a.S * a.H;
         cfg.gridDim = dim3((unsigned)((warps + 3) / 4));
         cfg.blockDim = dim3(128);
         cfg.dynamicSmemBytes = merge_smem(a.S);
-        e = set_limit(&L.merge[dev], (const void*)paged_decode_merge<T, D, B>, cfg.dynamicSmemBytes);
+        e = set_limit(&L.merge[dev], (const void*)paged_decode_merge<T, D, B, CONTIG>, cfg.dynamicSmemBytes);
         if (e != cudaSuccess) return e;
-        e = cudaLaunchKernelEx(&cfg, paged_decode_merge<T, D, B>, a);
+        e = cudaLaunchKernelEx(&cfg, paged_decode_merge<T, D, B, CONTIG>, a);
         if (e != cudaSuccess) return e;
         return cudaGetLastError();
     }

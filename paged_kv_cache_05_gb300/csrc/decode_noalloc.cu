@@ -63,12 +63,17 @@ pkv_status pkv_paged_attention_decode_noalloc(void* out, const void* q, const vo
                          "%s: these sizes need %zu bytes of scratch but the static array holds "
                          "%zu; use pkv_paged_attention_decode with a workspace",
                          fn, need, (size_t)PKV_NOALLOC_SCRATCH_BYTES);
-    if (num_seqs == 0) return PKV_OK;
     void* scratch = nullptr;
     st = scratch_address(&scratch);
     if (st != PKV_OK) return st;
-    // The scratch needs no clearing: the decode kernels write every byte
-    // they later read within the same call.
+    // The scratch needs no clearing.  Within one call the header, the step
+    // prefix and the partials are written before they are read.  The one word
+    // read before this call writes it, the claim word of the dynamic chunks,
+    // carries the tag of the call that stamped it; a claimant ignores a word
+    // whose tag is not its own call's, so what an earlier call left there is
+    // never counted.  The remaining argument checks (num_blocks, dtype, scale,
+    // pointers) and the empty batch are handled by the workspace entry point,
+    // so both entry points answer the same arguments with the same status.
     return pkv_paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale,
                                       num_seqs, num_heads, head_dim, block_size,
                                       max_blocks_per_seq, num_blocks, dtype, partition_size,

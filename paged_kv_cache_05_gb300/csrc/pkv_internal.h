@@ -79,11 +79,15 @@ struct DecodeArgs {
     const int32_t* context_lens;
     float scale_log2;        // softmax scale * log2(e)
     int S, H, max_blocks;
+    int ctx_cap;             // largest valid context length (max_blocks * B, or the
+                             // contiguous layout's token stride)
+    int64_t kv_stride;       // contiguous layout: tokens per (sequence, head) row
     int64_t num_blocks;
     int64_t L_steps;         // fixed chunk length in steps, 0 = balanced
     int min_chunk_steps;     // balanced mode: lower bound of the chunk length
     int main_grid;           // CTAs of the main kernel
     uint64_t epoch;          // 40-bit tag of this call (claims of the dynamic chunks)
+    uint64_t wait_ns;        // bound of the pipeline waits (pkv_set_decode_wait_limit)
     char* ws;
     WsLayout ws_l;
     int32_t* err;
@@ -101,6 +105,9 @@ struct DecodeKernel {
 
 const DecodeKernel* decode_kernel_f16(int D, int B);
 const DecodeKernel* decode_kernel_bf16(int D, int B);
+// the same kernels over a contiguous [seq][head][token][D] K/V layout (no block table)
+const DecodeKernel* decode_kernel_contig_f16(int D);
+const DecodeKernel* decode_kernel_contig_bf16(int D);
 
 // ---- cache kernels -----------------------------------------------------------
 cudaError_t launch_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,

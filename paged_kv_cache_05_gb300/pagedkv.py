@@ -57,6 +57,10 @@ def lib():
             "pkv_decode_workspace_size": ([i32, i32, i32, i32, i32, i32, ctypes.POINTER(sz)], i32),
             "pkv_paged_attention_decode": ([P, P, P, P, P, P, f32, i32, i32, i32, i32, i32, i64,
                                             i32, i32, P, sz, P], i32),
+            "pkv_contiguous_workspace_size": ([i32, i32, i32, i32, i32, ctypes.POINTER(sz)],
+                                              i32),
+            "pkv_contiguous_attention_decode": ([P, P, P, P, P, f32, i32, i32, i32, i32, i32,
+                                                 i32, P, sz, P], i32),
             "pkv_paged_attention_decode_noalloc": ([P, P, P, P, P, P, f32, i32, i32, i32, i32,
                                                     i32, i64, i32, i32, P], i32),
             "pkv_paged_attention_prefill": ([P, P, P, P, P, P, P, f32, i32, i32, i32, i32,
@@ -65,6 +69,7 @@ def lib():
             "pkv_copy_blocks": ([P, P, P, i32, i32, i32, i32, i64, i32, P], i32),
             "pkv_swap_blocks": ([P, P, P, P, P, i32, i32, i32, i32, i64, i64, i32, P], i32),
             "pkv_get_device_error": ([ctypes.POINTER(ctypes.c_int32), i32, P], i32),
+            "pkv_set_decode_wait_limit": ([u64, ctypes.POINTER(u64)], i32),
             "pkv_last_error": ([], ctypes.c_char_p),
             "pkv_version": ([], ctypes.c_char_p),
             "pkv_bm_create": ([i64, i32, u64, ctypes.POINTER(P)], i32),
@@ -193,6 +198,40 @@ def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens,
     return out
 
 
+def contiguous_workspace_size(num_seqs, num_heads, head_dim, max_context_len,
+                              partition_size=0) -> int:
+    out = ctypes.c_size_t(0)
+    _check("pkv_contiguous_workspace_size",
+           lib().pkv_contiguous_workspace_size(num_seqs, num_heads, head_dim, max_context_len,
+                                               partition_size, ctypes.byref(out)))
+    return out.value
+
+
+def contiguous_attention_decode(out, q, k, v, context_lens, scale, partition_size=0,
+                                workspace=None, stream=None):
+    """The decode attention over a contiguous [S, H, max_context_len, D] K/V
+    layout (no block table): the baseline layout paging is measured against."""
+    torch = _torch()
+    S, H, D = q.shape
+    if k.dim() != 4 or tuple(k.shape[:2]) != (S, H) or k.shape[3] != D or \
+            tuple(v.shape) != tuple(k.shape):
+        raise ValueError("k and v must be [num_seqs, num_heads, max_context_len, head_dim]")
+    if tuple(out.shape) != (S, H, D) or out.dtype != q.dtype or k.dtype != q.dtype or \
+            v.dtype != q.dtype:
+        raise ValueError("out/q/k/v dtype or shape mismatch")
+    T = k.shape[2]
+    if workspace is None:
+        n = contiguous_workspace_size(S, H, D, T, partition_size)
+        workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
+    _check("pkv_contiguous_attention_decode",
+           lib().pkv_contiguous_attention_decode(
+               _dev(out, "out"), _dev(q, "q"), _dev(k, "k"), _dev(v, "v"),
+               _dev(context_lens, "context_lens", torch.int32, 1), float(scale), S, H, D, T,
+               _dtype_code(q.dtype), int(partition_size), _dev(workspace, "workspace"),
+               workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
 def paged_attention_prefill(out, q, k_cache, v_cache, block_tables, context_lens, query_start,
                             scale, max_query_len, stream=None):
     """Causal attention of each sequence's new tokens (rows query_start[s] ..
@@ -317,6 +356,16 @@ def get_device_error(clear=True, stream=None) -> int:
     if st not in (PKV_OK, PKV_ERR_DEVICE):
         _check("pkv_get_device_error", st)
     return bits.value
+
+
+def set_decode_wait_limit(ns: int) -> int:
+    """Bound (ns) of the decode kernels' pipeline waits for later launches;
+    returns the bound it replaces (default 1 s).  Short bounds exist to
+    exercise the timeout path."""
+    prev = ctypes.c_uint64(0)
+    _check("pkv_set_decode_wait_limit",
+           lib().pkv_set_decode_wait_limit(int(ns), ctypes.byref(prev)))
+    return prev.value
 
 
 # ------------------------------------------------------------- block manager

@@ -82,6 +82,15 @@ def compact_rows(kc: np.ndarray, vc: np.ndarray, tables: np.ndarray, ctx, seqs, 
     return kc[idx], vc[idx], bt, np.array([ctx[s] for s in seqs], np.int32), uniq
 
 
+def host_threads() -> int:
+    """Host cores this process may use (threads for the oracle's C routine)."""
+    import os
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except Exception:
+        return os.cpu_count() or 1
+
+
 def sampled_oracle(q_host: np.ndarray, kc_host: np.ndarray, vc_host: np.ndarray,
                    tables: np.ndarray, ctx, seqs, scale, dtype: str) -> np.ndarray:
     """fp64 oracle rows [len(seqs), H, D] for selected sequences of a batch whose
@@ -90,7 +99,7 @@ def sampled_oracle(q_host: np.ndarray, kc_host: np.ndarray, vc_host: np.ndarray,
     kc, vc, bt, cl, _ = compact_rows(kc_host, vc_host, tables, ctx, seqs, B)
     return oracle.paged_attention_decode_threaded(q_host[list(seqs)], kc, vc, bt, cl,
                                                   float(np.float32(scale)), ORC_DTYPE[dtype],
-                                                  threads=8)
+                                                  threads=host_threads())
 
 
 def device_blocks_to_host(k_cache, v_cache, block_ids):

@@ -284,3 +284,50 @@ def test_swap_refuses_pageable_host_memory(pkv):
     st = L.pkv_swap_blocks(p, p, p, p, pairs.ctypes.data, 1, 2, 64, 16, 4, 4, 0, None)
     assert st == 1 and "pinned" in pkv.pagedkv.last_error()
     assert L.pkv_swap_blocks(p, p, p, p, pairs.ctypes.data, 0, 2, 64, 16, 4, 4, 0, None) == 0
+
+
+def test_documented_status_and_error_codes(pkv):
+    """The status codes and device error bits the header documents, and the
+    binding's copies of them, are the same numbers."""
+    text = open(os.path.join(ROOT, "include", "pagedkv.h")).read()
+    enum = dict((n, int(v)) for n, v in re.findall(r"\b(PKV_(?:OK|ERR_\w+))\s*=\s*(\d+)", text))
+    assert enum == {"PKV_OK": 0, "PKV_ERR_INVALID": 1, "PKV_ERR_CUDA": 2, "PKV_ERR_OOM": 3,
+                    "PKV_ERR_DEVICE": 4}
+    bits = dict((n, int(v)) for n, v in re.findall(r"#define\s+(PKV_DEVERR_\w+)\s+(\d+)", text))
+    assert bits == {"PKV_DEVERR_BAD_BLOCK": 1, "PKV_DEVERR_BAD_SLOT": 2,
+                    "PKV_DEVERR_BAD_CONTEXT": 4, "PKV_DEVERR_TIMEOUT": 8,
+                    "PKV_DEVERR_WORKSPACE": 16}
+    P = pkv.pagedkv
+    assert (P.PKV_OK, P.PKV_ERR_INVALID, P.PKV_ERR_CUDA, P.PKV_ERR_OOM, P.PKV_ERR_DEVICE) == \
+        (0, 1, 2, 3, 4)
+    assert (P.DEVERR_BAD_BLOCK, P.DEVERR_BAD_SLOT, P.DEVERR_BAD_CONTEXT, P.DEVERR_TIMEOUT,
+            P.DEVERR_WORKSPACE) == (1, 2, 4, 8, 16)
+    # one status per outcome: a bad argument is INVALID and names the argument
+    L = pkv.lib()
+    out = ctypes.c_size_t(0)
+    assert L.pkv_decode_workspace_size(4, 8, 96, 16, 4, 0, ctypes.byref(out)) == 1
+    assert "head_dim" in P.last_error()
+    assert L.pkv_decode_workspace_size(4, 8, 64, 16, 4, 0, None) == 1
+    bm = P.BlockManager(4, 16, 1)
+    bm.add_sequence(0, 64)
+    with pytest.raises(P.OutOfBlocks) as e:
+        bm.add_sequence(1, 1)
+    assert e.value.status == 3
+
+
+def test_decode_wait_limit_setter(pkv):
+    """The bound of the decode kernels' pipeline waits: default 1 s, settable
+    up to 10 s, returns the bound it replaces, a larger value is refused and
+    leaves the bound unchanged."""
+    P = pkv.pagedkv
+    first = P.set_decode_wait_limit(5_000)
+    try:
+        assert first == 1_000_000_000
+        assert P.set_decode_wait_limit(0) == 5_000
+        with pytest.raises(P.PagedKVError) as e:
+            P.set_decode_wait_limit(10_000_000_001)
+        assert e.value.status == 1
+        assert P.set_decode_wait_limit(10_000_000_000) == 0
+    finally:
+        P.set_decode_wait_limit(first)
+    assert P.set_decode_wait_limit(first) == first

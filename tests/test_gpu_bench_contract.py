@@ -35,10 +35,12 @@ def test_bench_line():
         assert k in r, k
     assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] > 0
     assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-3
+    assert d["roofline_region"]["calls"] >= 30
     e = d["e2e"]
     assert e["unit"] == d["unit"] and e["value"] > 0 and e["steps"] == 20
     assert e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
-    assert e["us_per_step"] > 0 and e["serial_us_per_step"] > 0
+    assert e["us_per_step"] > 0 and e["serial_us_per_step"] > 0 and e["graph_us_per_step"] > 0
+    assert d["api_us_per_step"] == e["us_per_step"] and e["host_issue_us_per_step"] > 0
     c = d["clocks"]
     assert "sm_mhz" in c and "sm_max_mhz" in c and isinstance(c["reasons"], list)
 

@@ -299,3 +299,50 @@ def test_batch_size_limit(pkv):
     assert ei.value.status == 1 and "num_seqs" in str(ei.value)
     torch.cuda.synchronize()
     assert torch.isnan(o1).all() and pkv.get_device_error() == 0
+
+
+@pytest.mark.parametrize("partition", [0, 512])
+def test_pipeline_wait_timeout_is_reported_and_the_next_call_is_correct(pkv, partition):
+    """The timeout path of the decode kernels, made to run out on purpose by
+    a short wait bound (no wait is broken: with a 0 ns bound a pipeline wait
+    gives up at its first check that finds the phase incomplete, which on a
+    batch of about 57K steps happens in some CTA on essentially every call).
+    The call must return, set PKV_DEVERR_TIMEOUT and nothing else; a normal
+    call on the same stream right after it must match the oracle."""
+    import torch
+    from paged_kv_cache_05_gb300 import pagedkv as P
+    rs = np.random.default_rng(1400 + partition)
+    S, H, D, B = 128, 16, 128, 16
+    ctx = [int(c) for c in rs.integers(1, 900, size=S)]
+    case = random_case(rs, S, H, D, B, ctx, "f16")
+    scale = float(np.float32(1 / math.sqrt(D)))
+    ref = run_oracle(case, scale)
+    q = to_dev(case["q"], "f16")
+    kc, vc = to_dev(case["kc"], "f16"), to_dev(case["vc"], "f16")
+    bt = torch.from_numpy(case["bt"]).cuda()
+    cl = torch.from_numpy(case["ctx"]).cuda()
+    ws = pkv.alloc_workspace(S, H, D, B, bt.shape[1], partition, q.device)
+    out = torch.empty_like(q)
+    assert pkv.get_device_error() == 0
+    prev = P.set_decode_wait_limit(0)
+    seen = []
+    try:
+        for _ in range(5):
+            pkv.paged_attention_decode(out, q, kc, vc, bt, cl, scale, partition_size=partition,
+                                       workspace=ws)
+            torch.cuda.synchronize()
+            bits = pkv.get_device_error()
+            seen.append(bits)
+            assert bits & ~P.DEVERR_TIMEOUT == 0, bits
+            if bits:
+                break
+    finally:
+        P.set_decode_wait_limit(prev)
+    assert any(b & P.DEVERR_TIMEOUT for b in seen), seen
+    for i in range(2):
+        out.fill_(float("nan"))
+        pkv.paged_attention_decode(out, q, kc, vc, bt, cl, scale, partition_size=partition,
+                                   workspace=ws)
+        torch.cuda.synchronize()
+        assert pkv.get_device_error() == 0
+        attn_check(out, ref, "normal call %d after a timed-out call" % i)
