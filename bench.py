@@ -149,7 +149,7 @@ class Workload:
     """Device-resident inputs of one workload plus the algorithmic byte counts."""
 
     def __init__(self, name: str, device, partition=None, block_size=None, layers=None,
-                 placement: str = "scattered"):
+                 placement: str = "scattered", decode: str = "auto"):
         import torch
         import paged_kv_cache_05_gb300 as pkv
         self.pkv = pkv
@@ -246,7 +246,16 @@ class Workload:
         self.ctx = torch.from_numpy(ctx).to(dev)
         self.slots = torch.from_numpy(slots).to(dev)
         self.pairs = torch.from_numpy(pairs).to(dev)
-        self.ws = pkv.alloc_workspace(S, H, D, B, self.max_blocks, self.partition, dev)
+        # the shared-prefix entry point (each group's common prefix read once)
+        # for the workload whose sequences are forks of shared prompts
+        self.shared = decode == "shared" or (decode == "auto" and name == "shared_prefix")
+        self.decode_fn = (pkv.paged_attention_decode_shared if self.shared
+                          else pkv.paged_attention_decode)
+        if self.shared:
+            self.ws = torch.empty(pkv.decode_shared_workspace_size(
+                S, H, D, B, self.max_blocks, self.partition), dtype=torch.uint8, device=dev)
+        else:
+            self.ws = pkv.alloc_workspace(S, H, D, B, self.max_blocks, self.partition, dev)
         self.scale = spec.scale
         e = 2
         self.kv_bytes = int(ctx.astype(np.int64).sum()) * H * D * 2 * e
@@ -255,7 +264,7 @@ class Workload:
         self.reshape_bytes = 2 * (2 * S * H * D * e)
         self.copy_bytes = len(pairs) * 2 * 2 * H * B * D * e
         self.step_bytes = self.attn_bytes + self.reshape_bytes + self.copy_bytes
-        self.launches_per_step = 3 + (1 if len(pairs) else 0)
+        self.launches_per_step = 3 + (1 if len(pairs) else 0) + (1 if self.shared else 0)
         self.unique_kv_bytes = None
         if name == "shared_prefix":
             blocks = set()
@@ -270,23 +279,25 @@ class Workload:
         if len(self.pairs_host):
             pkv.copy_blocks(kc, vc, self.pairs)
         pkv.reshape_and_cache(self.k_new, self.v_new, kc, vc, self.slots)
-        pkv.paged_attention_decode(self.out, self.q, kc, vc, self.tables, self.ctx, self.scale,
-                                   self.partition, self.ws)
+        self.decode_fn(self.out, self.q, kc, vc, self.tables, self.ctx, self.scale,
+                       self.partition, self.ws)
 
     def attention(self, i: int):
         layer = i % self.layers
-        self.pkv.paged_attention_decode(self.out, self.q, self.kc[layer], self.vc[layer],
-                                        self.tables, self.ctx, self.scale, self.partition, self.ws)
+        self.decode_fn(self.out, self.q, self.kc[layer], self.vc[layer], self.tables, self.ctx,
+                       self.scale, self.partition, self.ws)
 
     def describe(self) -> str:
         sp = self.spec
         c = self.ctx_host
         return ("%s: %d seqs x %d heads x %d, %s K/V, B=%d, ctx %d..%d (sum %d), pool %d blocks"
-                " x %d layer pool(s), split %s, %s placement" % (
+                " x %d layer pool(s), split %s, %s placement%s" % (
                     self.name, self.S, self.H, self.D, sp.dtype, self.B, int(c.min()),
                     int(c.max()), int(c.sum()), self.nb, self.layers,
                     "balanced" if self.partition == 0 else "%d tokens" % self.partition,
-                    self.placement))
+                    self.placement,
+                    ", shared prefixes read once (paged_attention_decode_shared)"
+                    if self.shared else ""))
 
 
 # ------------------------------------------------------------------ oracle leg
@@ -427,6 +438,10 @@ def main():
     ap.add_argument("--placement", choices=["scattered", "contiguous"], default="scattered",
                     help="physical block placement: the block manager's scattered free list, "
                          "or every sequence's blocks consecutive (contiguous baseline)")
+    ap.add_argument("--decode", choices=["auto", "plain", "shared"], default="auto",
+                    help="decode entry point: plain, shared (groups of sequences sharing "
+                         "prefix blocks read them once), auto = shared for the shared-prefix "
+                         "workload")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--roofline-seconds", type=float, default=0.5,
@@ -470,7 +485,7 @@ def main():
     from paged_kv_cache_05_gb300 import build
     build.build()
     wl = Workload(args.workload, device, args.partition, args.block_size, args.layers,
-                  args.placement)
+                  args.placement, args.decode)
     stream = torch.cuda.current_stream()
 
     K = args.steps
@@ -581,7 +596,9 @@ def main():
                              "launches (2 kernels each) for the roofline" % (
                                  wl.launches_per_step,
                                  "copy_blocks, " * bool(len(wl.pairs_host))
-                                 + "reshape_and_cache, paged_decode_main, paged_decode_merge",
+                                 + "reshape_and_cache, "
+                                 + "paged_decode_groups, " * wl.shared
+                                 + "paged_decode_main, paged_decode_merge",
                                  n_attn),
         "roofline_region": {"calls": n_attn, "ms": round(attn_avg * n_attn, 2)},
         "clocks": clocks,
@@ -653,9 +670,8 @@ def timed_attention(wl: Workload, seconds: float, warmup: int, device, partition
 
     def call(i):
         layer = i % wl.layers
-        wl.pkv.paged_attention_decode(wl.out, wl.q, wl.kc[layer], wl.vc[layer], wl.tables, wl.ctx,
-                                      wl.scale, wl.partition if partition is None else partition,
-                                      wl.ws if ws is None else ws)
+        wl.decode_fn(wl.out, wl.q, wl.kc[layer], wl.vc[layer], wl.tables, wl.ctx, wl.scale,
+                     wl.partition if partition is None else partition, wl.ws if ws is None else ws)
 
     for i in range(max(3, warmup)):
         call(i)
@@ -757,15 +773,20 @@ def measure_configs(device, seconds: float, warmup: int, dist, headline_attn_us:
             e.update(extra)
         return e
 
-    for name, parts in (("long", (512, 0)), ("short", (None,)), ("shared_prefix", (None,))):
-        wl = Workload(name, device)
+    for name, parts, decode in (("long", (512, 0), "auto"), ("short", (None,), "auto"),
+                                ("shared_prefix", (None,), "plain"),
+                                ("shared_prefix", (None,), "shared")):
+        wl = Workload(name, device, decode=decode)
         for part in parts:
             ws = None
             if part is not None and part != wl.partition:
                 ws = wl.pkv.alloc_workspace(wl.S, wl.H, wl.D, wl.B, wl.max_blocks, part, device)
+                assert not wl.shared
             t = timed_attention(wl, seconds, warmup, device, part, ws)
             key = name if part is None else "%s_split_%s" % (
                 name, "balanced" if part == 0 else str(part))
+            if wl.shared:
+                key += "_groups"
             extra = None
             if wl.unique_kv_bytes is not None:
                 ub = wl.unique_kv_bytes + (wl.attn_bytes - wl.kv_bytes)
@@ -847,8 +868,8 @@ def measure_e2e_api(wl: Workload, steps: int, device, dist):
         if len(wl.pairs_host):
             pkv.copy_blocks(kc, vc, v["pairs"], stream=comp)
         pkv.reshape_and_cache(v["k_new"], v["v_new"], kc, vc, v["slots"], stream=comp)
-        pkv.paged_attention_decode(outs[p], v["q"], kc, vc, v["tables"], v["ctx"], wl.scale,
-                                   wl.partition, wl.ws, stream=comp)
+        wl.decode_fn(outs[p], v["q"], kc, vc, v["tables"], v["ctx"], wl.scale, wl.partition,
+                     wl.ws, stream=comp)
         done[p].record(comp)
         # the copy stream: step i-1's output out, then step i+1's inputs in
         # (step i-1's kernels are done with input buffer 1-p)
@@ -944,8 +965,7 @@ def measure_e2e(wl: Workload, steps: int, device, dist):
         if len(wl.pairs_host):
             pkv.copy_blocks(kc, vc, v["pairs"])
         pkv.reshape_and_cache(v["k_new"], v["v_new"], kc, vc, v["slots"])
-        pkv.paged_attention_decode(out, v["q"], kc, vc, v["tables"], v["ctx"],
-                                   wl.scale, wl.partition, wl.ws)
+        wl.decode_fn(out, v["q"], kc, vc, v["tables"], v["ctx"], wl.scale, wl.partition, wl.ws)
 
     side = torch.cuda.Stream(device=device)
     cps = torch.cuda.Stream(device=device)

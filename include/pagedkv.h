@@ -134,6 +134,38 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* k_ca
                                       size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * The same decode attention for batches whose sequences share prefix blocks
+ * (parallel sampling, beam search: sequences forked from one prompt hold the
+ * prompt's blocks by reference; wywy.jp notes, "Copy-on-write" and the
+ * parallel-sampling walkthrough; ricepunchb garden section 5.1, the shared
+ * physical blocks of the sharing diagram).  The sharing structure is read from
+ * the block tables themselves: sequences ADJACENT in the batch whose tables
+ * begin with the same full blocks (at least 4 steps' worth: 64 tokens at
+ * head_dim 128) form a group of at most 8; the group's common prefix is read
+ * from HBM once and attended by every member together (tensor-core products of
+ * the prefix's keys with the members' queries), and each member's own blocks
+ * are read as usual; a merge pass combines both with the log-sum-exp rule.
+ * Results are those of pkv_paged_attention_decode (same definition, within the
+ * same tolerance; not bit-identical, the summation order differs).  Sharers
+ * that are not adjacent are computed correctly, each reading its blocks.
+ * Three launches on `stream` (a one-CTA group pass, the main pass, the merge).
+ * Arguments as for pkv_paged_attention_decode; the workspace is sized by
+ * pkv_decode_shared_workspace_size.  Batches above 4096 sequences run the
+ * plain kernels (no grouping).
+ */
+pkv_status pkv_decode_shared_workspace_size(int num_seqs, int num_heads, int head_dim,
+                                            int block_size, int max_blocks_per_seq,
+                                            int partition_size, size_t* bytes);
+pkv_status pkv_paged_attention_decode_shared(void* out, const void* q, const void* k_cache,
+                                             const void* v_cache, const int32_t* block_tables,
+                                             const int32_t* context_lens, float scale,
+                                             int num_seqs, int num_heads, int head_dim,
+                                             int block_size, int max_blocks_per_seq,
+                                             int64_t num_blocks, pkv_dtype dtype,
+                                             int partition_size, void* workspace,
+                                             size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * The same decode attention over a CONTIGUOUS K/V layout, for measuring what
  * paging costs: the baseline the pages compare PagedAttention with keeps each
  * sequence's KV cache in one contiguous region reserved for its maximum

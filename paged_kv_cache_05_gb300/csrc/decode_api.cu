@@ -2,8 +2,11 @@
 #include <atomic>
 #include <chrono>
 #include <cmath>
+#include <cstring>
 #include <mutex>
 #include <random>
+
+#include <cudaTypedefs.h>
 
 #include "pkv_internal.h"
 
@@ -65,6 +68,36 @@ cudaError_t ctas_per_sm(const pkv::DecodeKernel* k, int dev, size_t smem, int* o
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+// The driver's tiled tensor-map encoder (a host computation), looked up once.
+PFN_cuTensorMapEncodeTiled_v12000 map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// A pool [num_blocks][H][B][D] seen as rows of D 16-bit elements; boxes of
+// 64 columns x box_rows rows, 128-byte swizzle (the shared-prefix steps).
+bool pool_map(CUtensorMap* m, bool bf16, const void* pool, int64_t rows, int D, int box_rows) {
+    const PFN_cuTensorMapEncodeTiled_v12000 fn = map_encoder();
+    if (!fn || rows >= (1LL << 31)) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+              const_cast<void*>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Host-only checks shared by the workspace query and the launch.
 pkv_status check_shape(int S, int H, int D, int B, int max_blocks, int partition_size,
                        const char* fn) {
@@ -86,6 +119,19 @@ pkv_status check_shape(int S, int H, int D, int B, int max_blocks, int partition
     return PKV_OK;
 }
 
+// Capacities of the shared-prefix regions (group units, group partial slots):
+// a sequence belongs to at most one group, whose prefix (at most the
+// sequence's steps) is cut into units of group_unit_steps(D, B) steps.
+// False when grouping is not offered for these sizes (the plain kernel runs).
+bool group_caps(int S, int H, int D, int B, int max_blocks, int64_t* units, int64_t* slots) {
+    if (S < 2 || S > pkv::kGroupMaxSeqs) return false;
+    const int64_t lg = pkv::group_unit_steps(D, B);
+    const int64_t nc = (pkv::max_steps_per_seq(D, B, max_blocks) + lg - 1) / lg;
+    *slots = (int64_t)S * H * nc;
+    *units = (int64_t)(S / 2) * H * nc;
+    return *slots < (1LL << 31);
+}
+
 int64_t max_chunks(int S, int H, int D, int B, int max_blocks, int partition_size) {
     if (partition_size == 0) return (int64_t)PKV_MAX_GRID * (1 + PKV_DECODE_DYN_PER_CTA);
     const int64_t L = partition_size / pkv::step_tokens(D);
@@ -100,7 +146,9 @@ pkv_status launch_decode(const char* fn, const pkv::DecodeKernel* k, pkv::Decode
                          void* out, const void* q, const void* k_cache, const void* v_cache,
                          const int32_t* context_lens, float scale, int num_seqs, int num_heads,
                          int head_dim, int block_size, int max_blocks, int partition_size,
-                         void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream,
+                         int64_t gunit_cap = 0, int64_t gslot_cap = 0,
+                         const CUtensorMap* tk = nullptr, const CUtensorMap* tv = nullptr) {
     if (!out || !q || !k_cache || !v_cache || !context_lens || !workspace)
         return pkv::fail(PKV_ERR_INVALID, "%s: NULL pointer", fn);
     if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
@@ -111,7 +159,7 @@ pkv_status launch_decode(const char* fn, const pkv::DecodeKernel* k, pkv::Decode
         return pkv::fail(PKV_ERR_INVALID, "%s: workspace must be 256-byte aligned", fn);
     const int64_t mc = max_chunks(num_seqs, num_heads, head_dim, block_size, max_blocks,
                                   partition_size);
-    const pkv::WsLayout wl = pkv::ws_layout(num_seqs, num_heads, head_dim, mc);
+    const pkv::WsLayout wl = pkv::ws_layout(num_seqs, num_heads, head_dim, mc, gunit_cap, gslot_cap);
     if (workspace_bytes < wl.total)
         return pkv::fail(PKV_ERR_INVALID, "%s: workspace too small (%zu < %zu bytes)", fn,
                          workspace_bytes, wl.total);
@@ -158,7 +206,9 @@ pkv_status launch_decode(const char* fn, const pkv::DecodeKernel* k, pkv::Decode
     a.ws = static_cast<char*>(workspace);
     a.ws_l = wl;
     a.err = err;
-    e = k->launch(a, grid, stream);
+    CUtensorMap none;
+    memset(&none, 0, sizeof(none));
+    e = k->launch(a, grid, stream, tk ? *tk : none, tv ? *tv : none);
     if (e != cudaSuccess) return pkv::cuda_fail(e, fn);
     return PKV_OK;
 }
@@ -208,6 +258,7 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* k_ca
     a.ctx_cap = max_blocks_per_seq * block_size;
     a.kv_stride = 0;
     a.num_blocks = num_blocks;
+    a.mode = pkv::kModePaged;
     return launch_decode(fn, k, a, out, q, k_cache, v_cache, context_lens, scale, num_seqs,
                          num_heads, head_dim, block_size, max_blocks_per_seq, partition_size,
                          workspace, workspace_bytes, stream);
@@ -254,8 +305,77 @@ pkv_status pkv_contiguous_attention_decode(void* out, const void* q, const void*
     a.ctx_cap = max_context_len;
     a.kv_stride = max_context_len;
     a.num_blocks = 1;
+    a.mode = pkv::kModeContig;
     return launch_decode(fn, kern, a, out, q, k, v, context_lens, scale, num_seqs, num_heads,
                          head_dim, sub, mb, partition_size, workspace, workspace_bytes, stream);
+}
+
+pkv_status pkv_decode_shared_workspace_size(int num_seqs, int num_heads, int head_dim,
+                                            int block_size, int max_blocks_per_seq,
+                                            int partition_size, size_t* bytes) {
+    const char* fn = "pkv_decode_shared_workspace_size";
+    if (!bytes) return pkv::fail(PKV_ERR_INVALID, "%s: bytes is NULL", fn);
+    pkv_status st = check_shape(num_seqs, num_heads, head_dim, block_size, max_blocks_per_seq,
+                                partition_size, fn);
+    if (st != PKV_OK) return st;
+    int64_t gu = 0, gs = 0;
+    if (!group_caps(num_seqs, num_heads, head_dim, block_size, max_blocks_per_seq, &gu, &gs))
+        gu = gs = 0;
+    const int64_t mc = max_chunks(num_seqs, num_heads, head_dim, block_size, max_blocks_per_seq,
+                                  partition_size);
+    *bytes = pkv::ws_layout(num_seqs, num_heads, head_dim, mc, gu, gs).total;
+    return PKV_OK;
+}
+
+pkv_status pkv_paged_attention_decode_shared(void* out, const void* q, const void* k_cache,
+                                             const void* v_cache, const int32_t* block_tables,
+                                             const int32_t* context_lens, float scale,
+                                             int num_seqs, int num_heads, int head_dim,
+                                             int block_size, int max_blocks_per_seq,
+                                             int64_t num_blocks, pkv_dtype dtype,
+                                             int partition_size, void* workspace,
+                                             size_t workspace_bytes, cudaStream_t stream) {
+    const char* fn = "pkv_paged_attention_decode_shared";
+    pkv_status st = check_shape(num_seqs, num_heads, head_dim, block_size, max_blocks_per_seq,
+                                partition_size, fn);
+    if (st != PKV_OK) return st;
+    if (num_blocks < 1) return pkv::fail(PKV_ERR_INVALID, "%s: num_blocks must be >= 1", fn);
+    if (dtype != PKV_F16 && dtype != PKV_BF16)
+        return pkv::fail(PKV_ERR_INVALID, "%s: unknown dtype", fn);
+    if (!std::isfinite(scale)) return pkv::fail(PKV_ERR_INVALID, "%s: scale is not finite", fn);
+    if (num_seqs == 0) return PKV_OK;
+    if (!block_tables) return pkv::fail(PKV_ERR_INVALID, "%s: NULL pointer", fn);
+    if (!aligned(block_tables, 4))
+        return pkv::fail(PKV_ERR_INVALID, "%s: int32 arrays must be 4-byte aligned", fn);
+    int64_t gu = 0, gs = 0;
+    bool groups =
+        group_caps(num_seqs, num_heads, head_dim, block_size, max_blocks_per_seq, &gu, &gs);
+    CUtensorMap tk, tv;
+    if (groups) {
+        // the prefix steps' tiled copies address pool rows with 32-bit coordinates
+        const int64_t rows = num_blocks * num_heads * (int64_t)block_size;
+        const int sub = pkv::step_tokens(head_dim);
+        const int box = block_size < sub ? block_size : sub;
+        groups = pool_map(&tk, dtype == PKV_BF16, k_cache, rows, head_dim, box) &&
+                 pool_map(&tv, dtype == PKV_BF16, v_cache, rows, head_dim, box);
+    }
+    const pkv::DecodeKernel* k =
+        groups ? (dtype == PKV_F16 ? pkv::decode_kernel_shared_f16(head_dim, block_size)
+                                   : pkv::decode_kernel_shared_bf16(head_dim, block_size))
+               : (dtype == PKV_F16 ? pkv::decode_kernel_f16(head_dim, block_size)
+                                   : pkv::decode_kernel_bf16(head_dim, block_size));
+    if (!k) return pkv::fail(PKV_ERR_INVALID, "%s: unsupported head_dim/block_size", fn);
+    pkv::DecodeArgs a = {};
+    a.block_tables = block_tables;
+    a.max_blocks = max_blocks_per_seq;
+    a.ctx_cap = max_blocks_per_seq * block_size;
+    a.kv_stride = 0;
+    a.num_blocks = num_blocks;
+    a.mode = groups ? pkv::kModeShared : pkv::kModePaged;
+    return launch_decode(fn, k, a, out, q, k_cache, v_cache, context_lens, scale, num_seqs,
+                         num_heads, head_dim, block_size, max_blocks_per_seq, partition_size,
+                         workspace, workspace_bytes, stream, groups ? gu : 0, groups ? gs : 0,
+                         groups ? &tk : nullptr, groups ? &tv : nullptr);
 }
 
 pkv_status pkv_set_decode_wait_limit(uint64_t ns, uint64_t* previous) {

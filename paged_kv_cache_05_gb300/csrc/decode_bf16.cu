@@ -21,8 +21,8 @@ const DecodeKernel* decode_kernel_bf16(int D, int B) {
 const DecodeKernel* decode_kernel_contig_bf16(int D) {
     using dec::Launcher;
     switch (D) {
-        case 64: return Launcher<__nv_bfloat16, 64, step_tokens(64), true>::get();
-        case 128: return Launcher<__nv_bfloat16, 128, step_tokens(128), true>::get();
+        case 64: return Launcher<__nv_bfloat16, 64, step_tokens(64), kModeContig>::get();
+        case 128: return Launcher<__nv_bfloat16, 128, step_tokens(128), kModeContig>::get();
         default: return nullptr;
     }
 }

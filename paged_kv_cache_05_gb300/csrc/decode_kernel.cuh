@@ -61,6 +61,7 @@
 #include <stdint.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "pkv_internal.h"
 
@@ -116,6 +117,17 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
             smem_addr(dst)),
         "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// 2-D tiled bulk tensor copy global -> this CTA's shared memory (the map's
+// swizzle applies), completion counted in bytes on `bar`.
+__device__ __forceinline__ void tensor_g2s(void* dst, const CUtensorMap* map, int x, int y,
+                                           uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
         : "memory");
 }
 
@@ -345,14 +357,16 @@ __device__ __forceinline__ void next_segment(Pos& p, const int* base, int S, int
     }
 }
 
-// Exclusive prefix of steps per sequence: base[s] = sum_{s' < s} ceil(ctx[s'] / SUB).
+// Exclusive prefix of steps per sequence: base[s] = sum_{s' < s} ceil(ctx[s'] / SUB)
+// - skip[s'] (skip: the steps a group reads for the sequence, or null).
 template <int SUB>
-__device__ void scan_steps(const int* ctx, int* base, int S, int* scratch) {
+__device__ void scan_steps(const int* ctx, int* base, int S, int* scratch,
+                           const int* skip = nullptr) {
     const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, w = tid >> 5;
     const int per = (S + nt - 1) / nt;
     const int b = min(tid * per, S), e = min(b + per, S);
     int local = 0;
-    for (int i = b; i < e; ++i) local += (ctx[i] + SUB - 1) / SUB;
+    for (int i = b; i < e; ++i) local += (ctx[i] + SUB - 1) / SUB - (skip ? skip[i] : 0);
     int incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -365,7 +379,7 @@ __device__ void scan_steps(const int* ctx, int* base, int S, int* scratch) {
     for (int i = 0; i < w; ++i) run += scratch[i];
     for (int i = b; i < e; ++i) {
         base[i] = run;
-        run += (ctx[i] + SUB - 1) / SUB;
+        run += (ctx[i] + SUB - 1) / SUB - (skip ? skip[i] : 0);
     }
     if (tid == nt - 1) base[S] = run;
     __syncthreads();
@@ -456,11 +470,432 @@ __device__ __forceinline__ int64_t claim_chunk(unsigned long long* word, uint64_
     return (int64_t)(old & 0xffffffull);
 }
 
-// ------------------------------------------------------------ the main kernel
-template <typename T, int D, int B, bool CONTIG>
-__global__ void __launch_bounds__(Cfg<D, B>::THREADS, PKV_DECODE_MIN_CTAS)
-    paged_decode_main(const DecodeArgs a) {
+// ------------------------------------------------------------ shared prefixes
+// Sequences adjacent in the batch whose tables begin with the same full blocks
+// (forks: parallel sampling, beam search) form groups; the group pass below
+// finds them and cuts each group's common prefix into units (a head and at
+// most group_unit_steps steps).  In the main kernel a unit's K/V steps are
+// staged once and one warp attends every member's query to them together:
+// scores S^T = K Q^T (16 tokens x 8 members per tensor-core product) and the
+// output O^T += V^T P^T, with the online softmax per member; the unit ends in
+// one partial (m, l, acc) per member, which the merge kernel combines with
+// the member's own (suffix) partials.  Results are the same attention: the
+// prefix is a contiguous run of each member's tokens, and the split-K rule
+// combines any partition of a row's tokens.
+
+// D = A B + C, m16n8k16, A row-major, B column-major, fp32 accumulate.
+template <typename T>
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1);
+template <>
+__device__ __forceinline__ void mma16816<__half>(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                                 uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+template <>
+__device__ __forceinline__ void mma16816<__nv_bfloat16>(float (&c)[4], const uint32_t (&a)[4],
+                                                        uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+// Transpose of an 8x8 16-bit matrix held one row pair per thread (the
+// fragment layout of the tensor-core products).
+__device__ __forceinline__ uint32_t movm_t(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+template <typename T>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi);
+template <>
+__device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+template <>
+__device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, float hi) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+template <typename T>
+__device__ __forceinline__ float2 unpack2(uint32_t w) {
+    if constexpr (std::is_same<T, __half>::value) {
+        return __half22float2(*reinterpret_cast<const __half2*>(&w));
+    } else {
+        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    }
+}
+
+// Block-wide scans over S values held one per sequence in shared memory, each
+// thread a contiguous range (in place).  `scratch` holds one int per warp.
+static __device__ void block_scan_max_incl(int* v, int S, int* scratch) {
+    const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, w = tid >> 5;
+    const int per = (S + nt - 1) / nt;
+    const int b = min(tid * per, S), e = min(b + per, S);
+    int local = -1;
+    for (int i = b; i < e; ++i) local = max(local, v[i]);
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl = max(incl, y);
+    }
+    if (lane == 31) scratch[w] = incl;
+    __syncthreads();
+    int run = -1;
+    for (int i = 0; i < w; ++i) run = max(run, scratch[i]);
+    const int y = __shfl_up_sync(kFull, incl, 1);
+    if (lane >= 1) run = max(run, y);
+    for (int i = b; i < e; ++i) {
+        run = max(run, v[i]);
+        v[i] = run;
+    }
+    __syncthreads();
+}
+// out[i] = sum_{i' < i} v[i'] for i <= S (out may alias nothing).
+static __device__ void block_scan_sum_excl(const int* v, int* out, int S, int* scratch) {
+    const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, w = tid >> 5;
+    const int per = (S + nt - 1) / nt;
+    const int b = min(tid * per, S), e = min(b + per, S);
+    int local = 0;
+    for (int i = b; i < e; ++i) local += v[i];
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) scratch[w] = incl;
+    __syncthreads();
+    int run = incl - local;
+    for (int i = 0; i < w; ++i) run += scratch[i];
+    for (int i = b; i < e; ++i) {
+        out[i] = run;
+        run += v[i];
+    }
+    if (tid == nt - 1) out[S] = run;
+    __syncthreads();
+}
+
+// The group pass: one CTA of kGroupPassThreads threads.  For each sequence s
+// >= 1 it counts the leading table entries equal to sequence s-1's among the
+// full blocks of both (the shared prefix), forms groups of adjacent
+// sequences, and writes per sequence its group prefix (in steps), member
+// index and first partial slot, and the list of units, into the workspace.
+// Groups only ever read the same blocks a member would read itself: when the
+// workspace cannot hold the units or their partials, nothing is grouped.
+constexpr int kGroupPassThreads = 1024;
+
+template <int D, int B>
+__global__ void __launch_bounds__(kGroupPassThreads) paged_decode_groups(const DecodeArgs a) {
+    constexpr int SUB = step_tokens(D);
+    constexpr int LG = group_unit_steps(D, B);
+    extern __shared__ int gsm[];
+    const int S = a.S, H = a.H, tid = threadIdx.x, nt = blockDim.x;
+    int* cs = gsm;                 // [S] clamped context lengths, later a leader's size
+    int* nf = cs + S;              // [S] full blocks s and s-1 both hold, later member slots
+    int* first = nf + S;           // [S] leading equal entries, then shared steps
+    int* rs = first + S;           // [S] start of s's run of followers
+    int* units = rs + S;           // [S] units of a leader's group, else 0
+    int* gP = units + S;           // [S] a leader's group prefix (steps)
+    int* ub = gP + S;              // [S + 1] pair prefix, then unit prefix
+    int* mb = ub + S + 1;          // [S + 1] member-slot prefix
+    int* scratch = mb + S + 1;     // [32]
+
+    grid_launch_dependents();      // the main kernel waits for this grid to end
+    grid_dependency_wait();
+    const int cap = a.ctx_cap;
+    for (int s = tid; s < S; s += nt) {
+        int c = a.context_lens[s];
+        cs[s] = c < 0 ? 0 : (c > cap ? cap : c);
+    }
+    __syncthreads();
+    for (int s = tid; s < S; s += nt) {
+        const int n = s >= 1 ? min(cs[s], cs[s - 1]) / B : 0;
+        nf[s] = n;
+        first[s] = n;
+    }
+    __syncthreads();
+    block_scan_sum_excl(nf, ub, S, scratch);
+    // the first entry that differs: every (sequence, entry) pair at once,
+    // four per thread per round with their loads issued together
+    const int pairs = ub[S];
+    for (int i0 = tid; i0 < pairs; i0 += 4 * nt) {
+        int ps[4], pj[4];
+        int32_t x[4], y[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int idx = i0 + k * nt;
+            ps[k] = -1;
+            x[k] = y[k] = 0;
+            if (idx < pairs) {
+                int lo = 1, hi = S - 1;            // the sequence: largest s with ub[s] <= idx
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (ub[mid] <= idx) lo = mid;
+                    else hi = mid - 1;
+                }
+                ps[k] = lo;
+                pj[k] = idx - ub[lo];
+                const int32_t* r0 = a.block_tables + (int64_t)lo * a.max_blocks + pj[k];
+                x[k] = __ldg(r0);
+                y[k] = __ldg(r0 - a.max_blocks);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            if (ps[k] >= 0 && x[k] != y[k]) atomicMin(&first[ps[k]], pj[k]);
+    }
+    __syncthreads();
+    // followers (a long enough prefix shared with s - 1) and runs of them
+    for (int s = tid; s < S; s += nt) {
+        const int steps = s >= 1 ? (first[s] * B) / SUB : 0;
+        first[s] = steps;
+        rs[s] = (s >= 1 && steps >= kGroupMinSteps) ? -1 : s;
+    }
+    __syncthreads();
+    block_scan_max_incl(rs, S, scratch);
+    // groups: every kGroupMax-th sequence of a run leads the next ones
+    int* gG = cs;                  // (context lengths no longer needed)
+    for (int s = tid; s < S; s += nt) {
+        int g = 1, P = 0;
+        if ((s - rs[s]) % kGroupMax == 0) {
+            P = kGroupMaxPrefixSteps;
+            for (int f = s + 1; f < S && f - s < kGroupMax && rs[f] == rs[s]; ++f) {
+                ++g;
+                P = min(P, first[f]);
+            }
+        }
+        if (g < 2) {
+            g = 1;
+            P = 0;
+        }
+        gG[s] = g;
+        gP[s] = P;
+        units[s] = g >= 2 ? H * ((P + LG - 1) / LG) : 0;
+        nf[s] = g * units[s];          // member slots of a leader's group
+    }
+    __syncthreads();
+    block_scan_sum_excl(units, ub, S, scratch);
+    block_scan_sum_excl(nf, mb, S, scratch);
+    const bool fits = (int64_t)ub[S] <= a.ws_l.gunit_cap && (int64_t)mb[S] <= a.ws_l.gslot_cap;
+    const int U = fits ? ub[S] : 0;
+    int* gh = reinterpret_cast<int*>(a.ws + a.ws_l.gh_off);
+    int* gseq = reinterpret_cast<int*>(a.ws + a.ws_l.gseq_off);
+    int* gslot = reinterpret_cast<int*>(a.ws + a.ws_l.gslot_off);
+    GroupUnit* gu = reinterpret_cast<GroupUnit*>(a.ws + a.ws_l.gunit_off);
+    if (tid == 0) {
+        gh[0] = U;
+        gh[1] = fits ? mb[S] : 0;
+    }
+    for (int s = tid; s < S; s += nt) {
+        const int L = s - (s - rs[s]) % kGroupMax;
+        const int g = gG[L];
+        int info = 0, slot = 0;
+        if (fits && g >= 2) {
+            const int n = s - L;
+            info = gP[L] | (n << 20) | ((g - 1) << 24);
+            slot = mb[L] + n * units[L];
+        }
+        gseq[s] = info;
+        gslot[s] = slot;
+    }
+    for (int u = tid; u < U; u += nt) {
+        int lo = 0, hi = S - 1;                  // the leader: largest s with ub[s] <= u
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (ub[mid] <= u) lo = mid;
+            else hi = mid - 1;
+        }
+        const int L = lo, P = gP[L], nc = units[L] / H;
+        const int r = u - ub[L], h = r / nc, c = r - h * nc;
+        GroupUnit x;
+        x.L = L;
+        x.h = h;
+        x.j0 = (int)((int64_t)c * P / nc);
+        x.len = (int)((int64_t)(c + 1) * P / nc) - x.j0;
+        x.g = gG[L];
+        x.slot0 = mb[L] + h * nc + c;
+        x.mstride = units[L];
+        x.pad = 0;
+        gu[u] = x;
+    }
+}
+
+// One unit of a group in one consumer warp: the warp owns steps g0 + NW i +
+// warp (i < n) of the ring; it attends every member of `x` to the unit's
+// steps (i < x.len; the rest are empty steps that only pass through), then
+// writes one partial per member.
+template <typename T, int D, int B>
+__device__ __forceinline__ void group_unit_consume(const DecodeArgs& a, const GroupUnit& x,
+                                                   bool valid, int n, uint32_t g0,
+                                                   unsigned char* ring, uint64_t* full,
+                                                   uint64_t* empty, volatile int* abort_flag,
+                                                   int warp, int lane) {
     using C = Cfg<D, B>;
+    constexpr int NKT = D / 16;          // k-tiles of a score product
+    constexpr int NMT = D / 16;          // m-tiles of the output product
+    constexpr int NTT = C::SUB / 16;     // 16-token tiles per step
+    constexpr bool BF = std::is_same<T, __nv_bfloat16>::value;
+    const int mem = lane >> 2, c4 = lane & 3;
+    uint32_t qb[NKT][2];
+    if (valid && mem < x.g) {
+        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+            static_cast<const T*>(a.q) + ((int64_t)(x.L + mem) * a.H + x.h) * D);
+#pragma unroll
+        for (int kt = 0; kt < NKT; ++kt) {
+            qb[kt][0] = __ldg(qrow + kt * 8 + c4);
+            qb[kt][1] = __ldg(qrow + kt * 8 + 4 + c4);
+        }
+    } else {
+#pragma unroll
+        for (int kt = 0; kt < NKT; ++kt) qb[kt][0] = qb[kt][1] = 0u;
+    }
+    float o[NMT][4];
+#pragma unroll
+    for (int mt = 0; mt < NMT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    // ldmatrix row addresses: K as the A operand (rows = tokens), V^T (rows = dims).
+    // A step's K (and V) is stored per 64-column half of D as SUB rows of 128
+    // bytes, 16-byte chunk c of row r at chunk c ^ (r mod 8) (the copies'
+    // 128-byte swizzle).
+    const int krow = ((lane >> 3) & 1) * 8 + (lane & 7), kcol = (lane >> 4) * 8;
+    const int vrow = (lane >> 4) * 8 + (lane & 7), vcol = ((lane >> 3) & 1) * 8;
+    auto swz = [](int row, int col) -> uint32_t {      // col: element index in [0, D)
+        return (uint32_t)((col >> 6) * (C::SUB * 128) + row * 128 +
+                          ((((col & 63) >> 3) ^ (row & 7)) << 4));
+    };
+    for (int i = 0; i < n; ++i) {
+        const uint32_t g = g0 + (uint32_t)(C::NW * i + warp);
+        const int stage = (int)(g % C::NSTAGE);
+        const uint32_t par = (g / C::NSTAGE) & 1u;
+        const bool got = !*abort_flag && wait_phase(&full[stage], par, abort_flag, a.wait_ns);
+        const bool have = __all_sync(kFull, got);
+        if (!have && lane == 0) note_timeout(abort_flag, a.err);
+        if (have && valid && i < x.len) {
+            const uint32_t ks = smem_addr(ring + (size_t)stage * C::STAGE);
+            const uint32_t vs = ks + C::CHUNK;
+            float sc[NTT][4];
+#pragma unroll
+            for (int tt = 0; tt < NTT; ++tt) {
+                sc[tt][0] = sc[tt][1] = sc[tt][2] = sc[tt][3] = 0.f;
+#pragma unroll
+                for (int kt = 0; kt < NKT; ++kt) {
+                    uint32_t af[4];
+                    ldsm_x4(af, ks + swz(tt * 16 + krow, kt * 16 + kcol));
+                    mma16816<T>(sc[tt], af, qb[kt][0], qb[kt][1]);
+                }
+            }
+            float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+            for (int tt = 0; tt < NTT; ++tt) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sc[tt][e] *= a.scale_log2;
+                mx0 = fmaxf(mx0, fmaxf(sc[tt][0], sc[tt][2]));
+                mx1 = fmaxf(mx1, fmaxf(sc[tt][1], sc[tt][3]));
+            }
+#pragma unroll
+            for (int o_ = 4; o_ < 32; o_ <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, o_));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, o_));
+            }
+            const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+            const float al0 = exp2f(m0 - n0), al1 = exp2f(m1 - n1);
+            m0 = n0;
+            m1 = n1;
+            l0 *= al0;
+            l1 *= al1;
+#pragma unroll
+            for (int mt = 0; mt < NMT; ++mt) {
+                o[mt][0] *= al0;
+                o[mt][1] *= al1;
+                o[mt][2] *= al0;
+                o[mt][3] *= al1;
+            }
+            uint32_t pb[NTT][2], pr[NTT][2];
+#pragma unroll
+            for (int tt = 0; tt < NTT; ++tt) {
+                const float p0 = exp2f(sc[tt][0] - n0), p1 = exp2f(sc[tt][1] - n1);
+                const float p2 = exp2f(sc[tt][2] - n0), p3 = exp2f(sc[tt][3] - n1);
+                l0 += p0 + p2;
+                l1 += p1 + p3;
+                const uint32_t hlo = pack2<T>(p0, p1), hhi = pack2<T>(p2, p3);
+                pb[tt][0] = movm_t(hlo);
+                pb[tt][1] = movm_t(hhi);
+                if constexpr (BF) {
+                    // bf16 keeps 8 significant bits: the weights go in as a
+                    // high part and the bf16 residual, two products
+                    const float2 q01 = unpack2<T>(hlo), q23 = unpack2<T>(hhi);
+                    pr[tt][0] = movm_t(pack2<T>(p0 - q01.x, p1 - q01.y));
+                    pr[tt][1] = movm_t(pack2<T>(p2 - q23.x, p3 - q23.y));
+                }
+            }
+#pragma unroll
+            for (int mt = 0; mt < NMT; ++mt) {
+#pragma unroll
+                for (int tt = 0; tt < NTT; ++tt) {
+                    uint32_t af[4];
+                    ldsm_x4_t(af, vs + swz(tt * 16 + vrow, mt * 16 + vcol));
+                    mma16816<T>(o[mt], af, pb[tt][0], pb[tt][1]);
+                    if constexpr (BF) mma16816<T>(o[mt], af, pr[tt][0], pr[tt][1]);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0 && have) mbar_arrive(&empty[stage]);
+    }
+    if (!valid || __any_sync(kFull, *abort_flag)) return;
+#pragma unroll
+    for (int o_ = 4; o_ < 32; o_ <<= 1) {
+        l0 += __shfl_xor_sync(kFull, l0, o_);
+        l1 += __shfl_xor_sync(kFull, l1, o_);
+    }
+    float2* gml = reinterpret_cast<float2*>(a.ws + a.ws_l.gml_off);
+    float* gacc = reinterpret_cast<float*>(a.ws + a.ws_l.gacc_off);
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const int member = 2 * c4 + e;
+        if (member >= x.g) continue;
+        const int64_t slot = (int64_t)x.slot0 + (int64_t)member * x.mstride;
+        if (mem == 0) gml[slot] = make_float2(e ? m1 : m0, e ? l1 : l0);
+        float* dst = gacc + slot * D + mem;
+#pragma unroll
+        for (int mt = 0; mt < NMT; ++mt) {
+            dst[mt * 16] = o[mt][e];
+            dst[mt * 16 + 8] = o[mt][2 + e];
+        }
+    }
+}
+
+// ------------------------------------------------------------ the main kernel
+// (with shared prefixes the tensor-core path raises the register count; the
+// bound keeps five CTAs per SM, as the plain kernel has)
+template <typename T, int D, int B, int MODE>
+__global__ void __launch_bounds__(Cfg<D, B>::THREADS,
+                                  MODE == kModeShared ? 5 : PKV_DECODE_MIN_CTAS)
+    paged_decode_main(const __grid_constant__ CUtensorMap tmk,
+                      const __grid_constant__ CUtensorMap tmv, const DecodeArgs a) {
+    using C = Cfg<D, B>;
+    constexpr bool CONTIG = MODE == kModeContig;
+    constexpr bool GROUPS = MODE == kModeShared;
     extern __shared__ __align__(1024) unsigned char smem[];
     unsigned char* ring = smem;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
@@ -471,6 +906,8 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, PKV_DECODE_MIN_CTAS)
     int* scratch = reinterpret_cast<int*>(smem + C::MISC_OFF) + 4;   // NW + 1 ints
     int* s_ctx = reinterpret_cast<int*>(smem + C::CTX_OFF);
     int* s_base = s_ctx + a.S;
+    // shared prefixes: the steps a group reads for each sequence, then the unit count
+    int* s_pfx = s_base + a.S + 1;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int S = a.S, H = a.H;
@@ -485,6 +922,11 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, PKV_DECODE_MIN_CTAS)
             c = c < 0 ? 0 : cap;
         }
         s_ctx[s] = c;
+        if constexpr (GROUPS)
+            s_pfx[s] = reinterpret_cast<const int*>(a.ws + a.ws_l.gseq_off)[s] & kGroupMaxPrefixSteps;
+    }
+    if constexpr (GROUPS) {
+        if (tid == 0) s_pfx[S] = reinterpret_cast<const int*>(a.ws + a.ws_l.gh_off)[0];
     }
     uint64_t* qfull = reinterpret_cast<uint64_t*>(smem + C::QBAR_OFF);
     int* qid = reinterpret_cast<int*>(smem + C::QID_OFF);
@@ -501,7 +943,9 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, PKV_DECODE_MIN_CTAS)
         *abort_flag = 0;
     }
     __syncthreads();
-    scan_steps<C::SUB>(s_ctx, s_base, S, scratch);
+    scan_steps<C::SUB>(s_ctx, s_base, S, scratch, GROUPS ? s_pfx : nullptr);
+    const int U = GROUPS ? s_pfx[S] : 0;                 // group units
+    const bool has_units = GROUPS && (int)blockIdx.x < U;
 
     // 2. the split of the step space, and this CTA's static range
     const Split sp = make_split((int64_t)H * s_base[S], (int)gridDim.x, a.L_steps,
@@ -529,20 +973,23 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, PKV_DECODE_MIN_CTAS)
         }
     }
     grid_launch_dependents();
-    if (!ws_ok || total == 0) return;
-    int64_t xb, xe;
-    if (sp.fixed) {
+    if (!ws_ok || (total == 0 && !has_units)) return;
+    int64_t xb = 0, xe = 0;
+    if (total == 0) {
+        // group units only
+    } else if (sp.fixed) {
         const int64_t K = (total + sp.Ls - 1) / sp.Ls;
         const int64_t kb = (int64_t)blockIdx.x * K / gridDim.x;
         const int64_t ke = (int64_t)(blockIdx.x + 1) * K / gridDim.x;
         xb = kb * sp.Ls;
         xe = ke * sp.Ls < total ? ke * sp.Ls : total;
-        if (xb >= xe) return;
+        if (xb >= xe && !has_units) return;
+        if (xb > xe) xb = xe;
     } else {
         xb = (int64_t)blockIdx.x * sp.Ls;
         xe = xb + sp.Ls < sp.X ? xb + sp.Ls : sp.X;
         if (xb > xe) xb = xe;                    // no static share: claimed chunks only
-        if (xb >= xe && sp.Kd == 0) return;
+        if (xb >= xe && sp.Kd == 0 && !has_units) return;
     }
     if (warp == C::NW) {
         // ================================================= producer warp
@@ -554,7 +1001,7 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, PKV_DECODE_MIN_CTAS)
         // block-table cache, warp-wide: the current 32-entry window, the next
         // window of the same sequence, and the first window of the next
         // sequence (both prefetched so no table read sits on the copy path)
-        int tc_s = -1, tc_win = 0, tc_val = 0, tn_val = 0, ts_s = -1, ts_val = 0;
+        int tc_s = -1, tc_win = 0, tc_val = 0, tn_val = 0, ts_s = -1, ts_val = 0, ts_win = 0;
         bool tn_ok = false;
         bool stop = false;
         // issue the copies of the steps [rb, re), in order, into the ring
@@ -565,8 +1012,10 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, PKV_DECODE_MIN_CTAS)
                 const int ns = s_base[p.s + 1] - s_base[p.s];
                 const int64_t left = re - x;
                 const int run = (int64_t)(ns - p.j) < left ? ns - p.j : (int)left;
+                // (a member of a group starts after the steps its group reads)
+                const int skip = GROUPS ? s_pfx[p.s] : 0;
                 for (int i = 0; i < run; ++i) {
-                    const int j = p.j + i;
+                    const int j = p.j + i + skip;
                     // first logical block of the step, and the step's token offset in it
                     const int jb = C::BPS > 1 ? j * C::BPS : j / C::SPB;
                     const int sub = C::BPS > 1 ? 0 : j - jb * C::SPB;
@@ -578,7 +1027,7 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, PKV_DECODE_MIN_CTAS)
                     if (p.s != tc_s || win != tc_win) {
                         if (p.s == tc_s && win == tc_win + 32 && tn_ok) {
                             tc_val = tn_val;
-                        } else if (p.s == ts_s && win == 0) {
+                        } else if (p.s == ts_s && win == ts_win) {
                             tc_val = ts_val;
                         } else {
                             tc_val = (win + lane < nblk) ? __ldg(row + win + lane) : 0;
@@ -589,8 +1038,12 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, PKV_DECODE_MIN_CTAS)
                             ts_s = -1;
                             if (s2 < S) {
                                 const int nb2 = (s_ctx[s2] + B - 1) / B;
-                                ts_val = lane < nb2 ? __ldg(a.block_tables + (int64_t)s2 * a.max_blocks + lane)
-                                                    : 0;
+                                const int j2 = GROUPS ? s_pfx[s2] : 0;
+                                ts_win = (C::BPS > 1 ? j2 * C::BPS : j2 / C::SPB) & ~31;
+                                ts_val = ts_win + lane < nb2
+                                             ? __ldg(a.block_tables + (int64_t)s2 * a.max_blocks +
+                                                     ts_win + lane)
+                                             : 0;
                                 ts_s = s2;
                             }
                         }
@@ -605,11 +1058,11 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, PKV_DECODE_MIN_CTAS)
                     }  // !CONTIG
                     int ok = 1;
                     if (lane == 0) {
-                        // an aborted CTA issues nothing more
-                        ok = (!*abort_flag &&
-                              wait_phase(&empty[stage], phase ^ 1u, abort_flag, a.wait_ns))
-                                 ? 1
-                                 : 0;
+                        // (after an abort a stage the consumers released is still
+                        // safe to fill -- its copy landed -- and the first one they
+                        // did not release stops this loop; the drain below waits
+                        // for everything issued)
+                        ok = wait_phase(&empty[stage], phase ^ 1u, abort_flag, a.wait_ns) ? 1 : 0;
                         if (ok) {
                             // only the step's valid tokens move (the last step of a
                             // row is usually partial); the rest of the stage keeps
@@ -667,6 +1120,95 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, PKV_DECODE_MIN_CTAS)
                 if (p.j == ns && x < re) next_segment(p, s_base, S, H);
             }
         };
+        if constexpr (GROUPS) {
+            // group units first: a batch of NW units (this CTA's next ones,
+            // one per consumer warp), interleaved step by step so that step g
+            // belongs to warp g mod NW; a unit that has run out is padded with
+            // empty steps (an arrival without bytes)
+            const GroupUnit* gu = reinterpret_cast<const GroupUnit*>(a.ws + a.ws_l.gunit_off);
+            for (int u0 = blockIdx.x; u0 < U && !stop; u0 += C::NW * (int)gridDim.x) {
+                GroupUnit ux[C::NW];
+                int tw[C::NW], jb0[C::NW], n = 0;
+#pragma unroll
+                for (int w = 0; w < C::NW; ++w) {
+                    const int u = u0 + w * (int)gridDim.x;
+                    if (u < U) {
+                        ux[w] = gu[u];
+                    } else {
+                        ux[w].L = 0;
+                        ux[w].h = 0;
+                        ux[w].j0 = 0;
+                        ux[w].len = 0;
+                    }
+                    n = max(n, ux[w].len);
+                    jb0[w] = C::BPS > 1 ? ux[w].j0 * C::BPS : ux[w].j0 / C::SPB;
+                    const int nblk = (s_ctx[ux[w].L] + B - 1) / B;
+                    tw[w] = (ux[w].len > 0 && jb0[w] + lane < nblk)
+                                ? __ldg(a.block_tables + (int64_t)ux[w].L * a.max_blocks + jb0[w] +
+                                        lane)
+                                : 0;
+                }
+                for (int i = 0; i < n && !stop; ++i) {
+#pragma unroll
+                    for (int w = 0; w < C::NW; ++w) {
+                        if (stop) break;
+                        const bool real = i < ux[w].len;
+                        const int j = ux[w].j0 + i;
+                        const int jb = C::BPS > 1 ? j * C::BPS : j / C::SPB;
+                        const int sub = C::BPS > 1 ? 0 : j - jb * C::SPB;
+                        int phys_raw[C::BPS];
+#pragma unroll
+                        for (int b = 0; b < C::BPS; ++b)
+                            phys_raw[b] = __shfl_sync(kFull, tw[w], (jb + b - jb0[w]) & 31);
+                        int ok = 1;
+                        if (lane == 0) {
+                            ok = wait_phase(&empty[stage], phase ^ 1u, abort_flag, a.wait_ns) ? 1 : 0;
+                            if (ok && !real) {
+                                mbar_arrive(&full[stage]);
+                            } else if (ok) {
+                                // a prefix step is whole (every member holds all of
+                                // its tokens); it is copied by tiled tensor copies
+                                // with the 128-byte swizzle: per 64-column half of
+                                // D, the step's rows of 128 bytes, chunk c of row r
+                                // at chunk c ^ (r mod 8), so that the tensor-core
+                                // fragment loads hit distinct banks
+                                unsigned char* dst = ring + (size_t)stage * C::STAGE;
+                                mbar_arrive_expect_tx(&full[stage], 2u * C::CHUNK);
+#pragma unroll
+                                for (int b = 0; b < C::BPS; ++b) {
+                                    int64_t phys = phys_raw[b];
+                                    if (phys < 0 || phys >= a.num_blocks) {
+                                        atomicOr(a.err, PKV_DEVERR_BAD_BLOCK);
+                                        phys = 0;
+                                    }
+                                    const int y = (int)((phys * H + ux[w].h) * B +
+                                                        (int64_t)sub * C::SUB);
+#pragma unroll
+                                    for (int hh = 0; hh < D / 64; ++hh) {
+                                        const uint32_t doff =
+                                            (uint32_t)(hh * C::SUB * 128 + b * C::TPC * 128);
+                                        tensor_g2s(dst + doff, &tmk, hh * 64, y, &full[stage]);
+                                        tensor_g2s(dst + C::CHUNK + doff, &tmv, hh * 64, y,
+                                                   &full[stage]);
+                                    }
+                                }
+                            }
+                        }
+                        ok = __shfl_sync(kFull, ok, 0);
+                        if (!ok) {
+                            if (lane == 0) note_timeout(abort_flag, a.err);
+                            stop = true;
+                            break;
+                        }
+                        ++issued;
+                        if (++stage == C::NSTAGE) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                }
+            }
+        }
         // the static range first; then (balanced split) claimed chunks, each
         // handed to the consumers through the queue with the query slice of
         // its first row
@@ -756,6 +1298,29 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, PKV_DECODE_MIN_CTAS)
 #if PKV_DECODE_DYN_PER_CTA != 0
     int qe = 0;
 #endif
+    if constexpr (GROUPS) {
+        // group units: the same batches as the producer's, this warp's unit
+        const GroupUnit* gu = reinterpret_cast<const GroupUnit*>(a.ws + a.ws_l.gunit_off);
+        for (int u0 = blockIdx.x; u0 < U; u0 += C::NW * (int)gridDim.x) {
+            int n = 0;
+#pragma unroll
+            for (int w = 0; w < C::NW; ++w) {
+                const int u = u0 + w * (int)gridDim.x;
+                if (u < U) n = max(n, gu[u].len);
+            }
+            const int um = u0 + warp * (int)gridDim.x;
+            const bool valid = um < U;
+            GroupUnit x;
+            if (valid) {
+                x = gu[um];
+            } else {
+                x.L = x.h = x.j0 = x.len = x.g = x.slot0 = x.mstride = x.pad = 0;
+            }
+            group_unit_consume<T, D, B>(a, x, valid, n, g0, ring, full, empty, abort_flag, warp,
+                                        lane);
+            g0 += (uint32_t)(C::NW * n);
+        }
+    }
     while (true) {
         if (rb >= re) {
 #if PKV_DECODE_DYN_PER_CTA == 0
@@ -792,7 +1357,8 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, PKV_DECODE_MIN_CTAS)
             if (cend - x < len64) len64 = cend - x;
             if (re - x < len64) len64 = re - x;
             const int len = (int)len64;
-            const bool whole = (p.j == 0 && len == ns);
+            const int skip = GROUPS ? s_pfx[p.s] : 0;   // steps its group read
+            const bool whole = (p.j == 0 && len == ns && skip == 0);
             const int ctx = s_ctx[p.s];
             const int64_t row = (int64_t)p.s * H + p.h;
     
@@ -826,7 +1392,7 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, PKV_DECODE_MIN_CTAS)
                 if (!have && lane == 0) note_timeout(abort_flag, a.err);
                 const uint4* Ks = reinterpret_cast<const uint4*>(ring + (size_t)stage * C::STAGE);
                 const uint4* Vs = Ks + C::CHUNK / 16;
-                const int nvalid = ctx - (p.j + i) * C::SUB;   // >= 1
+                const int nvalid = ctx - (p.j + i + skip) * C::SUB;   // >= 1
     
                 float part[C::NL];
     #pragma unroll
@@ -933,26 +1499,33 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, PKV_DECODE_MIN_CTAS)
 //   M = max_k m_k,  out = sum_k 2^(m_k - M) acc_k / sum_k 2^(m_k - M) l_k.
 constexpr int kMergeBatch = 8;
 
-template <typename T, int D, int B, bool CONTIG>
+template <typename T, int D, int B, int MODE>
 __global__ void __launch_bounds__(128) paged_decode_merge(const DecodeArgs a) {
     using C = Cfg<D, B>;
+    constexpr bool GROUPS = MODE == kModeShared;
+    constexpr int LG = group_unit_steps(D, B);
     extern __shared__ int msm[];            // base[S + 1], then 8 scan partials
     int* base = msm;
     int* scratch = msm + a.S + 1;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int S = a.S, H = a.H;
+    const int* gseq = reinterpret_cast<const int*>(a.ws + a.ws_l.gseq_off);
+    // With groups every CTA waits first: the steps a group read for each
+    // sequence (written by the group pass) enter the step prefix.
+    if constexpr (GROUPS) grid_dependency_wait();
 
     // the step prefix, as the main kernel forms it (same clamping)
     {
         const int cap = a.ctx_cap;
         const int per = (S + 127) / 128;
         const int b = min(tid * per, S), e = min(b + per, S);
-        int local = 0;
-        for (int i = b; i < e; ++i) {
+        auto steps = [&](int i) {
             int c = a.context_lens[i];
             c = c < 0 ? 0 : (c > cap ? cap : c);
-            local += (c + C::SUB - 1) / C::SUB;
-        }
+            return (c + C::SUB - 1) / C::SUB - (GROUPS ? (gseq[i] & kGroupMaxPrefixSteps) : 0);
+        };
+        int local = 0;
+        for (int i = b; i < e; ++i) local += steps(i);
         int incl = local;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -965,9 +1538,7 @@ __global__ void __launch_bounds__(128) paged_decode_merge(const DecodeArgs a) {
         for (int i = 0; i < warp; ++i) run += scratch[i];
         for (int i = b; i < e; ++i) {
             base[i] = run;
-            int c = a.context_lens[i];
-            c = c < 0 ? 0 : (c > cap ? cap : c);
-            run += (c + C::SUB - 1) / C::SUB;
+            run += steps(i);
         }
         if (tid == 127) base[S] = run;
         __syncthreads();
@@ -978,67 +1549,80 @@ __global__ void __launch_bounds__(128) paged_decode_merge(const DecodeArgs a) {
     // output rely on.  The other CTAs wait only where they merge, so those
     // with nothing to do leave at once.
     const bool anchor = blockIdx.x == 0;
-    if (anchor) grid_dependency_wait();
+    if (!GROUPS && anchor) grid_dependency_wait();
     const int64_t sh = (int64_t)blockIdx.x * 4 + warp;
     if (sh >= (int64_t)S * H) return;
     const int s = (int)(sh / H), h = (int)(sh - (int64_t)s * H);
     const int ns = base[s + 1] - base[s];
+    const int pfx = GROUPS ? (gseq[s] & kGroupMaxPrefixSteps) : 0;   // steps its group read
     const Split sp = make_split((int64_t)H * base[S], a.main_grid, a.L_steps, a.min_chunk_steps);
     const int64_t x0 = (int64_t)H * base[s] + (int64_t)h * ns;
     const int64_t kf = ns ? sp.chunk(x0) : 0, kl = ns ? sp.chunk(x0 + ns - 1) : 0;
-    if (ns > 0 && kf == kl) return;          // written by the main kernel
+    if (ns > 0 && kf == kl && pfx == 0) return;          // written by the main kernel
 
-    if (!anchor) grid_dependency_wait();
+    if (!GROUPS && !anchor) grid_dependency_wait();
     // the main kernel writes 0 here when it could not run (workspace too small)
     if (reinterpret_cast<const int64_t*>(a.ws)[0] != sp.Ls) return;
     constexpr int PER = D / 32;
     T* o = static_cast<T*>(a.out) + sh * D + lane * PER;
-    if (ns == 0) {
+    if (ns == 0 && pfx == 0) {
 #pragma unroll
         for (int e = 0; e < PER; ++e) o[e] = Elem<T>::zero();
         return;
     }
-    const float2* ml = reinterpret_cast<const float2*>(a.ws + a.ws_l.ml_off) + sh;
-    const float* accw = reinterpret_cast<const float*>(a.ws + a.ws_l.acc_off) + sh * D + lane * PER;
-    const int nk = (int)(kl - kf + 1);
     float M = -INFINITY, ls = 0.f, acc[PER];
 #pragma unroll
     for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-    for (int k0 = 0; k0 < nk; k0 += kMergeBatch) {
-        float2 mv[kMergeBatch];
-        float av[kMergeBatch][PER];
+    // fold partial slots [first, first + count) of (mlw, accw) into the state
+    auto absorb = [&](const float2* mlw, const float* accw, int64_t first, int count) {
+        for (int k0 = 0; k0 < count; k0 += kMergeBatch) {
+            float2 mv[kMergeBatch];
+            float av[kMergeBatch][PER];
 #pragma unroll
-        for (int u = 0; u < kMergeBatch; ++u) {
-            if (k0 + u < nk) {
-                const int64_t k = kf + k0 + u;
-                mv[u] = ml[k];
-                const float* r = accw + k * D;
-                if constexpr (PER == 4) {
-                    const float4 f = *reinterpret_cast<const float4*>(r);
-                    av[u][0] = f.x; av[u][1] = f.y; av[u][2] = f.z; av[u][3] = f.w;
-                } else {
-                    const float2 f = *reinterpret_cast<const float2*>(r);
-                    av[u][0] = f.x; av[u][1] = f.y;
+            for (int u = 0; u < kMergeBatch; ++u) {
+                if (k0 + u < count) {
+                    const int64_t k = first + k0 + u;
+                    mv[u] = mlw[k];
+                    const float* r = accw + k * D + lane * PER;
+                    if constexpr (PER == 4) {
+                        const float4 f = *reinterpret_cast<const float4*>(r);
+                        av[u][0] = f.x; av[u][1] = f.y; av[u][2] = f.z; av[u][3] = f.w;
+                    } else {
+                        const float2 f = *reinterpret_cast<const float2*>(r);
+                        av[u][0] = f.x; av[u][1] = f.y;
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kMergeBatch; ++u) {
+                if (k0 + u < count) {
+                    if (mv[u].x > M) {
+                        const float r = exp2f(M - mv[u].x);
+                        ls *= r;
+#pragma unroll
+                        for (int e = 0; e < PER; ++e) acc[e] *= r;
+                        M = mv[u].x;
+                    }
+                    const float sc = exp2f(mv[u].x - M);
+                    ls = fmaf(sc, mv[u].y, ls);
+#pragma unroll
+                    for (int e = 0; e < PER; ++e) acc[e] = fmaf(sc, av[u][e], acc[e]);
                 }
             }
         }
-#pragma unroll
-        for (int u = 0; u < kMergeBatch; ++u) {
-            if (k0 + u < nk) {
-                if (mv[u].x > M) {
-                    const float r = exp2f(M - mv[u].x);
-                    ls *= r;
-#pragma unroll
-                    for (int e = 0; e < PER; ++e) acc[e] *= r;
-                    M = mv[u].x;
-                }
-                const float sc = exp2f(mv[u].x - M);
-                ls = fmaf(sc, mv[u].y, ls);
-#pragma unroll
-                for (int e = 0; e < PER; ++e) acc[e] = fmaf(sc, av[u][e], acc[e]);
-            }
-        }
+    };
+    if (GROUPS && pfx > 0) {
+        // the group's partials of this member and head: one per unit
+        const int nc = (pfx + LG - 1) / LG;
+        const int64_t g0 =
+            (int64_t)reinterpret_cast<const int*>(a.ws + a.ws_l.gslot_off)[s] + (int64_t)h * nc;
+        absorb(reinterpret_cast<const float2*>(a.ws + a.ws_l.gml_off),
+               reinterpret_cast<const float*>(a.ws + a.ws_l.gacc_off), g0, nc);
     }
+    if (ns > 0)
+        absorb(reinterpret_cast<const float2*>(a.ws + a.ws_l.ml_off) + sh,
+               reinterpret_cast<const float*>(a.ws + a.ws_l.acc_off) + sh * D, kf,
+               (int)(kl - kf + 1));
 #pragma unroll
     for (int e = 0; e < PER; ++e) o[e] = Elem<T>::from_f32(acc[e] / ls);
 }
@@ -1046,11 +1630,13 @@ __global__ void __launch_bounds__(128) paged_decode_merge(const DecodeArgs a) {
 // ------------------------------------------------------------ host glue
 constexpr int kLimitDevices = 64;
 
-template <typename T, int D, int B, bool CONTIG = false>
+template <typename T, int D, int B, int MODE = kModePaged>
 struct Launcher {
     using C = Cfg<D, B>;
-    static size_t smem_bytes(int S) { return C::smem(S); }
+    static constexpr bool GROUPS = MODE == kModeShared;
+    static size_t smem_bytes(int S) { return C::smem(S) + (GROUPS ? 4 * (size_t)(S + 1) : 0); }
     static size_t merge_smem(int S) { return 4 * (size_t)(S + 1 + 8); }
+    static size_t groups_smem(int S) { return 4 * (8 * (size_t)S + 2 + 32); }
     // The dynamic shared memory limit of a kernel also steers the L1/shared
     // carveout the driver picks for it: with the limit at the device maximum
     // every launch got the largest carveout (228 KiB, the least L1), whatever
@@ -1062,6 +1648,7 @@ struct Launcher {
         std::mutex mu;
         int main[kLimitDevices] = {};
         int merge[kLimitDevices] = {};
+        int groups[kLimitDevices] = {};
     };
     static Limits& limits() {
         static Limits l;
@@ -1087,15 +1674,17 @@ struct Launcher {
         }
         Limits& L = limits();
         std::lock_guard<std::mutex> lk(L.mu);
-        e = set_limit(&L.main[dev], (const void*)paged_decode_main<T, D, B, CONTIG>, smem);
+        e = set_limit(&L.main[dev], (const void*)paged_decode_main<T, D, B, MODE>, smem);
         if (e != cudaSuccess) return e;
-        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, paged_decode_main<T, D, B, CONTIG>,
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, paged_decode_main<T, D, B, MODE>,
                                                              C::THREADS, smem);
     }
-    // Both kernels are launched as programmatic dependents of their
-    // predecessor in the stream: each waits (griddepcontrol.wait) before it
-    // reads anything, so only the launch latency overlaps the predecessor.
-    static cudaError_t launch(const DecodeArgs& args, int grid, cudaStream_t stream) {
+    // Every kernel is launched as a programmatic dependent of its predecessor
+    // in the stream: each waits (griddepcontrol.wait) before it reads anything,
+    // so only the launch latency overlaps the predecessor.  With shared
+    // prefixes the group pass (one CTA) runs first.
+    static cudaError_t launch(const DecodeArgs& args, int grid, cudaStream_t stream,
+                              const CUtensorMap& tk, const CUtensorMap& tv) {
         DecodeArgs a = args;
         a.main_grid = grid;
         int dev = 0;
@@ -1106,25 +1695,35 @@ struct Launcher {
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)grid);
-        cfg.blockDim = dim3(C::THREADS);
-        cfg.dynamicSmemBytes = C::smem(a.S);
         cfg.stream = stream;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         Limits& L = limits();
         std::lock_guard<std::mutex> lk(L.mu);
-        e = set_limit(&L.main[dev], (const void*)paged_decode_main<T, D, B, CONTIG>, cfg.dynamicSmemBytes);
+        if constexpr (GROUPS) {
+            cfg.gridDim = dim3(1);
+            cfg.blockDim = dim3(kGroupPassThreads);
+            cfg.dynamicSmemBytes = groups_smem(a.S);
+            e = set_limit(&L.groups[dev], (const void*)paged_decode_groups<D, B>,
+                          cfg.dynamicSmemBytes);
+            if (e != cudaSuccess) return e;
+            e = cudaLaunchKernelEx(&cfg, paged_decode_groups<D, B>, a);
+            if (e != cudaSuccess) return e;
+        }
+        cfg.gridDim = dim3((unsigned)grid);
+        cfg.blockDim = dim3(C::THREADS);
+        cfg.dynamicSmemBytes = smem_bytes(a.S);
+        e = set_limit(&L.main[dev], (const void*)paged_decode_main<T, D, B, MODE>, cfg.dynamicSmemBytes);
         if (e != cudaSuccess) return e;
-        e = cudaLaunchKernelEx(&cfg, paged_decode_main<T, D, B, CONTIG>, a);
+        e = cudaLaunchKernelEx(&cfg, paged_decode_main<T, D, B, MODE>, tk, tv, a);
         if (e != cudaSuccess) return e;
         const int64_t warps = (int64_t)a.S * a.H;
         cfg.gridDim = dim3((unsigned)((warps + 3) / 4));
         cfg.blockDim = dim3(128);
         cfg.dynamicSmemBytes = merge_smem(a.S);
-        e = set_limit(&L.merge[dev], (const void*)paged_decode_merge<T, D, B, CONTIG>, cfg.dynamicSmemBytes);
+        e = set_limit(&L.merge[dev], (const void*)paged_decode_merge<T, D, B, MODE>, cfg.dynamicSmemBytes);
         if (e != cudaSuccess) return e;
-        e = cudaLaunchKernelEx(&cfg, paged_decode_merge<T, D, B, CONTIG>, a);
+        e = cudaLaunchKernelEx(&cfg, paged_decode_merge<T, D, B, MODE>, a);
         if (e != cudaSuccess) return e;
         return cudaGetLastError();
     }

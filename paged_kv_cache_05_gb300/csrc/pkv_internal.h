@@ -5,6 +5,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <cuda.h>
 #include <cuda_runtime_api.h>
 
 #include "pagedkv.h"
@@ -35,6 +36,11 @@ int sm_count(int device);
 #define PKV_DECODE_DYN_PER_CTA 4
 #endif
 
+// Tokens per pipeline step: a step moves 4 KiB of K and 4 KiB of V (16 tokens
+// at head_dim 128, 32 at head_dim 64), from one block or from several
+// consecutive logical blocks when the block size is smaller.
+__host__ __device__ constexpr int step_tokens(int D) { return 2048 / D; }
+
 // ---- decode workspace layout -------------------------------------------------
 // [0, 64)                  header: int64 static chunk length, int64 total steps,
 //                          uint64 claim word of the dynamic chunks (epoch << 24 | count)
@@ -42,27 +48,68 @@ int sm_count(int device);
 // then, 256-aligned:       float2 ml[cap]   (running max in log2 units, sum)
 // then, 256-aligned:       float  acc[cap][D] (unnormalised output)
 // cap = S * H + (max number of chunks)
+//
+// The shared-prefix entry point appends, 256-aligned:
+//   int32 gh[16]             U (group units), slots used, written by the group pass
+//   int32 gseq[S]            per sequence: group prefix steps (bits 0-19), member
+//                            index (20-23), group size - 1 (24-26); 0 = no group
+//   int32 gslot[S]           per sequence: its first group partial slot (head 0)
+//   GroupUnit gunit[gunit_cap]
+//   float2 gml[gslot_cap], float gacc[gslot_cap][D]   group partials
 struct WsLayout {
     size_t base_off, ml_off, acc_off, total;
     int64_t cap;
+    size_t gh_off, gseq_off, gslot_off, gunit_off, gml_off, gacc_off;
+    int64_t gunit_cap, gslot_cap;
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-__host__ __device__ inline WsLayout ws_layout(int S, int H, int D, int64_t max_chunks) {
+__host__ __device__ inline WsLayout ws_layout(int S, int H, int D, int64_t max_chunks,
+                                              int64_t gunit_cap = 0, int64_t gslot_cap = 0) {
     WsLayout w;
     w.cap = (int64_t)S * H + max_chunks;
     w.base_off = 64;
     w.ml_off = align_up(w.base_off + 4 * (size_t)(S + 1), 256);
     w.acc_off = align_up(w.ml_off + 8 * (size_t)w.cap, 256);
     w.total = align_up(w.acc_off + 4 * (size_t)w.cap * D, 256);
+    w.gunit_cap = gunit_cap;
+    w.gslot_cap = gslot_cap;
+    w.gh_off = w.gseq_off = w.gslot_off = w.gunit_off = w.gml_off = w.gacc_off = w.total;
+    if (gslot_cap > 0) {
+        w.gh_off = w.total;
+        w.gseq_off = w.gh_off + 64;
+        w.gslot_off = align_up(w.gseq_off + 4 * (size_t)S, 16);
+        w.gunit_off = align_up(w.gslot_off + 4 * (size_t)S, 256);
+        w.gml_off = align_up(w.gunit_off + 32 * (size_t)gunit_cap, 256);
+        w.gacc_off = align_up(w.gml_off + 8 * (size_t)gslot_cap, 256);
+        w.total = align_up(w.gacc_off + 4 * (size_t)gslot_cap * D, 256);
+    }
     return w;
 }
 
-// Tokens per pipeline step: a step moves 4 KiB of K and 4 KiB of V (16 tokens
-// at head_dim 128, 32 at head_dim 64), from one block or from several
-// consecutive logical blocks when the block size is smaller.
-__host__ __device__ constexpr int step_tokens(int D) { return 2048 / D; }
+// ---- shared prefixes -----------------------------------------------------------
+// Sequences adjacent in the batch whose block tables begin with the same full
+// blocks form a group (at most kGroupMax members, a common prefix of at least
+// kGroupMinSteps steps).  The group's common prefix is read once and attended
+// by every member together; each member's own blocks are read as usual.
+constexpr int kGroupMax = 8;
+constexpr int kGroupMinSteps = 4;
+constexpr int kGroupMaxSeqs = 4096;
+constexpr int kGroupMaxPrefixSteps = (1 << 20) - 1;
+// Steps per group unit: a unit's blocks fit one 32-entry table window.
+__host__ __device__ constexpr int group_unit_steps(int D, int B) {
+    return B < step_tokens(D) ? 32 / (step_tokens(D) / B) : 32;
+}
+struct GroupUnit {
+    int L;        // the group's first sequence (its table is read)
+    int h;        // head
+    int j0, len;  // steps [j0, j0 + len) of the common prefix
+    int g;        // members: sequences L .. L + g - 1
+    int slot0;    // partial slot of member 0; member n at slot0 + n * mstride
+    int mstride;
+    int pad;
+};
 
 // Upper bound of the steps one sequence can have.
 __host__ __device__ inline int64_t max_steps_per_seq(int D, int B, int max_blocks) {
@@ -88,14 +135,17 @@ struct DecodeArgs {
     int main_grid;           // CTAs of the main kernel
     uint64_t epoch;          // 40-bit tag of this call (claims of the dynamic chunks)
     uint64_t wait_ns;        // bound of the pipeline waits (pkv_set_decode_wait_limit)
+    int mode;                // decode kind (kModePaged, kModeContig, kModeShared)
     char* ws;
     WsLayout ws_l;
     int32_t* err;
 };
 
 struct DecodeKernel {
-    // launch main + merge on `stream`; grid = number of persistent CTAs
-    cudaError_t (*launch)(const DecodeArgs& a, int grid, cudaStream_t stream);
+    // launch main + merge on `stream`; grid = number of persistent CTAs; tk/tv:
+    // tiled maps of the K and V pools (read by the shared-prefix kernels only)
+    cudaError_t (*launch)(const DecodeArgs& a, int grid, cudaStream_t stream,
+                          const CUtensorMap& tk, const CUtensorMap& tv);
     // dynamic shared memory of the main kernel for S sequences
     size_t (*smem_bytes)(int S);
     // CTAs per SM the main kernel can keep resident with that shared memory
@@ -108,6 +158,10 @@ const DecodeKernel* decode_kernel_bf16(int D, int B);
 // the same kernels over a contiguous [seq][head][token][D] K/V layout (no block table)
 const DecodeKernel* decode_kernel_contig_f16(int D);
 const DecodeKernel* decode_kernel_contig_bf16(int D);
+// the paged kernels with shared prefixes read once (a group pass launched first)
+const DecodeKernel* decode_kernel_shared_f16(int D, int B);
+const DecodeKernel* decode_kernel_shared_bf16(int D, int B);
+enum : int { kModePaged = 0, kModeContig = 1, kModeShared = 2 };
 
 // ---- cache kernels -----------------------------------------------------------
 cudaError_t launch_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,

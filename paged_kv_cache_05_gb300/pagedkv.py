@@ -57,6 +57,10 @@ def lib():
             "pkv_decode_workspace_size": ([i32, i32, i32, i32, i32, i32, ctypes.POINTER(sz)], i32),
             "pkv_paged_attention_decode": ([P, P, P, P, P, P, f32, i32, i32, i32, i32, i32, i64,
                                             i32, i32, P, sz, P], i32),
+            "pkv_decode_shared_workspace_size": ([i32, i32, i32, i32, i32, i32,
+                                                  ctypes.POINTER(sz)], i32),
+            "pkv_paged_attention_decode_shared": ([P, P, P, P, P, P, f32, i32, i32, i32, i32,
+                                                   i32, i64, i32, i32, P, sz, P], i32),
             "pkv_contiguous_workspace_size": ([i32, i32, i32, i32, i32, ctypes.POINTER(sz)],
                                               i32),
             "pkv_contiguous_attention_decode": ([P, P, P, P, P, f32, i32, i32, i32, i32, i32,
@@ -195,6 +199,45 @@ def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens,
                                             int(partition_size), wsp,
                                             workspace.numel() * workspace.element_size(),
                                             _stream(stream)))
+    return out
+
+
+def decode_shared_workspace_size(num_seqs, num_heads, head_dim, block_size, max_blocks_per_seq,
+                                 partition_size=0) -> int:
+    out = ctypes.c_size_t(0)
+    _check("pkv_decode_shared_workspace_size",
+           lib().pkv_decode_shared_workspace_size(num_seqs, num_heads, head_dim, block_size,
+                                                  max_blocks_per_seq, partition_size,
+                                                  ctypes.byref(out)))
+    return out.value
+
+
+def paged_attention_decode_shared(out, q, k_cache, v_cache, block_tables, context_lens, scale,
+                                  partition_size=0, workspace=None, stream=None):
+    """paged_attention_decode for batches whose adjacent sequences share prefix
+    blocks: each group's common prefix is read once for all its members."""
+    torch = _torch()
+    S, H, D = q.shape
+    nb, H2, B, D2 = k_cache.shape
+    if (H2, D2) != (H, D) or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("q / cache shape mismatch")
+    if tuple(out.shape) != (S, H, D) or out.dtype != q.dtype or k_cache.dtype != q.dtype:
+        raise ValueError("out/q/cache dtype or shape mismatch")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S:
+        raise ValueError("block_tables must be [num_seqs, max_blocks]")
+    if workspace is None:
+        n = decode_shared_workspace_size(S, H, D, B, block_tables.shape[1], partition_size)
+        workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
+    ptrs = [_dev(out, "out"), _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+            _dev(block_tables, "block_tables", torch.int32),
+            _dev(context_lens, "context_lens", torch.int32, 1)]
+    _check("pkv_paged_attention_decode_shared",
+           lib().pkv_paged_attention_decode_shared(*ptrs, float(scale), S, H, D, B,
+                                                   block_tables.shape[1], nb,
+                                                   _dtype_code(q.dtype), int(partition_size),
+                                                   _dev(workspace, "workspace"),
+                                                   workspace.numel() * workspace.element_size(),
+                                                   _stream(stream)))
     return out
 
 

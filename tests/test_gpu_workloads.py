@@ -185,6 +185,13 @@ def test_shared_prefix_copy_on_write(pkv):
         pkv.paged_attention_decode(out, q, kc, vc, bt, cl, spec.scale, partition_size=part)
         assert pkv.get_device_error() == 0
         attn_check(out, expect, "shared prefix partition=%d" % part)
+    # the shared-prefix entry point: each group's prompt blocks read once
+    for part in (0, 512):
+        out = torch.full_like(q, float("nan"))
+        pkv.paged_attention_decode_shared(out, q, kc, vc, bt, cl, spec.scale,
+                                          partition_size=part)
+        assert pkv.get_device_error() == 0
+        attn_check(out, expect, "shared prefix, groups read once, partition=%d" % part)
 
 
 def test_long_context_split_k(pkv):
