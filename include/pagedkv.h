@@ -148,7 +148,7 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* k_ca
  * Results are those of pkv_paged_attention_decode (same definition, within the
  * same tolerance; not bit-identical, the summation order differs).  Sharers
  * that are not adjacent are computed correctly, each reading its blocks.
- * Three launches on `stream` (a one-CTA group pass, the main pass, the merge).
+ * Three launches on `stream` (a small group pass, the main pass, the merge).
  * Arguments as for pkv_paged_attention_decode; the workspace is sized by
  * pkv_decode_shared_workspace_size.  Batches above 4096 sequences run the
  * plain kernels (no grouping).

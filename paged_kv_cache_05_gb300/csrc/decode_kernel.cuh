@@ -595,7 +595,50 @@ static __device__ void block_scan_sum_excl(const int* v, int* out, int S, int* s
     __syncthreads();
 }
 
-// The group pass: one CTA of kGroupPassThreads threads.  For each sequence s
+// out1[i] = sum_{i' < i} v1[i'], out2 likewise, for i <= S, in one pass.
+static __device__ void block_scan_sum2_excl(const int* v1, const int* v2, int* out1, int* out2,
+                                            int S, int* scratch) {
+    const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, w = tid >> 5;
+    const int per = (S + nt - 1) / nt;
+    const int b = min(tid * per, S), e = min(b + per, S);
+    int l1 = 0, l2 = 0;
+    for (int i = b; i < e; ++i) {
+        l1 += v1[i];
+        l2 += v2[i];
+    }
+    int i1 = l1, i2 = l2;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y1 = __shfl_up_sync(kFull, i1, o), y2 = __shfl_up_sync(kFull, i2, o);
+        if (lane >= o) {
+            i1 += y1;
+            i2 += y2;
+        }
+    }
+    if (lane == 31) {
+        scratch[w] = i1;
+        scratch[32 + w] = i2;
+    }
+    __syncthreads();
+    int r1 = i1 - l1, r2 = i2 - l2;
+    for (int i = 0; i < w; ++i) {
+        r1 += scratch[i];
+        r2 += scratch[32 + i];
+    }
+    for (int i = b; i < e; ++i) {
+        out1[i] = r1;
+        out2[i] = r2;
+        r1 += v1[i];
+        r2 += v2[i];
+    }
+    if (tid == nt - 1) {
+        out1[S] = r1;
+        out2[S] = r2;
+    }
+    __syncthreads();
+}
+
+// The group pass: kGroupPassCtas CTAs of kGroupPassThreads threads.  For each sequence s
 // >= 1 it counts the leading table entries equal to sequence s-1's among the
 // full blocks of both (the shared prefix), forms groups of adjacent
 // sequences, and writes per sequence its group prefix (in steps), member
@@ -603,6 +646,7 @@ static __device__ void block_scan_sum_excl(const int* v, int* out, int S, int* s
 // Groups only ever read the same blocks a member would read itself: when the
 // workspace cannot hold the units or their partials, nothing is grouped.
 constexpr int kGroupPassThreads = 1024;
+constexpr int kGroupPassCtas = 8;      // all find the groups; they share the unit writes
 
 template <int D, int B>
 __global__ void __launch_bounds__(kGroupPassThreads) paged_decode_groups(const DecodeArgs a) {
@@ -618,7 +662,7 @@ __global__ void __launch_bounds__(kGroupPassThreads) paged_decode_groups(const D
     int* gP = units + S;           // [S] a leader's group prefix (steps)
     int* ub = gP + S;              // [S + 1] pair prefix, then unit prefix
     int* mb = ub + S + 1;          // [S + 1] member-slot prefix
-    int* scratch = mb + S + 1;     // [32]
+    int* scratch = mb + S + 1;     // [64]
 
     grid_launch_dependents();      // the main kernel waits for this grid to end
     grid_dependency_wait();
@@ -634,35 +678,28 @@ __global__ void __launch_bounds__(kGroupPassThreads) paged_decode_groups(const D
         first[s] = n;
     }
     __syncthreads();
-    block_scan_sum_excl(nf, ub, S, scratch);
-    // the first entry that differs: every (sequence, entry) pair at once,
-    // four per thread per round with their loads issued together
-    const int pairs = ub[S];
-    for (int i0 = tid; i0 < pairs; i0 += 4 * nt) {
-        int ps[4], pj[4];
-        int32_t x[4], y[4];
+    // the first entry that differs: tps threads per sequence, each taking
+    // every tps-th entry, four entries' loads issued together
+    {
+        const int tps = S < nt ? nt / S : 1;
+        const int r = tid % tps;
+        for (int s = 1 + tid / tps; s < S; s += nt / tps) {
+            const int n = nf[s];
+            const int32_t* r0 = a.block_tables + (int64_t)s * a.max_blocks;
+            const int32_t* r1 = r0 - a.max_blocks;
+            for (int j0 = r; j0 < n; j0 += 4 * tps) {
+                int32_t x[4], y[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int idx = i0 + k * nt;
-            ps[k] = -1;
-            x[k] = y[k] = 0;
-            if (idx < pairs) {
-                int lo = 1, hi = S - 1;            // the sequence: largest s with ub[s] <= idx
-                while (lo < hi) {
-                    const int mid = (lo + hi + 1) >> 1;
-                    if (ub[mid] <= idx) lo = mid;
-                    else hi = mid - 1;
+                for (int k = 0; k < 4; ++k) {
+                    const int j = j0 + k * tps;
+                    x[k] = j < n ? __ldg(r0 + j) : 0;
+                    y[k] = j < n ? __ldg(r1 + j) : 0;
                 }
-                ps[k] = lo;
-                pj[k] = idx - ub[lo];
-                const int32_t* r0 = a.block_tables + (int64_t)lo * a.max_blocks + pj[k];
-                x[k] = __ldg(r0);
-                y[k] = __ldg(r0 - a.max_blocks);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    if (x[k] != y[k]) atomicMin(&first[s], j0 + k * tps);
             }
         }
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-            if (ps[k] >= 0 && x[k] != y[k]) atomicMin(&first[ps[k]], pj[k]);
     }
     __syncthreads();
     // followers (a long enough prefix shared with s - 1) and runs of them
@@ -694,44 +731,48 @@ __global__ void __launch_bounds__(kGroupPassThreads) paged_decode_groups(const D
         nf[s] = g * units[s];          // member slots of a leader's group
     }
     __syncthreads();
-    block_scan_sum_excl(units, ub, S, scratch);
-    block_scan_sum_excl(nf, mb, S, scratch);
+    block_scan_sum2_excl(units, nf, ub, mb, S, scratch);
     const bool fits = (int64_t)ub[S] <= a.ws_l.gunit_cap && (int64_t)mb[S] <= a.ws_l.gslot_cap;
     const int U = fits ? ub[S] : 0;
     int* gh = reinterpret_cast<int*>(a.ws + a.ws_l.gh_off);
     int* gseq = reinterpret_cast<int*>(a.ws + a.ws_l.gseq_off);
     int* gslot = reinterpret_cast<int*>(a.ws + a.ws_l.gslot_off);
     GroupUnit* gu = reinterpret_cast<GroupUnit*>(a.ws + a.ws_l.gunit_off);
-    if (tid == 0) {
-        gh[0] = U;
-        gh[1] = fits ? mb[S] : 0;
-    }
-    for (int s = tid; s < S; s += nt) {
-        const int L = s - (s - rs[s]) % kGroupMax;
-        const int g = gG[L];
-        int info = 0, slot = 0;
-        if (fits && g >= 2) {
-            const int n = s - L;
-            info = gP[L] | (n << 20) | ((g - 1) << 24);
-            slot = mb[L] + n * units[L];
+    if (blockIdx.x == 0) {
+        if (tid == 0) {
+            gh[0] = U;
+            gh[1] = fits ? mb[S] : 0;
         }
-        gseq[s] = info;
-        gslot[s] = slot;
+        for (int s = tid; s < S; s += nt) {
+            const int L = s - (s - rs[s]) % kGroupMax;
+            const int g = gG[L];
+            int info = 0, slot = 0;
+            if (fits && g >= 2) {
+                const int n = s - L;
+                info = gP[L] | (n << 20) | ((g - 1) << 24);
+                slot = mb[L] + n * units[L];
+            }
+            gseq[s] = info;
+            gslot[s] = slot;
+        }
     }
-    for (int u = tid; u < U; u += nt) {
+    // the units, this CTA's share: (leader, head, part); a prefix of P steps
+    // in nc parts, the first P mod nc of them one step longer
+    for (int u = blockIdx.x * nt + tid; u < U; u += gridDim.x * nt) {
         int lo = 0, hi = S - 1;                  // the leader: largest s with ub[s] <= u
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
             if (ub[mid] <= u) lo = mid;
             else hi = mid - 1;
         }
-        const int L = lo, P = gP[L], nc = units[L] / H;
+        const int L = lo, P = gP[L], nc = (P + LG - 1) / LG;
         const int r = u - ub[L], h = r / nc, c = r - h * nc;
+        const int q = P / nc, rem = P - q * nc;
         GroupUnit x;
         x.L = L;
         x.h = h;
-        x.j0 = (int)((int64_t)c * P / nc);
-        x.len = (int)((int64_t)(c + 1) * P / nc) - x.j0;
+        x.j0 = c * q + (c < rem ? c : rem);
+        x.len = q + (c < rem ? 1 : 0);
         x.g = gG[L];
         x.slot0 = mb[L] + h * nc + c;
         x.mstride = units[L];
@@ -1636,7 +1677,7 @@ struct Launcher {
     static constexpr bool GROUPS = MODE == kModeShared;
     static size_t smem_bytes(int S) { return C::smem(S) + (GROUPS ? 4 * (size_t)(S + 1) : 0); }
     static size_t merge_smem(int S) { return 4 * (size_t)(S + 1 + 8); }
-    static size_t groups_smem(int S) { return 4 * (8 * (size_t)S + 2 + 32); }
+    static size_t groups_smem(int S) { return 4 * (8 * (size_t)S + 2 + 64); }
     // The dynamic shared memory limit of a kernel also steers the L1/shared
     // carveout the driver picks for it: with the limit at the device maximum
     // every launch got the largest carveout (228 KiB, the least L1), whatever
@@ -1682,7 +1723,7 @@ struct Launcher {
     // Every kernel is launched as a programmatic dependent of its predecessor
     // in the stream: each waits (griddepcontrol.wait) before it reads anything,
     // so only the launch latency overlaps the predecessor.  With shared
-    // prefixes the group pass (one CTA) runs first.
+    // prefixes the group pass (kGroupPassCtas CTAs) runs first.
     static cudaError_t launch(const DecodeArgs& args, int grid, cudaStream_t stream,
                               const CUtensorMap& tk, const CUtensorMap& tv) {
         DecodeArgs a = args;
@@ -1701,7 +1742,7 @@ struct Launcher {
         Limits& L = limits();
         std::lock_guard<std::mutex> lk(L.mu);
         if constexpr (GROUPS) {
-            cfg.gridDim = dim3(1);
+            cfg.gridDim = dim3(kGroupPassCtas);
             cfg.blockDim = dim3(kGroupPassThreads);
             cfg.dynamicSmemBytes = groups_smem(a.S);
             e = set_limit(&L.groups[dev], (const void*)paged_decode_groups<D, B>,
