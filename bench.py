@@ -425,9 +425,11 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--op", choices=["step", "swap", "sharing", "prefill"], default="step",
+    ap.add_argument("--op", choices=["step", "swap", "sharing", "prefill", "layout"],
+                    default="step",
                     help="step: the decode layer-step (default); swap: block swap GPU<->CPU; "
-                         "sharing: memory saved by block sharing (host only)")
+                         "sharing: memory saved by block sharing (host only); prefill: the "
+                         "prompt phase; layout: paged against contiguous-layout decode")
     ap.add_argument("--workload", default="opt13b", choices=sorted(W.SPECS))
     ap.add_argument("--dtype", choices=["f16", "bf16"], default="f16",
                     help="storage type of q and the caches for --op prefill")
@@ -477,6 +479,8 @@ def main():
         return bench_swap(args)
     if args.op == "prefill":
         return bench_prefill(args)
+    if args.op == "layout":
+        return bench_layout(args)
 
     if not torch.cuda.is_available():
         raise SystemExit("bench.py: no CUDA device")
@@ -1194,6 +1198,65 @@ def bench_swap(args):
                       "config": {"heads": H, "head_dim": D, "dtype": "f16",
                                  "bytes_per_direction": total},
                       "results": rows}), flush=True)
+
+
+def bench_layout(args):
+    """Paged against contiguous-layout decode attention on the OPT-13B, short
+    and long batches: three alternating rounds of back-to-back calls of each
+    in one process (attention call only; the contiguous K/V are [S][H][T][D]
+    with T the batch's longest context, no block table)."""
+    import torch
+    from paged_kv_cache_05_gb300 import build
+    build.build()
+    dev = torch.device("cuda", 0)
+    out_all = {}
+    for name in ("opt13b", "short", "long"):
+        wl = Workload(name, dev, layers=(8 if name == "opt13b" else None))
+        spec = W.SPECS[name]
+        ctx = W.context_lens(spec)
+        S, H, D = spec.num_seqs, spec.num_heads, spec.head_dim
+        T = int(ctx.max())
+        k = W.device_normal((S, H, T, D), spec.dtype, spec.seed * 1000 + 903, dev)
+        v = W.device_normal((S, H, T, D), spec.dtype, spec.seed * 1000 + 904, dev)
+        ws = torch.empty(wl.pkv.contiguous_workspace_size(S, H, D, T, wl.partition),
+                         dtype=torch.uint8, device=dev)
+        out = torch.empty_like(wl.q)
+
+        def contig(i):
+            wl.pkv.contiguous_attention_decode(out, wl.q, k, v, wl.ctx, wl.scale, wl.partition,
+                                               ws)
+
+        def timed(fn, n):
+            for i in range(10):
+                fn(i)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            a.record()
+            for i in range(n):
+                fn(i)
+            b.record()
+            torch.cuda.synchronize()
+            return a.elapsed_time(b) / n * 1e3
+
+        n = 600 if name == "long" else 1500
+        pg, ct = [], []
+        for _ in range(3):
+            pg.append(timed(wl.attention, n))
+            ct.append(timed(contig, n))
+        if wl.pkv.get_device_error() != 0:
+            raise SystemExit("bench.py --op layout: device error bits")
+        cbytes = wl.attn_bytes - sum(-(-int(c) // wl.B) for c in ctx) * 4
+        pm, cm = float(np.median(pg)), float(np.median(ct))
+        out_all[name] = {"paged_us": [round(x, 2) for x in pg],
+                         "contiguous_us": [round(x, 2) for x in ct],
+                         "paged_over_contiguous": round(pm / cm, 4),
+                         "paged_GB/s": round(wl.attn_bytes / (pm * 1e-6) / 1e9, 1),
+                         "contiguous_GB/s": round(cbytes / (cm * 1e-6) / 1e9, 1),
+                         "contiguous_T": T, "paged_pool_blocks": wl.nb}
+        del wl, k, v, ws
+        torch.cuda.empty_cache()
+    print(json.dumps({"op": "layout", "metric": "paged / contiguous decode attention time",
+                      "results": out_all}), flush=True)
 
 
 def bench_prefill(args):
