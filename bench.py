@@ -1307,8 +1307,13 @@ def measure_prefill(dt: str, warmup: int, seconds: float, min_calls: int = 10) -
     def attn():
         pkv.paged_attention_prefill(out, q, kc, vc, bt, cl, qs, spec.scale, maxq)
 
+    def fused():
+        # the same step in one kernel: the cache write beside the attention
+        pkv.paged_attention_prefill_write(out, q, k, v, kc, vc, bt, cl, qs, spec.scale, maxq)
+
     for _ in range(max(3, warmup)):
         step()
+        fused()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record()
     for _ in range(5):
@@ -1331,6 +1336,12 @@ def measure_prefill(dt: str, warmup: int, seconds: float, min_calls: int = 10) -
     b.record()
     torch.cuda.synchronize()
     t_attn = a.elapsed_time(b) / K * 1e-3
+    a.record()
+    for _ in range(K):
+        fused()
+    b.record()
+    torch.cuda.synchronize()
+    t_fused = a.elapsed_time(b) / K * 1e-3
     clocks = sampler.stop()
     if pkv.get_device_error() != 0:
         raise SystemExit("bench.py prefill: device error bits")
@@ -1344,7 +1355,12 @@ def measure_prefill(dt: str, warmup: int, seconds: float, min_calls: int = 10) -
     return {
         "value": round(tf, 1), "us_per_call": round(t_attn * 1e6, 1), "calls": K,
         "us_per_step_with_cache_write": round(t_step * 1e6, 1),
-        "tokens_per_s": round(T / t_step, 1), "dtype": "%s in, f32 accumulate" % dt,
+        "us_per_step_fused": round(t_fused * 1e6, 1),
+        "tokens_per_s": round(T / t_fused, 1),
+        "tokens_per_s_two_step": round(T / t_step, 1), "dtype": "%s in, f32 accumulate" % dt,
+        "step_note": "us_per_step_with_cache_write: reshape_and_cache then paged_attention_prefill; "
+                     "us_per_step_fused: paged_attention_prefill_write (the cache write in the "
+                     "attention kernel); tokens_per_s from the fused step",
         "config": {"workload": "prefill: %d prompts, lengths %d..%d (sum %d), 40 heads x 128, "
                                "B=16, %s" % (S, int(ctx.min()), int(ctx.max()), T,
                                              {"f16": "fp16", "bf16": "bf16"}[dt]),

@@ -274,6 +274,32 @@ pkv_status pkv_paged_attention_prefill(void* out, const void* q, const void* k_c
                                        int max_query_len, int num_query_tokens, pkv_dtype dtype,
                                        cudaStream_t stream);
 
+/*
+ * The prompt phase with the prompts' cache write done by the same kernel,
+ * for whole prompts (every sequence's qlen == context_lens[s]; a sequence
+ * that is not is skipped and sets PKV_DEVERR_BAD_CONTEXT).  k, v:
+ * [num_query_tokens][num_heads][head_dim], device, the prompt tokens' K and V
+ * in the rows of q.  Computes out as pkv_paged_attention_prefill does, reading
+ * the keys and values from k and v rather than from the cache, and writes
+ * every prompt token's K and V into the cache at its position (slot
+ * block_tables[s][t / B] * B + t mod B for position t: what
+ * pkv_reshape_and_cache would write; other slots are left untouched).  One
+ * launch instead of the cache write followed by the attention: the stores
+ * run beside the tensor-core work (the wywy.jp notes' prompt phase, the block
+ * manager's slot rule of the ricepunchb garden, section 3.2).  Other arguments
+ * and rules as pkv_paged_attention_prefill; q, k, v 16-byte aligned.
+ */
+pkv_status pkv_paged_attention_prefill_write(void* out, const void* q, const void* k,
+                                             const void* v, void* k_cache, void* v_cache,
+                                             const int32_t* block_tables,
+                                             const int32_t* context_lens,
+                                             const int32_t* query_start, float scale,
+                                             int num_seqs, int num_heads, int head_dim,
+                                             int block_size, int max_blocks_per_seq,
+                                             int64_t num_blocks, int max_query_len,
+                                             int num_query_tokens, pkv_dtype dtype,
+                                             cudaStream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Cache maintenance                                                         */
 /* ------------------------------------------------------------------------ */

@@ -8,12 +8,12 @@ from .pagedkv import (BlockManager, OutOfBlocks, PagedKVError, alloc_workspace, 
                       contiguous_attention_decode, contiguous_workspace_size,
                       decode_shared_workspace_size, decode_workspace_size, get_device_error, lib, paged_attention_decode,
                       paged_attention_decode_noalloc, paged_attention_decode_shared,
-                      paged_attention_prefill,
+                      paged_attention_prefill, paged_attention_prefill_write,
                       reshape_and_cache, set_decode_wait_limit, swap_blocks, version)
 
 __all__ = ["BlockManager", "OutOfBlocks", "PagedKVError", "alloc_workspace", "copy_blocks",
            "contiguous_attention_decode", "contiguous_workspace_size",
            "decode_shared_workspace_size", "decode_workspace_size", "get_device_error", "lib", "paged_attention_decode",
            "paged_attention_decode_noalloc", "paged_attention_decode_shared",
-           "paged_attention_prefill",
+           "paged_attention_prefill", "paged_attention_prefill_write",
            "reshape_and_cache", "set_decode_wait_limit", "swap_blocks", "version"]

@@ -57,6 +57,10 @@ constexpr int kRows = 2 * kBM;      // query rows per work item (tiles A and B)
 constexpr int kBN = 128;            // keys per K/V tile (MMA N of S, K of P V)
 constexpr int kWarps = 11;          // K producer, MMA issuer, 2 x 4 softmax warps, V producer
 constexpr int kThreads = kWarps * 32;
+// With the prompt's K/V read from the input tensors (FUSED), a twelfth warp
+// writes them into the paged cache.
+constexpr int kWriterWarp = kWarps;
+__host__ __device__ constexpr int threads_for(bool fused) { return (kWarps + (fused ? 1 : 0)) * 32; }
 constexpr uint32_t kTmemCols = 512;
 // tensor-memory columns: S_X (and P_X over it) at X kBN, O_X at kColO + X D;
 // P_X: keys 32 q .. + 31 packed in pairs in the columns 32 q .. + 15 of S_X,
@@ -82,7 +86,7 @@ struct PCfg {
     // dynamic shared memory: 1 KiB of alignment slack, the buffers, 256 B of
     // barriers; never below 116 KiB so that one CTA holds an SM (each CTA
     // allocates 512 tensor-memory columns, the SM's whole tensor memory)
-    static constexpr size_t SMEM_NEED = 1024 + (size_t)BAR_OFF + 256;
+    static constexpr size_t SMEM_NEED = 1024 + (size_t)BAR_OFF + 512;
     static constexpr size_t SMEM = SMEM_NEED < (116u << 10) ? (116u << 10) : SMEM_NEED;
     static_assert(SMEM <= 232448, "shared memory");
     static_assert(kColO + 2 * D <= kTmemCols, "tensor memory columns");
@@ -179,6 +183,24 @@ __device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap* map, int
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
         : "memory");
 }
+
+// 2-D tiled bulk tensor copy shared -> global (the map's swizzle applies to
+// the shared-memory side), in this thread's bulk async-group.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y, uint32_t src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// wait until the shared memory read by this thread's committed bulk stores
+// may be reused / until those stores have completed
+__device__ __forceinline__ void bulk_wait_read0() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Shared-memory matrix descriptor: start address, leading and stride byte
 // offsets (16-byte units), the fixed version bit 46, 128-byte swizzle.
@@ -396,6 +418,8 @@ struct Pk<__nv_bfloat16> {
 
 struct PrefillArgs {
     void* out;
+    void* k_cache;               // (FUSED: the cache writer's plain stores)
+    void* v_cache;
     int out_v8;                  // out is 32-byte aligned: 32-byte stores
     const int32_t* block_tables;
     const int32_t* context_lens;
@@ -419,7 +443,9 @@ enum : int {
     kBarPFull = 20,   // + group: P_X written, O_X rescaled
     kBarPvDone = 22,  // + group: an item's last O_X += P_X V completed
     kBarMmaDone = 24,
-    kBarCount = 25
+    kBarKStored = 25, // + stage: the cache writer is done with a K stage (FUSED)
+    kBarVStored = 29, // + stage: ... with a V stage
+    kBarCount = 33
 };
 
 // One work item: 256 query rows (tiles A and B) of one (sequence, head).
@@ -435,7 +461,8 @@ struct Item {
 // item (past the sequence's query rows) or a sequence whose lengths are out
 // of range (flagged once).
 constexpr int kGroupPairs = 16;
-__device__ __forceinline__ bool item_at(const PrefillArgs& a, int64_t w, bool flag, Item& it) {
+__device__ __forceinline__ bool item_at(const PrefillArgs& a, int64_t w, bool flag, Item& it,
+                                        bool whole = false) {
     const int64_t sh = (int64_t)a.S * a.H;
     const int64_t per_group = (int64_t)a.q_items * kGroupPairs;
     const int64_t grp = w / per_group;
@@ -450,7 +477,7 @@ __device__ __forceinline__ bool item_at(const PrefillArgs& a, int64_t w, bool fl
     it.qlen = a.query_start[it.s + 1] - it.q0;
     it.ctx = a.context_lens[it.s];
     if (it.ctx < 0 || it.ctx > a.max_blocks * a.B || it.qlen < 0 || it.qlen > it.ctx ||
-        it.q0 < 0 || (int64_t)it.q0 + it.qlen > a.num_tokens) {
+        it.q0 < 0 || (int64_t)it.q0 + it.qlen > a.num_tokens || (whole && it.qlen != it.ctx)) {
         if (flag && t == 0 && it.h == 0) atomicOr(a.err, PKV_DEVERR_BAD_CONTEXT);
         return false;
     }
@@ -468,11 +495,13 @@ __device__ __forceinline__ bool item_at(const PrefillArgs& a, int64_t w, bool fl
     return true;
 }
 
-template <typename T, int D>
-__global__ void __launch_bounds__(kThreads, 1)
+template <typename T, int D, bool FUSED>
+__global__ void __launch_bounds__(threads_for(FUSED), 1)
     paged_prefill_tc(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_v, const PrefillArgs a) {
+                     const __grid_constant__ CUtensorMap tm_v,
+                     const __grid_constant__ CUtensorMap tm_kin,
+                     const __grid_constant__ CUtensorMap tm_vin, const PrefillArgs a) {
     constexpr bool kSplit = Pk<T>::kSplit;
     using C = PCfg<D, kSplit>;
     constexpr int NST = C::NST;
@@ -522,14 +551,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             const bool kq = warp == 0;
             const CUtensorMap* map = kq ? &tm_k : &tm_v;
+            const CUtensorMap* in_map = kq ? &tm_kin : &tm_vin;
             const uint32_t ring = kq ? sK : sV;
             const int full0 = kq ? kBarKFull : kBarVFull, empty0 = kq ? kBarKEmpty : kBarVEmpty;
+            const int stored0 = kq ? kBarKStored : kBarVStored;
             int64_t g = 0;
             int items = 0;
             bool ok = true;
             for (int64_t w = w0; ok && w < n_items; w += dw) {
                 Item it;
-                if (!item_at(a, w, false, it)) continue;
+                if (!item_at(a, w, false, it, FUSED)) continue;
                 if (kq) {
                     // both query tiles, once the previous item's S products are done
                     if (items > 0 && !mbar_wait(bar(kBarQEmpty), (items - 1) & 1, abort_flag)) {
@@ -550,6 +581,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                         !mbar_wait(bar(empty0 + st), (uint32_t)((g / NST - 1) & 1), abort_flag)) {
                         ok = false;
                         break;
+                    }
+                    if constexpr (FUSED) {
+                        // the prompt's keys straight from the input tensor: 128
+                        // token rows per box (rows past the prompt are masked,
+                        // V's zeroed); the stage is free once the cache writer
+                        // is done with its previous tile too
+                        if (g >= NST && !mbar_wait(bar(stored0 + st), (uint32_t)((g / NST - 1) & 1),
+                                                   abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_expect_tx(bar(full0 + st), (uint32_t)(kBN * 128 * C::SLABS));
+                        for (int sl = 0; sl < C::SLABS; ++sl)
+                            tma_3d(ring + st * C::KV_BYTES + sl * C::SLAB_KV, in_map, sl * 64, it.h,
+                                   it.q0 + j * kBN, bar(full0 + st));
+                        continue;
                     }
                     const int tok0 = j * kBN;
                     const int tok1 = min(tok0 + kBN, it.ctx);  // tokens of the tile in the context
@@ -576,6 +623,96 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int64_t t = g - NST < 0 ? 0 : g - NST; t < g; ++t)
                     mbar_wait(bar(full0 + (int)(t % NST)), (uint32_t)((t / NST) & 1), nullptr);
             }
+        }
+    } else if (FUSED && warp == kWriterWarp) {
+        // ====================================================== cache writer
+        // Walks the same key tiles as the producers and observes every K and
+        // V stage as it fills (so it never falls two phases behind a
+        // barrier); for a diagonal tile (the last key tile of a query tile,
+        // which no other item owns) it writes the tile's tokens into the
+        // cache: whole blocks by tiled bulk stores from the swizzled stage,
+        // the tokens of a partial last block by plain stores; then it hands
+        // the stage back (the producers wait for that as well as for the MMAs).
+        bool ok = true;
+        int64_t g = 0;
+        unsigned char* kc = static_cast<unsigned char*>(a.k_cache);
+        unsigned char* vc = static_cast<unsigned char*>(a.v_cache);
+        for (int64_t w = w0; ok && w < n_items; w += dw) {
+            Item it;
+            if (!item_at(a, w, false, it, FUSED)) continue;
+            const int32_t* row_tab = a.block_tables + (int64_t)it.s * a.max_blocks;
+            for (int j = 0; j < it.n_kv; ++j, ++g) {
+                const int st = (int)(g % NST);
+                const uint32_t par = (uint32_t)((g / NST) & 1);
+                int got = 1;
+                if (lane == 0)
+                    got = mbar_wait(bar(kBarKFull + st), par, abort_flag) &&
+                          mbar_wait(bar(kBarVFull + st), par, abort_flag);
+                got = __shfl_sync(0xffffffffu, got, 0);
+                if (!got) {
+                    ok = false;
+                    break;
+                }
+                const bool diag = j == it.n[0] - 1 || (it.n[1] > 0 && j == it.n[1] - 1);
+                if (diag) {
+                    const int tok0 = j * kBN, tok1 = min(tok0 + kBN, it.ctx);
+                    const int jb0 = tok0 / a.B, jbf = tok1 / a.B;   // whole blocks [jb0, jbf)
+                    const uint32_t ks = sK + st * C::KV_BYTES, vs = sV + st * C::KV_BYTES;
+                    if (lane == 0) {
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                        for (int jb = jb0; jb < jbf; ++jb) {
+                            const int64_t phys = row_tab[jb];
+                            if (phys < 0 || phys >= a.num_blocks) {
+                                atomicOr(a.err, PKV_DEVERR_BAD_BLOCK);
+                                continue;
+                            }
+                            const int y = (int)((phys * a.H + it.h) * a.B);
+                            const uint32_t off = (uint32_t)(jb * a.B - tok0) * 128u;
+                            for (int sl = 0; sl < C::SLABS; ++sl) {
+                                tma_store_2d(&tm_k, sl * 64, y, ks + sl * C::SLAB_KV + off);
+                                tma_store_2d(&tm_v, sl * 64, y, vs + sl * C::SLAB_KV + off);
+                            }
+                        }
+                        bulk_commit();
+                    }
+                    const int rem = tok1 - jbf * a.B;        // tokens of a partial last block
+                    if (rem > 0) {
+                        const int64_t phys = row_tab[jbf];
+                        if (phys >= 0 && phys < a.num_blocks) {
+                            const int r0 = jbf * a.B - tok0;  // its first row in the stage
+                            const int64_t dst0 = ((phys * a.H + it.h) * a.B) * (int64_t)D * 2;
+                            for (int i = lane; i < rem * C::SLABS * 8; i += 32) {
+                                const int r = i / (C::SLABS * 8), c = i - r * (C::SLABS * 8);
+                                const int sl = c >> 3, ch = c & 7, sr = r0 + r;
+                                const uint32_t so = (uint32_t)(sl * C::SLAB_KV + sr * 128 +
+                                                               ((ch ^ (sr & 7)) << 4));
+                                const int64_t go = dst0 + ((int64_t)r * D + sl * 64 + ch * 8) * 2;
+                                uint4 kv4, vv4;
+                                asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                             : "=r"(kv4.x), "=r"(kv4.y), "=r"(kv4.z), "=r"(kv4.w)
+                                             : "r"(ks + so));
+                                asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                             : "=r"(vv4.x), "=r"(vv4.y), "=r"(vv4.z), "=r"(vv4.w)
+                                             : "r"(vs + so));
+                                *reinterpret_cast<uint4*>(kc + go) = kv4;
+                                *reinterpret_cast<uint4*>(vc + go) = vv4;
+                            }
+                        } else if (lane == 0) {
+                            atomicOr(a.err, PKV_DEVERR_BAD_BLOCK);
+                        }
+                    }
+                    if (lane == 0) bulk_wait_read0();
+                    __syncwarp();
+                }
+                if (lane == 0) {
+                    mbar_arrive(bar(kBarKStored + st));
+                    mbar_arrive(bar(kBarVStored + st));
+                }
+            }
+        }
+        if (lane == 0) {
+            if (!ok) fail();
+            bulk_wait0();                   // every store complete before the CTA ends
         }
     } else if (warp == 1) {
         // ======================================================= MMA issuer
@@ -608,7 +745,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int64_t g = 0;
             for (int64_t w = w0; ok && w < n_items; w += dw) {
                 Item it;
-                if (!item_at(a, w, true, it)) continue;
+                if (!item_at(a, w, true, it, FUSED)) continue;
                 // the last group whose S reads a key tile (B, unless B has no rows)
                 const int xl = it.n[1] > 0 ? 1 : 0;
                 if (!mbar_wait(bar(kBarQFull), (uint32_t)(items & 1), abort_flag)) {
@@ -706,7 +843,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int items = 0;
         for (int64_t w = w0; ok && w < n_items; w += dw) {
             Item it;
-            if (!item_at(a, w, false, it)) continue;
+            if (!item_at(a, w, false, it, FUSED)) continue;
             const int nx = x ? it.n[1] : it.n[0];
             const int pos0 = x ? it.pos0[1] : it.pos0[0];
             const int rows = x ? it.rows[1] : it.rows[0];
@@ -921,11 +1058,12 @@ bool make_map(CUtensorMap* m, bool bf16, uint32_t rank, const void* gaddr, const
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename T, int D>
+template <typename T, int D, bool FUSED>
 cudaError_t launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           const CUtensorMap& tkin, const CUtensorMap& tvin,
                            const PrefillArgs& a, cudaStream_t stream) {
     const size_t smem = PCfg<D, Pk<T>::kSplit>::SMEM;
-    cudaError_t e = cudaFuncSetAttribute(paged_prefill_tc<T, D>,
+    cudaError_t e = cudaFuncSetAttribute(paged_prefill_tc<T, D, FUSED>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     // Clusters of two CTAs, so that CTAs 2k and 2k + 1, which take
@@ -948,7 +1086,7 @@ cudaError_t launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const C
     const int sms = pkv::sm_count(dev);
     if (sms < 1) return cudaErrorInvalidDevice;
     cfg.gridDim = dim3((unsigned)(items < sms ? items : sms));
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(threads_for(FUSED));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -960,13 +1098,13 @@ cudaError_t launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const C
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    e = cudaLaunchKernelEx(&cfg, paged_prefill_tc<T, D>, tq, tk, tv, a);
+    e = cudaLaunchKernelEx(&cfg, paged_prefill_tc<T, D, FUSED>, tq, tk, tv, tkin, tvin, a);
     if (e == cudaErrorInvalidClusterSize && cfg.numAttrs == 1) {
         // the device refused the pairing: the same kernel, CTAs placed one
         // by one
         cudaGetLastError();
         cfg.numAttrs = 0;
-        e = cudaLaunchKernelEx(&cfg, paged_prefill_tc<T, D>, tq, tk, tv, a);
+        e = cudaLaunchKernelEx(&cfg, paged_prefill_tc<T, D, FUSED>, tq, tk, tv, tkin, tvin, a);
     }
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
@@ -976,16 +1114,16 @@ bool aligned(const void* p, uintptr_t al) { return (reinterpret_cast<uintptr_t>(
 
 }  // namespace
 
-extern "C" {
+namespace {
 
-pkv_status pkv_paged_attention_prefill(void* out, const void* q, const void* k_cache,
-                                       const void* v_cache, const int32_t* block_tables,
-                                       const int32_t* context_lens, const int32_t* query_start,
-                                       float scale, int num_seqs, int num_heads, int head_dim,
-                                       int block_size, int max_blocks_per_seq, int64_t num_blocks,
-                                       int max_query_len, int num_query_tokens, pkv_dtype dtype,
-                                       cudaStream_t stream) {
-    const char* fn = "pkv_paged_attention_prefill";
+pkv_status prefill_common(const char* fn, void* out, const void* q, const void* k_in,
+                          const void* v_in, void* k_cache, void* v_cache,
+                          const int32_t* block_tables, const int32_t* context_lens,
+                          const int32_t* query_start, float scale, int num_seqs, int num_heads,
+                          int head_dim, int block_size, int max_blocks_per_seq,
+                          int64_t num_blocks, int max_query_len, int num_query_tokens,
+                          pkv_dtype dtype, cudaStream_t stream) {
+    const bool fused = k_in != nullptr || v_in != nullptr;
     if (num_seqs < 0 || num_seqs > 65535)
         return pkv::fail(PKV_ERR_INVALID, "%s: num_seqs must be in [0, 65535]", fn);
     if (num_heads < 1 || num_heads > 65535)
@@ -1005,23 +1143,35 @@ pkv_status pkv_paged_attention_prefill(void* out, const void* q, const void* k_c
     if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f)
         return pkv::fail(PKV_ERR_INVALID, "%s: scale is not finite", fn);
     if (num_seqs == 0 || max_query_len == 0 || num_query_tokens == 0) return PKV_OK;
-    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !query_start)
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !query_start ||
+        (fused && (!k_in || !v_in)))
         return pkv::fail(PKV_ERR_INVALID, "%s: NULL pointer", fn);
-    if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
-        return pkv::fail(PKV_ERR_INVALID, "%s: out, q and the caches must be 16-byte aligned", fn);
+    if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        (fused && (!aligned(k_in, 16) || !aligned(v_in, 16))))
+        return pkv::fail(PKV_ERR_INVALID, "%s: out, q, k, v and the caches must be 16-byte aligned",
+                         fn);
     int32_t* err = pkv::device_error_word();
     if (!err) return pkv::fail(PKV_ERR_CUDA, "%s: no CUDA device", fn);
 
     const bool bf16 = dtype == PKV_BF16;
     const cuuint64_t D = (cuuint64_t)head_dim;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, tkin, tvin;
     {
-        // q: [tokens][heads][D], one box = 128 tokens x 64 elements of one head
+        // q (and the prompt's k, v): [tokens][heads][D], one box = 128 tokens
+        // x 64 elements of one head
         const cuuint64_t dims[3] = {D, (cuuint64_t)num_heads, (cuuint64_t)num_query_tokens};
         const cuuint64_t strides[2] = {D * 2, (cuuint64_t)num_heads * D * 2};
         const cuuint32_t box[3] = {64, 1, (cuuint32_t)kBM};
         if (!make_map(&tq, bf16, 3, q, dims, strides, box))
             return pkv::fail(PKV_ERR_CUDA, "%s: tensor map of q", fn);
+        if (fused) {
+            if (!make_map(&tkin, bf16, 3, k_in, dims, strides, box) ||
+                !make_map(&tvin, bf16, 3, v_in, dims, strides, box))
+                return pkv::fail(PKV_ERR_CUDA, "%s: tensor maps of k and v", fn);
+        } else {
+            tkin = tq;                       // unused
+            tvin = tq;
+        }
     }
     {
         // caches: rows (block, head, token) of D elements, one box = one block's
@@ -1035,6 +1185,8 @@ pkv_status pkv_paged_attention_prefill(void* out, const void* q, const void* k_c
     }
     PrefillArgs a;
     a.out = out;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
     a.out_v8 = aligned(out, 32) ? 1 : 0;
     a.block_tables = block_tables;
     a.context_lens = context_lens;
@@ -1050,14 +1202,63 @@ pkv_status pkv_paged_attention_prefill(void* out, const void* q, const void* k_c
     a.num_blocks = num_blocks;
     a.err = err;
     cudaError_t e;
-    if (!bf16)
-        e = head_dim == 128 ? launch_prefill<__half, 128>(tq, tk, tv, a, stream)
-                            : launch_prefill<__half, 64>(tq, tk, tv, a, stream);
-    else
-        e = head_dim == 128 ? launch_prefill<__nv_bfloat16, 128>(tq, tk, tv, a, stream)
-                            : launch_prefill<__nv_bfloat16, 64>(tq, tk, tv, a, stream);
+    if (fused) {
+        if (!bf16)
+            e = head_dim == 128
+                    ? launch_prefill<__half, 128, true>(tq, tk, tv, tkin, tvin, a, stream)
+                    : launch_prefill<__half, 64, true>(tq, tk, tv, tkin, tvin, a, stream);
+        else
+            e = head_dim == 128
+                    ? launch_prefill<__nv_bfloat16, 128, true>(tq, tk, tv, tkin, tvin, a, stream)
+                    : launch_prefill<__nv_bfloat16, 64, true>(tq, tk, tv, tkin, tvin, a, stream);
+    } else {
+        if (!bf16)
+            e = head_dim == 128
+                    ? launch_prefill<__half, 128, false>(tq, tk, tv, tkin, tvin, a, stream)
+                    : launch_prefill<__half, 64, false>(tq, tk, tv, tkin, tvin, a, stream);
+        else
+            e = head_dim == 128
+                    ? launch_prefill<__nv_bfloat16, 128, false>(tq, tk, tv, tkin, tvin, a, stream)
+                    : launch_prefill<__nv_bfloat16, 64, false>(tq, tk, tv, tkin, tvin, a, stream);
+    }
     if (e != cudaSuccess) return pkv::cuda_fail(e, fn);
     return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_paged_attention_prefill(void* out, const void* q, const void* k_cache,
+                                       const void* v_cache, const int32_t* block_tables,
+                                       const int32_t* context_lens, const int32_t* query_start,
+                                       float scale, int num_seqs, int num_heads, int head_dim,
+                                       int block_size, int max_blocks_per_seq, int64_t num_blocks,
+                                       int max_query_len, int num_query_tokens, pkv_dtype dtype,
+                                       cudaStream_t stream) {
+    return prefill_common("pkv_paged_attention_prefill", out, q, nullptr, nullptr,
+                          const_cast<void*>(k_cache), const_cast<void*>(v_cache), block_tables,
+                          context_lens, query_start, scale, num_seqs, num_heads, head_dim,
+                          block_size, max_blocks_per_seq, num_blocks, max_query_len,
+                          num_query_tokens, dtype, stream);
+}
+
+pkv_status pkv_paged_attention_prefill_write(void* out, const void* q, const void* k,
+                                             const void* v, void* k_cache, void* v_cache,
+                                             const int32_t* block_tables,
+                                             const int32_t* context_lens,
+                                             const int32_t* query_start, float scale,
+                                             int num_seqs, int num_heads, int head_dim,
+                                             int block_size, int max_blocks_per_seq,
+                                             int64_t num_blocks, int max_query_len,
+                                             int num_query_tokens, pkv_dtype dtype,
+                                             cudaStream_t stream) {
+    const char* fn = "pkv_paged_attention_prefill_write";
+    if (!k || !v) return pkv::fail(PKV_ERR_INVALID, "%s: NULL pointer", fn);
+    return prefill_common(fn, out, q, k, v, k_cache, v_cache, block_tables, context_lens,
+                          query_start, scale, num_seqs, num_heads, head_dim, block_size,
+                          max_blocks_per_seq, num_blocks, max_query_len, num_query_tokens, dtype,
+                          stream);
 }
 
 }  // extern "C"

@@ -69,6 +69,8 @@ def lib():
                                                     i32, i64, i32, i32, P], i32),
             "pkv_paged_attention_prefill": ([P, P, P, P, P, P, P, f32, i32, i32, i32, i32,
                                              i32, i64, i32, i32, i32, P], i32),
+            "pkv_paged_attention_prefill_write": ([P, P, P, P, P, P, P, P, P, f32, i32, i32, i32,
+                                                   i32, i32, i64, i32, i32, i32, P], i32),
             "pkv_reshape_and_cache": ([P, P, P, P, P, i32, i32, i32, i32, i64, i32, P], i32),
             "pkv_copy_blocks": ([P, P, P, i32, i32, i32, i32, i64, i32, P], i32),
             "pkv_swap_blocks": ([P, P, P, P, P, i32, i32, i32, i32, i64, i64, i32, P], i32),
@@ -293,6 +295,36 @@ def paged_attention_prefill(out, q, k_cache, v_cache, block_tables, context_lens
            lib().pkv_paged_attention_prefill(
                _dev(out, "out"), _dev(q, "q"), _dev(k_cache, "k_cache"),
                _dev(v_cache, "v_cache"), _dev(block_tables, "block_tables", torch.int32),
+               _dev(context_lens, "context_lens", torch.int32, 1),
+               _dev(query_start, "query_start", torch.int32, 1), float(scale), S, H, D, B,
+               block_tables.shape[1], nb, int(max_query_len), T, _dtype_code(q.dtype),
+               _stream(stream)))
+    return out
+
+
+def paged_attention_prefill_write(out, q, k, v, k_cache, v_cache, block_tables, context_lens,
+                                  query_start, scale, max_query_len, stream=None):
+    """Whole prompts: writes every prompt token's K and V (rows of k, v) into the
+    cache at its position and computes the causal attention of the prompts,
+    reading K and V from k and v, in one kernel."""
+    torch = _torch()
+    T, H, D = q.shape
+    nb, H2, B, D2 = k_cache.shape
+    S = context_lens.shape[0]
+    if (H2, D2) != (H, D) or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("q / cache shape mismatch")
+    if tuple(k.shape) != (T, H, D) or tuple(v.shape) != (T, H, D):
+        raise ValueError("k and v must be [num_query_tokens, num_heads, head_dim]")
+    if tuple(out.shape) != (T, H, D) or len({out.dtype, q.dtype, k.dtype, v.dtype,
+                                             k_cache.dtype, v_cache.dtype}) != 1:
+        raise ValueError("out/q/k/v/cache dtype or shape mismatch")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or query_start.shape != (S + 1,):
+        raise ValueError("block_tables [S, max_blocks], query_start [S+1] expected")
+    _check("pkv_paged_attention_prefill_write",
+           lib().pkv_paged_attention_prefill_write(
+               _dev(out, "out"), _dev(q, "q"), _dev(k, "k"), _dev(v, "v"),
+               _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+               _dev(block_tables, "block_tables", torch.int32),
                _dev(context_lens, "context_lens", torch.int32, 1),
                _dev(query_start, "query_start", torch.int32, 1), float(scale), S, H, D, B,
                block_tables.shape[1], nb, int(max_query_len), T, _dtype_code(q.dtype),
