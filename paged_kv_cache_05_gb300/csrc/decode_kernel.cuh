@@ -679,25 +679,28 @@ __global__ void __launch_bounds__(kGroupPassThreads) paged_decode_groups(const D
     }
     __syncthreads();
     // the first entry that differs: tps threads per sequence, each taking
-    // every tps-th entry, four entries' loads issued together
+    // every tps-th entry, sixteen entries' loads issued together
     {
+        constexpr int kBatch = 16;
         const int tps = S < nt ? nt / S : 1;
         const int r = tid % tps;
         for (int s = 1 + tid / tps; s < S; s += nt / tps) {
             const int n = nf[s];
             const int32_t* r0 = a.block_tables + (int64_t)s * a.max_blocks;
             const int32_t* r1 = r0 - a.max_blocks;
-            for (int j0 = r; j0 < n; j0 += 4 * tps) {
-                int32_t x[4], y[4];
+            for (int j0 = r; j0 < n; j0 += kBatch * tps) {
+                int32_t x[kBatch], y[kBatch];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
+                for (int k = 0; k < kBatch; ++k) {
                     const int j = j0 + k * tps;
                     x[k] = j < n ? __ldg(r0 + j) : 0;
                     y[k] = j < n ? __ldg(r1 + j) : 0;
                 }
+                int fm = n;
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    if (x[k] != y[k]) atomicMin(&first[s], j0 + k * tps);
+                for (int k = kBatch - 1; k >= 0; --k)
+                    if (x[k] != y[k]) fm = j0 + k * tps;
+                if (fm < n) atomicMin(&first[s], fm);
             }
         }
     }
@@ -758,14 +761,24 @@ __global__ void __launch_bounds__(kGroupPassThreads) paged_decode_groups(const D
     }
     // the units, this CTA's share: (leader, head, part); a prefix of P steps
     // in nc parts, the first P mod nc of them one step longer
-    for (int u = blockIdx.x * nt + tid; u < U; u += gridDim.x * nt) {
-        int lo = 0, hi = S - 1;                  // the leader: largest s with ub[s] <= u
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (ub[mid] <= u) lo = mid;
-            else hi = mid - 1;
+    for (int u0 = blockIdx.x * nt + (tid & ~31); u0 < U; u0 += gridDim.x * nt) {
+        // the leader of the warp's first unit by one search (lane 0), then
+        // each lane steps forward to its own (a leader owns H * nc >= H units)
+        const int lane = tid & 31, u = u0 + lane;
+        int L = 0;
+        if (lane == 0) {
+            int lo = 0, hi = S - 1;              // largest s with ub[s] <= u0
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (ub[mid] <= u0) lo = mid;
+                else hi = mid - 1;
+            }
+            L = lo;
         }
-        const int L = lo, P = gP[L], nc = (P + LG - 1) / LG;
+        L = __shfl_sync(kFull, L, 0);
+        if (u >= U) continue;
+        while (ub[L + 1] <= u) ++L;
+        const int P = gP[L], nc = (P + LG - 1) / LG;
         const int r = u - ub[L], h = r / nc, c = r - h * nc;
         const int q = P / nc, rem = P - q * nc;
         GroupUnit x;
