@@ -617,12 +617,12 @@ __global__ void __launch_bounds__(threads_for(FUSED), 1)
                 }
             }
             if (!ok) fail();
-            if (*abort_flag) {
-                // let the copies in flight land before the CTA can exit
-                if (kq && items > 0) mbar_wait(bar(kBarQFull), (items - 1) & 1, nullptr);
-                for (int64_t t = g - NST < 0 ? 0 : g - NST; t < g; ++t)
-                    mbar_wait(bar(full0 + (int)(t % NST)), (uint32_t)((t / NST) & 1), nullptr);
-            }
+            // let the latest copy into every stage (and the last query tiles)
+            // land before the CTA can exit, whatever the other roles did (on a
+            // normal run these have long landed)
+            if (kq && items > 0) mbar_wait(bar(kBarQFull), (items - 1) & 1, nullptr);
+            for (int64_t t = g - NST < 0 ? 0 : g - NST; t < g; ++t)
+                mbar_wait(bar(full0 + (int)(t % NST)), (uint32_t)((t / NST) & 1), nullptr);
         }
     } else if (FUSED && warp == kWriterWarp) {
         // ====================================================== cache writer
