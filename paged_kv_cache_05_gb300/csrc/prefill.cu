@@ -743,9 +743,22 @@ __global__ void __launch_bounds__(threads_for(FUSED), 1)
             };
             bool ok = true;
             int64_t g = 0;
-            for (int64_t w = w0; ok && w < n_items; w += dw) {
-                Item it;
-                if (!item_at(a, w, true, it, FUSED)) continue;
+            // The next item is looked up while the current one runs: its
+            // lengths are global loads whose latency would otherwise fall
+            // between two items, when nothing is queued on the tensor pipe.
+            int64_t wn = w0;
+            auto next_item = [&](Item& nit) -> bool {
+                for (; wn < n_items; wn += dw)
+                    if (item_at(a, wn, true, nit, FUSED)) {
+                        wn += dw;
+                        return true;
+                    }
+                return false;
+            };
+            Item nit;
+            bool have = next_item(nit);
+            while (ok && have) {
+                const Item it = nit;
                 // the last group whose S reads a key tile (B, unless B has no rows)
                 const int xl = it.n[1] > 0 ? 1 : 0;
                 if (!mbar_wait(bar(kBarQFull), (uint32_t)(items & 1), abort_flag)) {
@@ -766,6 +779,7 @@ __global__ void __launch_bounds__(threads_for(FUSED), 1)
                     umma_commit(bar(kBarKEmpty + st));
                     if (it.n_kv == 1) umma_commit(bar(kBarQEmpty));
                 }
+                have = next_item(nit);
                 for (int j = 0; ok && j < it.n_kv; ++j, ++g) {
                     const int st = (int)(g % NST);
                     if (!mbar_wait(bar(kBarVFull + st), (uint32_t)((g / NST) & 1), abort_flag)) {
@@ -795,6 +809,9 @@ __global__ void __launch_bounds__(threads_for(FUSED), 1)
                         }
                         ++gpx[x];
                         if (j == it.n[x] - 1) umma_commit(bar(kBarPvDone + x));
+                        // V_j's stage is free once its last P V (B's, or A's
+                        // where B has no tile j) completes, before the next S
+                        if (x == 1 || j >= it.n[1]) umma_commit(bar(kBarVEmpty + st));
                         // then S_X of the next key tile over P_X (in issue order)
                         if (j + 1 < it.n[x]) {
                             if (!k_next) {
@@ -815,7 +832,6 @@ __global__ void __launch_bounds__(threads_for(FUSED), 1)
                         }
                     }
                     if (!ok) break;
-                    umma_commit(bar(kBarVEmpty + st));
                 }
                 ++items;
             }
@@ -863,18 +879,22 @@ __global__ void __launch_bounds__(threads_for(FUSED), 1)
                 tc_fence_after();
                 const int kb = j * kBN;
                 const bool full = kb + kBN - 1 <= pos0;   // every key visible to every row
-                // row max of the masked, scaled scores (two halves of 64 keys,
-                // both loads issued before one wait: bf16 2% faster, fp16 the same)
+                // Row max of the visible scaled scores.  A full tile: both
+                // 64-column halves loaded before one wait, two max chains per
+                // half.  A tile crossing the diagonal runs once per query tile,
+                // so its code is kept small (it would otherwise miss in the
+                // instruction cache every time): a rolled loop over the 32-key
+                // quarters, skipping those no row of the warp sees.
                 float mx = -INFINITY;
-                uint32_t rr[2][64];
-                tmem_ld64_nw(tS, rr[0]);
-                tmem_ld64_nw(tS + 64u, rr[1]);
-                tmem_wait64(rr[0]);
-                tmem_wait64(rr[1]);
+                if (full) {
+                    uint32_t rr[2][64];
+                    tmem_ld64_nw(tS, rr[0]);
+                    tmem_ld64_nw(tS + 64u, rr[1]);
+                    tmem_wait64(rr[0]);
+                    tmem_wait64(rr[1]);
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    uint32_t (&r)[64] = rr[hh];
-                    if (full) {
+                    for (int hh = 0; hh < 2; ++hh) {
+                        uint32_t (&r)[64] = rr[hh];
                         float e0 = pos_scale ? -INFINITY : INFINITY, e1 = e0;
                         if (pos_scale) {
 #pragma unroll
@@ -890,11 +910,24 @@ __global__ void __launch_bounds__(threads_for(FUSED), 1)
                             }
                         }
                         mx = fmaxf(mx, (pos_scale ? fmaxf(e0, e1) : fminf(e0, e1)) * sl2);
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 64; ++e)
-                            if (kb + hh * 64 + e <= qpos) mx = fmaxf(mx, __uint_as_float(r[e]) * sl2);
                     }
+                } else {
+                    float e0 = -INFINITY, e1 = -INFINITY;
+#pragma unroll 1
+                    for (int q = 0; q < kBN / 32; ++q) {
+                        const int lq = qpos - kb - q * 32;   // last visible key of the quarter
+                        if (__all_sync(0xffffffffu, lq < 0)) continue;
+                        uint32_t r[32];
+                        tmem_ld32(tS + (uint32_t)(q * 32), r);
+#pragma unroll
+                        for (int e = 0; e < 32; e += 4) {
+                            e0 = max3(e0, e <= lq ? __uint_as_float(r[e]) * sl2 : -INFINITY,
+                                      e + 1 <= lq ? __uint_as_float(r[e + 1]) * sl2 : -INFINITY);
+                            e1 = max3(e1, e + 2 <= lq ? __uint_as_float(r[e + 2]) * sl2 : -INFINITY,
+                                      e + 3 <= lq ? __uint_as_float(r[e + 3]) * sl2 : -INFINITY);
+                        }
+                    }
+                    mx = fmaxf(e0, e1);
                 }
                 float m_new = m;
                 if (mx > m + kRescaleLog2 || (m == -INFINITY && mx > -INFINITY)) m_new = mx;
@@ -906,13 +939,22 @@ __global__ void __launch_bounds__(threads_for(FUSED), 1)
                 // quarter's scores, read again here
                 uint64_t rs2 = f2(0.f, 0.f);
                 const uint64_t sc2 = f2(sl2, sl2), nm2 = f2(-m_new, -m_new);
-                // the full-tile loop carries no mask code; the diagonal one
-                // compares each key with the row's last visible key
+                // The full-tile loop carries no mask code and is unrolled; the
+                // diagonal one compares each key with the row's last visible
+                // key, is rolled (small code, as for the max), and writes zero
+                // weights for a quarter no row of the warp sees.
                 auto weights = [&](auto masked) {
                     constexpr bool kMask = decltype(masked)::value;
                     const int lim = qpos - kb;       // last visible key of the tile
+                    auto quarter = [&](const int q) {
+                        if (kMask && __all_sync(0xffffffffu, lim < q * 32)) {
+                            uint32_t z[16];
 #pragma unroll
-                    for (int q = 0; q < kBN / 32; ++q) {
+                            for (int e = 0; e < 16; ++e) z[e] = 0u;
+                            tmem_st16(tS + (uint32_t)(q * 32), z);
+                            if constexpr (kSplit) tmem_st16(tS + (uint32_t)(q * 32 + 16), z);
+                            return;
+                        }
                         uint32_t r[32];
                         tmem_ld32(tS + (uint32_t)(q * 32), r);
                         uint32_t pk[16];
@@ -936,6 +978,13 @@ __global__ void __launch_bounds__(threads_for(FUSED), 1)
                         }
                         tmem_st16(tS + (uint32_t)(q * 32), pk);
                         if constexpr (kSplit) tmem_st16(tS + (uint32_t)(q * 32 + 16), pr);
+                    };
+                    if constexpr (kMask) {
+#pragma unroll 1
+                        for (int q = 0; q < kBN / 32; ++q) quarter(q);
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < kBN / 32; ++q) quarter(q);
                     }
                 };
                 if (full)

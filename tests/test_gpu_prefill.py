@@ -22,13 +22,14 @@ def pkv():
     return m
 
 
-def run_case(pkv, rs, ctx, qlen, H, D, B, dtype):
+def run_case(pkv, rs, ctx, qlen, H, D, B, dtype, scale=None):
     import torch
     case = random_case(rs, len(ctx), H, D, B, ctx, dtype)
     qs = np.concatenate([[0], np.cumsum(qlen)]).astype(np.int32)
     T = int(qs[-1])
     q = words((max(T, 1), H, D), dtype, rs)[:T]
-    scale = float(np.float32(1 / math.sqrt(D)))
+    if scale is None:
+        scale = float(np.float32(1 / math.sqrt(D)))
     ref = prefill_oracle_threaded(q, case["kc"], case["vc"], case["bt"], case["ctx"], qs, scale,
                                   dtype)
     dq = to_dev(q, dtype) if T else torch.empty((0, H, D), dtype=torch.float16, device="cuda")
@@ -54,6 +55,18 @@ def test_prefill_parity(pkv, dtype, D, B):
     ctx = [c for c, _ in pairs]
     qlen = [n for _, n in pairs]
     run_case(pkv, rs, ctx, qlen, 3, D, B, dtype)
+
+
+@pytest.mark.parametrize("scale", [-0.125, 0.0])
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_prefill_negative_and_zero_scale(pkv, scale, dtype):
+    """A negative scale turns the row max into the min of the raw scores, on
+    full tiles and on tiles that cross the diagonal alike; a zero scale gives
+    every visible key the same weight (the mean of V over positions 0..p)."""
+    rs = np.random.default_rng(650 + int(scale < 0) + 2 * (dtype == "bf16"))
+    pairs = [(1, 1), (130, 130), (300, 37), (500, 500), (129, 1)]
+    run_case(pkv, rs, [c for c, _ in pairs], [n for _, n in pairs], 3, 128, 16, dtype,
+             scale=scale)
 
 
 def test_prefill_long_prompt(pkv):
