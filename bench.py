@@ -2,11 +2,14 @@
 """Benchmark of the paged KV-cache decode hot path on one GB300.
 
 One step = one decode layer-step of the whole hot path over a seeded synthetic
-batch: the new token of every sequence is written into its slot
-(reshape_and_cache), copy-on-write pairs are applied (copy_blocks, when the
-workload has any), and paged_attention_decode (+ its split merge) runs over
-every sequence's context.  The block tables and slot mappings come from the
-C++ block manager (set-up, host).
+batch: copy-on-write pairs are applied (copy_blocks, when the workload has
+any), the new token of every sequence is written into its slot and the decode
+attention (+ its split merge) runs over every sequence's context.  By default
+the write is part of the attention call (paged_attention_decode_append: the
+newest token's K/V taken from the step's input and stored into its slot by
+the same kernel); with --step two-call, or for the shared-prefix entry point,
+reshape_and_cache writes it first.  The block tables and slot mappings come
+from the C++ block manager (set-up, host).
 
 Default workload: OPT-13B-shaped decode layer (64 sequences, 40 heads x 128,
 fp16 K/V, block size 16, lognormal context lengths with median 300 clipped to
@@ -149,7 +152,7 @@ class Workload:
     """Device-resident inputs of one workload plus the algorithmic byte counts."""
 
     def __init__(self, name: str, device, partition=None, block_size=None, layers=None,
-                 placement: str = "scattered", decode: str = "auto"):
+                 placement: str = "scattered", decode: str = "auto", step: str = "append"):
         import torch
         import paged_kv_cache_05_gb300 as pkv
         self.pkv = pkv
@@ -251,6 +254,9 @@ class Workload:
         self.shared = decode == "shared" or (decode == "auto" and name == "shared_prefix")
         self.decode_fn = (pkv.paged_attention_decode_shared if self.shared
                           else pkv.paged_attention_decode)
+        # the new token written by the attention call itself (not with the
+        # shared-prefix entry point)
+        self.append = step == "append" and not self.shared
         if self.shared:
             self.ws = torch.empty(pkv.decode_shared_workspace_size(
                 S, H, D, B, self.max_blocks, self.partition), dtype=torch.uint8, device=dev)
@@ -264,7 +270,8 @@ class Workload:
         self.reshape_bytes = 2 * (2 * S * H * D * e)
         self.copy_bytes = len(pairs) * 2 * 2 * H * B * D * e
         self.step_bytes = self.attn_bytes + self.reshape_bytes + self.copy_bytes
-        self.launches_per_step = 3 + (1 if len(pairs) else 0) + (1 if self.shared else 0)
+        self.launches_per_step = ((2 if self.append else 3) + (1 if len(pairs) else 0)
+                                  + (1 if self.shared else 0))
         self.unique_kv_bytes = None
         if name == "shared_prefix":
             blocks = set()
@@ -272,12 +279,17 @@ class Workload:
                 blocks.update(tables[s, :-(-int(ctx[s]) // B)].tolist())
             self.unique_kv_bytes = len(blocks) * H * B * D * 2 * e
 
-    def step(self, i: int):
+    def step(self, i: int, append=None):
         pkv = self.pkv
         layer = i % self.layers
         kc, vc = self.kc[layer], self.vc[layer]
         if len(self.pairs_host):
             pkv.copy_blocks(kc, vc, self.pairs)
+        if self.append if append is None else append:
+            pkv.paged_attention_decode_append(self.out, self.q, self.k_new, self.v_new, kc, vc,
+                                              self.tables, self.ctx, self.scale, self.partition,
+                                              self.ws)
+            return
         pkv.reshape_and_cache(self.k_new, self.v_new, kc, vc, self.slots)
         self.decode_fn(self.out, self.q, kc, vc, self.tables, self.ctx, self.scale,
                        self.partition, self.ws)
@@ -444,6 +456,10 @@ def main():
                     help="decode entry point: plain, shared (groups of sequences sharing "
                          "prefix blocks read them once), auto = shared for the shared-prefix "
                          "workload")
+    ap.add_argument("--step", choices=["append", "two-call"], default="append",
+                    help="how a step writes the new tokens: inside the attention call "
+                         "(paged_attention_decode_append, default) or by reshape_and_cache "
+                         "before it")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--roofline-seconds", type=float, default=0.5,
@@ -489,7 +505,7 @@ def main():
     from paged_kv_cache_05_gb300 import build
     build.build()
     wl = Workload(args.workload, device, args.partition, args.block_size, args.layers,
-                  args.placement, args.decode)
+                  args.placement, args.decode, args.step)
     stream = torch.cuda.current_stream()
 
     K = args.steps
@@ -537,6 +553,19 @@ def main():
     # attention (each call bracketed by its own events, which also breaks the
     # programmatic launch chain, so these calls cannot overlap their neighbours)
     parts = measure_parts(wl, device, args.warmup)
+    if wl.append:
+        # the same step as two calls (reshape_and_cache, then the attention), K steps
+        for i in range(3):
+            wl.step(i, append=False)
+        torch.cuda.synchronize()
+        t_start.record(stream)
+        for i in range(K):
+            wl.step(args.warmup + i, append=False)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        parts["two_call_step_us"] = round(t_start.elapsed_time(t_end) / K * 1e3, 2)
+        parts["two_call_step_note"] = ("the same step with the new tokens written by "
+                                       "reshape_and_cache before the attention call")
 
     # ---- end to end: host (pinned) inputs -> C ABI -> host output, every step
     e2e = api = None
@@ -600,7 +629,7 @@ def main():
                              "launches (2 kernels each) for the roofline" % (
                                  wl.launches_per_step,
                                  "copy_blocks, " * bool(len(wl.pairs_host))
-                                 + "reshape_and_cache, "
+                                 + "reshape_and_cache, " * (not wl.append)
                                  + "paged_decode_groups, " * wl.shared
                                  + "paged_decode_main, paged_decode_merge",
                                  n_attn),
@@ -624,8 +653,10 @@ def main():
                            wl.step_bytes, e2e["seconds"] / e2e["steps"], world), 1),
                        "serial_us_per_step": round(e2e["serial_us_per_step"], 2),
                        "how": "every step issued from the host through the public API (the "
-                              "Python binding of the C ABI: copy_blocks, reshape_and_cache, "
-                              "paged_attention_decode), pipelined over two input and two "
+                              "Python binding of the C ABI: " + (
+                                  "paged_attention_decode_append" if wl.append else
+                                  "copy_blocks, reshape_and_cache, paged_attention_decode")
+                              + "), pipelined over two input and two "
                               "output buffers: a copy stream brings step i+1's inputs from "
                               "pinned host memory and copies step i-1's output to pinned host "
                               "memory while step i's kernels run; the host reads every byte of "
@@ -822,9 +853,10 @@ def measure_configs(device, seconds: float, warmup: int, dist, headline_attn_us:
 
 def measure_e2e_api(wl: Workload, steps: int, device, dist):
     """End to end through the public API with host buffers, every step issued
-    by the host: the step's inputs (q, new K/V, slot mapping, block tables,
-    context lengths, copy pairs) are copied from pinned host memory in one
-    transfer, the step's three calls run on the compute stream, and its
+    by the host: the step's inputs (q, new K/V, the slot mapping when the
+    writes are a call of their own, block tables, context lengths, copy
+    pairs) are copied from pinned host memory in one transfer, the step's
+    calls run on the compute stream, and its
     output is copied to pinned host memory and read, every byte, by the host.
 
     Pipelined over two device input buffers and two output buffers: while
@@ -837,8 +869,10 @@ def measure_e2e_api(wl: Workload, steps: int, device, dist):
     read after the loop, inside the timed region.  Returns the wall-clock
     seconds and the host's own issue time per step."""
     import torch
-    parts = [("q", wl.q), ("k_new", wl.k_new), ("v_new", wl.v_new), ("slots", wl.slots),
-             ("tables", wl.tables), ("ctx", wl.ctx), ("pairs", wl.pairs)]
+    # (the slot mapping only when reshape_and_cache writes the new tokens)
+    parts = [("q", wl.q), ("k_new", wl.k_new), ("v_new", wl.v_new)]
+    parts += [] if wl.append else [("slots", wl.slots)]
+    parts += [("tables", wl.tables), ("ctx", wl.ctx), ("pairs", wl.pairs)]
     sizes = [t.numel() * t.element_size() for _, t in parts]
     offs, o = [], 0
     for n in sizes:
@@ -871,9 +905,14 @@ def measure_e2e_api(wl: Workload, steps: int, device, dist):
         comp.wait_event(in_ready[p])
         if len(wl.pairs_host):
             pkv.copy_blocks(kc, vc, v["pairs"], stream=comp)
-        pkv.reshape_and_cache(v["k_new"], v["v_new"], kc, vc, v["slots"], stream=comp)
-        wl.decode_fn(outs[p], v["q"], kc, vc, v["tables"], v["ctx"], wl.scale, wl.partition,
-                     wl.ws, stream=comp)
+        if wl.append:
+            pkv.paged_attention_decode_append(outs[p], v["q"], v["k_new"], v["v_new"], kc, vc,
+                                              v["tables"], v["ctx"], wl.scale, wl.partition,
+                                              wl.ws, stream=comp)
+        else:
+            pkv.reshape_and_cache(v["k_new"], v["v_new"], kc, vc, v["slots"], stream=comp)
+            wl.decode_fn(outs[p], v["q"], kc, vc, v["tables"], v["ctx"], wl.scale,
+                         wl.partition, wl.ws, stream=comp)
         done[p].record(comp)
         # the copy stream: step i-1's output out, then step i+1's inputs in
         # (step i-1's kernels are done with input buffer 1-p)
@@ -943,8 +982,10 @@ def measure_e2e(wl: Workload, steps: int, device, dist):
     step's output.  Serial (reported beside it): one graph per step, copy in,
     kernels, copy out, then a full stream synchronise before the next step."""
     import torch
-    parts = [("q", wl.q), ("k_new", wl.k_new), ("v_new", wl.v_new), ("slots", wl.slots),
-             ("tables", wl.tables), ("ctx", wl.ctx), ("pairs", wl.pairs)]
+    # (the slot mapping only when reshape_and_cache writes the new tokens)
+    parts = [("q", wl.q), ("k_new", wl.k_new), ("v_new", wl.v_new)]
+    parts += [] if wl.append else [("slots", wl.slots)]
+    parts += [("tables", wl.tables), ("ctx", wl.ctx), ("pairs", wl.pairs)]
     sizes = [t.numel() * t.element_size() for _, t in parts]
     offs, o = [], 0
     for n in sizes:
@@ -968,8 +1009,14 @@ def measure_e2e(wl: Workload, steps: int, device, dist):
         kc, vc = wl.kc[layer], wl.vc[layer]
         if len(wl.pairs_host):
             pkv.copy_blocks(kc, vc, v["pairs"])
-        pkv.reshape_and_cache(v["k_new"], v["v_new"], kc, vc, v["slots"])
-        wl.decode_fn(out, v["q"], kc, vc, v["tables"], v["ctx"], wl.scale, wl.partition, wl.ws)
+        if wl.append:
+            pkv.paged_attention_decode_append(out, v["q"], v["k_new"], v["v_new"], kc, vc,
+                                              v["tables"], v["ctx"], wl.scale, wl.partition,
+                                              wl.ws)
+        else:
+            pkv.reshape_and_cache(v["k_new"], v["v_new"], kc, vc, v["slots"])
+            wl.decode_fn(out, v["q"], kc, vc, v["tables"], v["ctx"], wl.scale, wl.partition,
+                         wl.ws)
 
     side = torch.cuda.Stream(device=device)
     cps = torch.cuda.Stream(device=device)

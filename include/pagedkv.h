@@ -134,6 +134,34 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* k_ca
                                       size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * One decode step in one call: each sequence's newest token (the one at
+ * position context_lens[s] - 1) is written into its cache slot and attended,
+ * as pkv_reshape_and_cache with slot table[s][(ctx - 1) / B] * B + (ctx - 1) % B
+ * followed by pkv_paged_attention_decode would (wywy.jp notes, "generation
+ * phase": each iteration produces only the new token's K/V; the
+ * zhaifeiyue.github.io detail page's block-indexed formula, the query
+ * attending its own position).  The attention takes that token's K and V
+ * from k_new / v_new rather than reading them back from the cache, so the
+ * write and the attention need no ordering between them.
+ *   k_new, v_new  [num_seqs][num_heads][head_dim], device, 16-byte aligned.
+ *   k_cache, v_cache  written at the newest token's slot of every sequence
+ *                 with context_lens[s] >= 1 (nothing else is written).
+ * Outputs and cache contents are bit-identical to the two-call path.  A slot
+ * whose table entry is out of [0, num_blocks) is not written
+ * (PKV_DEVERR_BAD_BLOCK).  Every other argument and rule is that of
+ * pkv_paged_attention_decode (same workspace size); two launches on `stream`.
+ */
+pkv_status pkv_paged_attention_decode_append(void* out, const void* q, const void* k_new,
+                                             const void* v_new, void* k_cache, void* v_cache,
+                                             const int32_t* block_tables,
+                                             const int32_t* context_lens, float scale,
+                                             int num_seqs, int num_heads, int head_dim,
+                                             int block_size, int max_blocks_per_seq,
+                                             int64_t num_blocks, pkv_dtype dtype,
+                                             int partition_size, void* workspace,
+                                             size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * The same decode attention for batches whose sequences share prefix blocks
  * (parallel sampling, beam search: sequences forked from one prompt hold the
  * prompt's blocks by reference; wywy.jp notes, "Copy-on-write" and the

@@ -7,6 +7,7 @@ seeded synthetic inputs.  Build with ``python -m paged_kv_cache_05_gb300.build``
 from .pagedkv import (BlockManager, OutOfBlocks, PagedKVError, alloc_workspace, copy_blocks,
                       contiguous_attention_decode, contiguous_workspace_size,
                       decode_shared_workspace_size, decode_workspace_size, get_device_error, lib, paged_attention_decode,
+                      paged_attention_decode_append,
                       paged_attention_decode_noalloc, paged_attention_decode_shared,
                       paged_attention_prefill, paged_attention_prefill_write,
                       reshape_and_cache, set_decode_wait_limit, swap_blocks, version)
@@ -14,6 +15,7 @@ from .pagedkv import (BlockManager, OutOfBlocks, PagedKVError, alloc_workspace, 
 __all__ = ["BlockManager", "OutOfBlocks", "PagedKVError", "alloc_workspace", "copy_blocks",
            "contiguous_attention_decode", "contiguous_workspace_size",
            "decode_shared_workspace_size", "decode_workspace_size", "get_device_error", "lib", "paged_attention_decode",
+           "paged_attention_decode_append",
            "paged_attention_decode_noalloc", "paged_attention_decode_shared",
            "paged_attention_prefill", "paged_attention_prefill_write",
            "reshape_and_cache", "set_decode_wait_limit", "swap_blocks", "version"]

@@ -20,8 +20,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpagedkv.so")
 SOURCES = ["errors.cu", "cache_ops.cu", "decode_api.cu", "decode_f16.cu", "decode_bf16.cu",
-           "decode_shared_f16.cu", "decode_shared_bf16.cu", "decode_noalloc.cu", "prefill.cu",
-           "block_manager.cpp"]
+           "decode_shared_f16.cu", "decode_shared_bf16.cu", "decode_append_f16.cu",
+           "decode_append_bf16.cu", "decode_noalloc.cu", "prefill.cu", "block_manager.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -264,6 +264,48 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* k_ca
                          workspace, workspace_bytes, stream);
 }
 
+pkv_status pkv_paged_attention_decode_append(void* out, const void* q, const void* k_new,
+                                             const void* v_new, void* k_cache, void* v_cache,
+                                             const int32_t* block_tables,
+                                             const int32_t* context_lens, float scale,
+                                             int num_seqs, int num_heads, int head_dim,
+                                             int block_size, int max_blocks_per_seq,
+                                             int64_t num_blocks, pkv_dtype dtype,
+                                             int partition_size, void* workspace,
+                                             size_t workspace_bytes, cudaStream_t stream) {
+    const char* fn = "pkv_paged_attention_decode_append";
+    pkv_status st = check_shape(num_seqs, num_heads, head_dim, block_size, max_blocks_per_seq,
+                                partition_size, fn);
+    if (st != PKV_OK) return st;
+    if (num_blocks < 1) return pkv::fail(PKV_ERR_INVALID, "%s: num_blocks must be >= 1", fn);
+    if (dtype != PKV_F16 && dtype != PKV_BF16)
+        return pkv::fail(PKV_ERR_INVALID, "%s: unknown dtype", fn);
+    if (!std::isfinite(scale)) return pkv::fail(PKV_ERR_INVALID, "%s: scale is not finite", fn);
+    if (num_seqs == 0) return PKV_OK;
+    if (!block_tables || !k_new || !v_new)
+        return pkv::fail(PKV_ERR_INVALID, "%s: NULL pointer", fn);
+    if (!aligned(block_tables, 4))
+        return pkv::fail(PKV_ERR_INVALID, "%s: int32 arrays must be 4-byte aligned", fn);
+    if (!aligned(k_new, 16) || !aligned(v_new, 16))
+        return pkv::fail(PKV_ERR_INVALID, "%s: k_new and v_new must be 16-byte aligned", fn);
+    const pkv::DecodeKernel* k = dtype == PKV_F16
+                                     ? pkv::decode_kernel_append_f16(head_dim, block_size)
+                                     : pkv::decode_kernel_append_bf16(head_dim, block_size);
+    if (!k) return pkv::fail(PKV_ERR_INVALID, "%s: unsupported head_dim/block_size", fn);
+    pkv::DecodeArgs a = {};
+    a.block_tables = block_tables;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.max_blocks = max_blocks_per_seq;
+    a.ctx_cap = max_blocks_per_seq * block_size;
+    a.kv_stride = 0;
+    a.num_blocks = num_blocks;
+    a.mode = pkv::kModeAppend;
+    return launch_decode(fn, k, a, out, q, k_cache, v_cache, context_lens, scale, num_seqs,
+                         num_heads, head_dim, block_size, max_blocks_per_seq, partition_size,
+                         workspace, workspace_bytes, stream);
+}
+
 pkv_status pkv_contiguous_workspace_size(int num_seqs, int num_heads, int head_dim,
                                          int max_context_len, int partition_size,
                                          size_t* bytes) {

@@ -269,7 +269,11 @@ struct Cfg {
     // an mbarrier and the query slice of the chunk's first row.  QN > 2 NSTAGE
     // + 1 so an entry is never rewritten before every consumer warp read it.
     static constexpr int QN = 16;
-    static constexpr size_t QBAR_OFF = MISC_OFF + MISC_BYTES;
+    // per stage: the byte offset in the pools of the cache slot that the
+    // stage's newest token (taken from the call's k_new / v_new) goes to,
+    // -1 when the stage holds none (written by the producer with the copy)
+    static constexpr size_t APP_OFF = MISC_OFF + MISC_BYTES;
+    static constexpr size_t QBAR_OFF = APP_OFF + 8 * (size_t)NSTAGE;
     static constexpr size_t QID_OFF = QBAR_OFF + 8 * QN;
     static constexpr size_t QBUF_OFF = QID_OFF + 4 * QN;
     static constexpr size_t CTX_OFF = QBUF_OFF + (size_t)QN * D * 2;
@@ -960,6 +964,9 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS,
     int* scratch = reinterpret_cast<int*>(smem + C::MISC_OFF) + 4;   // NW + 1 ints
     int* s_ctx = reinterpret_cast<int*>(smem + C::CTX_OFF);
     int* s_base = s_ctx + a.S;
+    // the newest tokens come with the call (k_new / v_new)
+    constexpr bool append = MODE == kModeAppend;
+    int64_t* app_word = reinterpret_cast<int64_t*>(smem + C::APP_OFF);
     // shared prefixes: the steps a group reads for each sequence, then the unit count
     int* s_pfx = s_base + a.S + 1;
 
@@ -1122,17 +1129,47 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS,
                             // row is usually partial); the rest of the stage keeps
                             // stale bytes that the consumers mask out
                             const int tok0 = j * C::SUB;
+                            // With the newest tokens given, the row's last step
+                            // takes its last token (the newest, tn within the
+                            // step) from k_new / v_new instead of the cache, and
+                            // the stage's word tells the consumer the token's
+                            // slot, which it then writes from the stage.
+                            const bool app = append && j == ns - 1;
+                            const int tn = s_ctx[p.s] - 1 - tok0;
                             uint32_t bytes[C::BPS];
                             uint32_t tx = 0;
 #pragma unroll
                             for (int b = 0; b < C::BPS; ++b) {
                                 int valid = s_ctx[p.s] - (tok0 + b * C::TPC);
                                 valid = valid < 0 ? 0 : (valid > C::TPC ? C::TPC : valid);
+                                if (app && b == tn / C::TPC) --valid;   // (its last valid token)
                                 bytes[b] = (uint32_t)valid * (uint32_t)(D * 2);
                                 tx += 2 * bytes[b];
                             }
                             unsigned char* dst = ring + (size_t)stage * C::STAGE;
+                            if (app) {
+                                tx += 2 * (uint32_t)(D * 2);
+                                const int bn = tn / C::TPC;
+                                int64_t phys = 0;
+                                if constexpr (!CONTIG) phys = phys_raw[bn];
+                                int64_t w = -1;
+                                if (phys >= 0 && phys < a.num_blocks)
+                                    w = ((phys * H + p.h) * B + (int64_t)sub * C::SUB +
+                                         (tn - bn * C::TPC)) *
+                                        (int64_t)D * 2;
+                                else    // (its block may have nothing else to copy)
+                                    atomicOr(a.err, PKV_DEVERR_BAD_BLOCK);
+                                app_word[stage] = w;            // before the arrive (release)
+                            }
                             mbar_arrive_expect_tx(&full[stage], tx);
+                            if (app) {
+                                const int64_t nrow = ((int64_t)p.s * H + p.h) * D * 2;
+                                bulk_g2s(dst + tn * D * 2, static_cast<const char*>(a.k_new) + nrow,
+                                         D * 2, &full[stage]);
+                                bulk_g2s(dst + C::CHUNK + tn * D * 2,
+                                         static_cast<const char*>(a.v_new) + nrow, D * 2,
+                                         &full[stage]);
+                            }
 #pragma unroll
                             for (int b = 0; b < C::BPS; ++b) {
                                 if (bytes[b] == 0) continue;
@@ -1479,6 +1516,24 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS,
                     }
                 }
                 m = m_new;
+                if constexpr (append) {
+                    // the row's last step with a new token: write its K and V
+                    // rows from the stage into the token's cache slot (lanes
+                    // 0 .. LPT-1 the K row, the next LPT the V row, 16 bytes
+                    // each), before the stage is released
+                    const int64_t w =
+                        have && i == len - 1 && p.j + len == ns ? app_word[stage] : -1;
+                    if (w >= 0 && lane < 2 * C::LPT) {
+                        const int isv = lane >= C::LPT ? 1 : 0;
+                        const int c16 = (lane & (C::LPT - 1)) * 16;
+                        const uint4 val = *reinterpret_cast<const uint4*>(
+                            ring + (size_t)stage * C::STAGE + isv * C::CHUNK +
+                            (nvalid - 1) * D * 2 + c16);
+                        char* pool = const_cast<char*>(
+                            static_cast<const char*>(isv ? a.v_cache : a.k_cache));
+                        *reinterpret_cast<uint4*>(pool + w + c16) = val;
+                    }
+                }
                 __syncwarp();
                 if (lane == 0 && have) mbar_arrive(&empty[stage]);
             }

@@ -124,6 +124,11 @@ struct DecodeArgs {
     const void* v_cache;
     const int32_t* block_tables;
     const int32_t* context_lens;
+    // paged layout only: the newest token's K and V ([S][H][D]), taken by the
+    // attention from here and stored into the token's cache slot (null: the
+    // cache already holds them)
+    const void* k_new;
+    const void* v_new;
     float scale_log2;        // softmax scale * log2(e)
     int S, H, max_blocks;
     int ctx_cap;             // largest valid context length (max_blocks * B, or the
@@ -135,7 +140,7 @@ struct DecodeArgs {
     int main_grid;           // CTAs of the main kernel
     uint64_t epoch;          // 40-bit tag of this call (claims of the dynamic chunks)
     uint64_t wait_ns;        // bound of the pipeline waits (pkv_set_decode_wait_limit)
-    int mode;                // decode kind (kModePaged, kModeContig, kModeShared)
+    int mode;                // decode kind (kModePaged, kModeContig, kModeShared, kModeAppend)
     char* ws;
     WsLayout ws_l;
     int32_t* err;
@@ -155,13 +160,18 @@ struct DecodeKernel {
 
 const DecodeKernel* decode_kernel_f16(int D, int B);
 const DecodeKernel* decode_kernel_bf16(int D, int B);
+// the same, writing each sequence's newest token (kModeAppend)
+const DecodeKernel* decode_kernel_append_f16(int D, int B);
+const DecodeKernel* decode_kernel_append_bf16(int D, int B);
 // the same kernels over a contiguous [seq][head][token][D] K/V layout (no block table)
 const DecodeKernel* decode_kernel_contig_f16(int D);
 const DecodeKernel* decode_kernel_contig_bf16(int D);
 // the paged kernels with shared prefixes read once (a group pass launched first)
 const DecodeKernel* decode_kernel_shared_f16(int D, int B);
 const DecodeKernel* decode_kernel_shared_bf16(int D, int B);
-enum : int { kModePaged = 0, kModeContig = 1, kModeShared = 2 };
+// kModeAppend: the paged layout, with the newest token of every sequence
+// taken from the call's k_new / v_new and written into its cache slot
+enum : int { kModePaged = 0, kModeContig = 1, kModeShared = 2, kModeAppend = 3 };
 
 // ---- cache kernels -----------------------------------------------------------
 cudaError_t launch_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,

@@ -57,6 +57,8 @@ def lib():
             "pkv_decode_workspace_size": ([i32, i32, i32, i32, i32, i32, ctypes.POINTER(sz)], i32),
             "pkv_paged_attention_decode": ([P, P, P, P, P, P, f32, i32, i32, i32, i32, i32, i64,
                                             i32, i32, P, sz, P], i32),
+            "pkv_paged_attention_decode_append": ([P, P, P, P, P, P, P, P, f32, i32, i32, i32,
+                                                   i32, i32, i64, i32, i32, P, sz, P], i32),
             "pkv_decode_shared_workspace_size": ([i32, i32, i32, i32, i32, i32,
                                                   ctypes.POINTER(sz)], i32),
             "pkv_paged_attention_decode_shared": ([P, P, P, P, P, P, f32, i32, i32, i32, i32,
@@ -201,6 +203,41 @@ def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens,
                                             int(partition_size), wsp,
                                             workspace.numel() * workspace.element_size(),
                                             _stream(stream)))
+    return out
+
+
+def paged_attention_decode_append(out, q, k_new, v_new, k_cache, v_cache, block_tables,
+                                  context_lens, scale, partition_size=0, workspace=None,
+                                  stream=None):
+    """One decode step: each sequence's newest token (position ctx - 1) is
+    written into its cache slot from k_new / v_new [S, H, D] and attended
+    (reshape_and_cache with the table's slot, then paged_attention_decode)."""
+    torch = _torch()
+    S, H, D = q.shape
+    nb, H2, B, D2 = k_cache.shape
+    if (H2, D2) != (H, D) or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("q / cache shape mismatch")
+    if tuple(out.shape) != (S, H, D) or out.dtype != q.dtype or k_cache.dtype != q.dtype:
+        raise ValueError("out/q/cache dtype or shape mismatch")
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        if tuple(t.shape) != (S, H, D) or t.dtype != q.dtype:
+            raise ValueError("%s must be [num_seqs, num_heads, head_dim] of q's dtype" % n)
+    if block_tables.dim() != 2 or block_tables.shape[0] != S:
+        raise ValueError("block_tables must be [num_seqs, max_blocks]")
+    if workspace is None:
+        workspace = alloc_workspace(S, H, D, B, block_tables.shape[1], partition_size,
+                                    q.device)
+    ptrs = [_dev(out, "out"), _dev(q, "q"), _dev(k_new, "k_new"), _dev(v_new, "v_new"),
+            _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+            _dev(block_tables, "block_tables", torch.int32),
+            _dev(context_lens, "context_lens", torch.int32, 1)]
+    wsp = _dev(workspace, "workspace")
+    _check("pkv_paged_attention_decode_append",
+           lib().pkv_paged_attention_decode_append(*ptrs, float(scale), S, H, D, B,
+                                                   block_tables.shape[1], nb,
+                                                   _dtype_code(q.dtype), int(partition_size), wsp,
+                                                   workspace.numel() * workspace.element_size(),
+                                                   _stream(stream)))
     return out
 
 

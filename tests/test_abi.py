@@ -79,6 +79,38 @@ def test_decode_rejects_bad_arguments_before_touching_a_gpu(pkv):
     assert call(S=0) == 0                   # empty batch: nothing to do
 
 
+def test_decode_append_rejects_bad_arguments_before_touching_a_gpu(pkv):
+    """The one-call decode step checks what pkv_paged_attention_decode checks,
+    plus its k_new / v_new pointers, and launches nothing when a check fails."""
+    L = pkv.lib()
+    ws = ctypes.c_size_t(0)
+    assert L.pkv_decode_workspace_size(4, 8, 64, 16, 4, 0, ctypes.byref(ws)) == 0
+    fake = 1 << 20   # never dereferenced: validation fails first
+    names = ["out", "q", "kn", "vn", "k", "v", "bt", "cl", "scale", "S", "H", "D", "B", "maxb",
+             "nb", "dtype", "part", "ws", "wsb", "stream"]
+    base = [fake, fake, fake, fake, fake, fake, fake, fake, 0.125, 4, 8, 64, 16, 4, 64, 0, 0,
+            fake * 256, ws.value, None]
+
+    def call(**kw):
+        args = list(base)
+        for k, v in kw.items():
+            args[names.index(k)] = v
+        return L.pkv_paged_attention_decode_append(*args)
+
+    assert call(kn=None) == 1 and "NULL" in pkv.pagedkv.last_error()
+    assert call(vn=None) == 1
+    assert call(kn=fake + 8) == 1 and "aligned" in pkv.pagedkv.last_error()
+    assert call(vn=fake + 4) == 1
+    assert call(D=80) == 1
+    assert call(B=4) == 1
+    assert call(nb=0) == 1
+    assert call(dtype=7) == 1
+    assert call(scale=float("inf")) == 1
+    assert call(out=0) == 1
+    assert call(wsb=ws.value - 1) == 1 and "workspace" in pkv.pagedkv.last_error()
+    assert call(S=0) == 0                   # empty batch: nothing to do
+
+
 def test_cache_ops_reject_bad_arguments(pkv):
     L = pkv.lib()
     f = 1 << 20

@@ -305,8 +305,9 @@ def test_batch_size_limit(pkv):
 def test_pipeline_wait_timeout_is_reported_and_the_next_call_is_correct(pkv, partition):
     """The timeout path of the decode kernels, made to run out on purpose by
     a short wait bound (no wait is broken: with a 0 ns bound a pipeline wait
-    gives up at its first check that finds the phase incomplete, which on a
-    batch of about 57K steps happens in some CTA on essentially every call).
+    gives up once its phase stays incomplete over 32 polls and a tick of the
+    global timer, which on a batch of about 57K steps happens in some CTA
+    within a few calls; how many depends on timing, so up to 40 are made).
     The call must return, set PKV_DEVERR_TIMEOUT and nothing else; a normal
     call on the same stream right after it must match the oracle."""
     import torch
@@ -327,7 +328,7 @@ def test_pipeline_wait_timeout_is_reported_and_the_next_call_is_correct(pkv, par
     prev = P.set_decode_wait_limit(0)
     seen = []
     try:
-        for _ in range(5):
+        for _ in range(40):
             pkv.paged_attention_decode(out, q, kc, vc, bt, cl, scale, partition_size=partition,
                                        workspace=ws)
             torch.cuda.synchronize()
