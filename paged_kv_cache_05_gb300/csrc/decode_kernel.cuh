@@ -43,6 +43,12 @@
 //     slots of each split (s, h) with the log-sum-exp rule.
 //   * CUDA cores, not tensor cores: decode attention is a matrix-vector
 //     product, about 0.5 flop per byte of K/V, bound by HBM bandwidth.
+//   * One decode step in one call (kModeAppend): the newest token of every
+//     sequence (position ctx - 1) comes with the call; the producer copies its
+//     K and V rows from k_new / v_new into their place in the row's last stage
+//     instead of the cache's slot, and the consumer warp that takes that step
+//     stores them from the stage into the slot.  No other step of the call
+//     reads the slot, so the write needs no ordering against the attention.
 //   * Every wait is bounded.  The pipeline waits (ring stages, claimed-chunk
 //     queue, the consumer warps' meeting at a piece end) give up after the
 //     launch's limit (1 s unless the caller shortened it): the warp sets the
