@@ -120,6 +120,12 @@ pkv_status pkv_decode_workspace_size(int num_seqs, int num_heads, int head_dim,
  * or a partial (max, sum, unnormalised output) that a second kernel merges
  * with the log-sum-exp rule.  Two launches on `stream`.
  *
+ * Reproducibility: with the balanced split (partition_size 0) the last
+ * quarter of the work is claimed by CTAs at run time, which decides the order
+ * in which a row's terms are summed, so two calls may differ in the last bits
+ * (each within rounding of the exact result); a nonzero partition_size gives
+ * every CTA the same work on every call and bit-identical results.
+ *
  * workspace: device, >= pkv_decode_workspace_size(...) bytes, 256-B aligned;
  * its contents need no initialisation and are scratch between calls; two
  * calls in flight at once must not share it.
