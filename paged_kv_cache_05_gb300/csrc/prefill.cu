@@ -9,10 +9,12 @@
 // positions 0 .. p (causal):
 //   out[i][h] = sum_{t <= p} softmax_t(scale * q[i][h] . K[t][h]) V[t][h].
 //
-// Design.  Persistent CTAs, one per SM, walk the work items longest first;
+// Design.  Persistent CTAs, one per SM, in pairs (clusters of two, one TPC);
 // an item is 256 query rows of one (sequence, head): two query tiles A and B
 // of 128 rows, one row per tensor-memory lane, that share every K/V tile of
-// 128 keys.  Eleven warps:
+// 128 keys.  Each pair takes a contiguous run, of equal estimated cost, of
+// the units (sequence, head pair, item; items from the last down), the two
+// CTAs the same item of adjacent heads.  Eleven warps:
 //   warps 0, 10 TMA producers: the two query tiles of each item and the K
 //               tiles (warp 0), the V tiles (warp 10), block by block through
 //               the block table (2-D tiled copies with the 128-byte swizzle),
@@ -455,44 +457,181 @@ struct Item {
     int n_kv;                        // key tiles loaded: the larger of n[0], n[1]
 };
 
-// Work items: (sequence, head) pairs in groups of kGroupPairs, and within a
-// group longest first (item q_items-1 down to 0, then pair), so that the CTAs
-// running at one time share the K/V of few pairs in L2.  False for an empty
-// item (past the sequence's query rows) or a sequence whose lengths are out
-// of range (flagged once).
-constexpr int kGroupPairs = 16;
-__device__ __forceinline__ bool item_at(const PrefillArgs& a, int64_t w, bool flag, Item& it,
-                                        bool whole = false) {
-    const int64_t sh = (int64_t)a.S * a.H;
-    const int64_t per_group = (int64_t)a.q_items * kGroupPairs;
-    const int64_t grp = w / per_group;
-    const int64_t r = w - grp * per_group;
-    const int64_t first = grp * kGroupPairs;
-    const int gs = (int)(sh - first < kGroupPairs ? sh - first : kGroupPairs);
-    const int t = a.q_items - 1 - (int)(r / gs);
-    const int64_t pair = first + r % gs;
-    it.s = (int)(pair / a.H);
-    it.h = (int)(pair - (int64_t)it.s * a.H);
-    it.q0 = a.query_start[it.s];
-    it.qlen = a.query_start[it.s + 1] - it.q0;
-    it.ctx = a.context_lens[it.s];
-    if (it.ctx < 0 || it.ctx > a.max_blocks * a.B || it.qlen < 0 || it.qlen > it.ctx ||
-        it.q0 < 0 || (int64_t)it.q0 + it.qlen > a.num_tokens || (whole && it.qlen != it.ctx)) {
-        if (flag && t == 0 && it.h == 0) atomicOr(a.err, PKV_DEVERR_BAD_CONTEXT);
+// Lengths of one sequence and its number of items (0 for a sequence whose
+// lengths are out of range, or, with whole, not a whole prompt).
+struct SeqInfo {
+    int q0, qlen, ctx, ni;
+};
+__device__ __forceinline__ bool seq_info(const PrefillArgs& a, int s, bool whole, SeqInfo& si) {
+    si.q0 = a.query_start[s];
+    si.qlen = a.query_start[s + 1] - si.q0;
+    si.ctx = a.context_lens[s];
+    si.ni = 0;
+    if (si.ctx < 0 || si.ctx > a.max_blocks * a.B || si.qlen < 0 || si.qlen > si.ctx ||
+        si.q0 < 0 || (int64_t)si.q0 + si.qlen > a.num_tokens || (whole && si.qlen != si.ctx))
         return false;
-    }
-    if (flag && t == 0 && it.h == 0 && it.qlen > a.max_query_len)
-        atomicOr(a.err, PKV_DEVERR_BAD_CONTEXT);     // rows past the last item stay unwritten
+    const int n = (si.qlen + kRows - 1) / kRows;   // rows past the last item stay unwritten
+    si.ni = n < a.q_items ? n : a.q_items;
+    return true;
+}
+
+// Item t of a sequence: per query tile its rows, first position and key tiles.
+__device__ __forceinline__ void item_tiles(const SeqInfo& si, int t, Item& it) {
     it.q_begin = t * kRows;
-    if (it.q_begin >= it.qlen) return false;
     for (int x = 0; x < 2; ++x) {
         const int b = it.q_begin + x * kBM;
-        it.rows[x] = it.qlen - b < kBM ? (it.qlen - b > 0 ? it.qlen - b : 0) : kBM;
-        it.pos0[x] = it.ctx - it.qlen + b;           // position of the tile's first query
+        it.rows[x] = si.qlen - b < kBM ? (si.qlen - b > 0 ? si.qlen - b : 0) : kBM;
+        it.pos0[x] = si.ctx - si.qlen + b;            // position of the tile's first query
         it.n[x] = it.rows[x] > 0 ? (it.pos0[x] + it.rows[x] - 1) / kBN + 1 : 0;
     }
     it.n_kv = it.n[1] > it.n[0] ? it.n[1] : it.n[0];
-    return true;
+}
+
+// Estimated cost of an item, in tenths of a 128 x 128 tile product issued
+// beside the other query tile's: a key tile both query tiles see costs 20, one
+// that only one of them sees 17 (its softmax, products and hand-offs then run
+// with nothing to overlap them), and the item's fixed work (its query load,
+// first products and output) 24.  Fitted to the per-CTA times of 16 prompts
+// of 543-1729 tokens (40 heads x 128) under several schedules.
+constexpr int kPairCost = 20, kSoloCost = 17, kItemCost = 24;
+__device__ __forceinline__ int item_cost(const SeqInfo& si, int t) {
+    Item it;
+    item_tiles(si, t, it);
+    const int lo = it.n[0] < it.n[1] ? it.n[0] : it.n[1];
+    const int hi = it.n[0] < it.n[1] ? it.n[1] : it.n[0];
+    return kPairCost * lo + kSoloCost * (hi - lo) + kItemCost;
+}
+
+// Work schedule.  A unit is item t of heads 2 hp and 2 hp + 1 of sequence s,
+// one head for each CTA of a pair (clusters of two); the units are ordered by
+// sequence, head pair, then t from the last item down, and each CTA pair takes
+// a contiguous run of them of equal estimated cost: unit u, whose cost c_u
+// follows P_u of cost before it, belongs to pair k when
+// th(k) <= 2 P_u + c_u < th(k + 1), th(k) = floor(2 k P_total / pairs), where
+// P_total is the cost of all units.  A CTA thus works on one (sequence, head)
+// at a time, item after item, each item finding in L2 the K/V tiles the one
+// before it loaded, and the two CTAs of a pair run the same item shapes side
+// by side.
+struct Sched {
+    int s, hp;         // first unit that may belong to the pair: (s, hp, last item)
+    int64_t P;         // cost of the units before it
+    int64_t lo, hi;    // the pair's thresholds th(k), th(k + 1)
+};
+
+struct Walker {
+    int s, hp, ti;     // the next unit: (sequence, head pair, items from the last)
+    int64_t P;         // cost of the units before it
+    __device__ __forceinline__ void init(const Sched& sc) {
+        s = sc.s;
+        hp = sc.hp;
+        ti = 0;
+        P = sc.P;
+    }
+    // the pair's next unit, as this CTA's item (its head 2 hp + rank)
+    __device__ __forceinline__ bool next(const PrefillArgs& a, const Sched& sc, bool whole,
+                                         Item& it) {
+        const int HP = (a.H + 1) >> 1;
+        const int rank = (int)(blockIdx.x & 1u);
+        while (s < a.S) {
+            SeqInfo si;
+            seq_info(a, s, whole, si);
+            if (si.ni == 0) {                         // no items: the next sequence
+                ++s;
+                hp = 0;
+                ti = 0;
+                continue;
+            }
+            const int t = si.ni - 1 - ti;
+            const int c = item_cost(si, t);
+            item_tiles(si, t, it);
+            const int64_t v = 2 * P + c;
+            if (v >= sc.hi) {
+                s = a.S;
+                return false;
+            }
+            const int h = 2 * hp + rank;
+            const bool mine = v >= sc.lo && h < a.H;
+            it.s = s;
+            it.h = h;
+            it.q0 = si.q0;
+            it.qlen = si.qlen;
+            it.ctx = si.ctx;
+            P += c;
+            if (++ti == si.ni) {
+                ti = 0;
+                if (++hp == HP) {
+                    ++s;
+                    hp = 0;
+                }
+            }
+            if (mine) return true;
+        }
+        return false;
+    }
+};
+
+// Locates the pair's first unit (one warp; every CTA computes the same
+// total).  CTA 0 flags each sequence whose lengths are out of range, or
+// whose rows pass max_query_len (those rows stay unwritten).
+__device__ __forceinline__ void plan(const PrefillArgs& a, bool whole, Sched* out, int lane) {
+    const int HP = (a.H + 1) >> 1;
+    long long tot = 0;
+    for (int s0 = 0; s0 < a.S; s0 += 32) {
+        const int s = s0 + lane;
+        if (s >= a.S) break;
+        SeqInfo si;
+        const bool good = seq_info(a, s, whole, si);
+        if (blockIdx.x == 0 && (!good || si.qlen > a.max_query_len))
+            atomicOr(a.err, PKV_DEVERR_BAD_CONTEXT);
+        for (int t = 0; t < si.ni; ++t) tot += item_cost(si, t);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    tot *= HP;
+    const int64_t np = gridDim.x >> 1, k = blockIdx.x >> 1;
+    const int64_t A = 2 * (int64_t)tot;
+    const int64_t lo = k * (A / np) + (k * (A % np)) / np;
+    const int64_t hi = (k + 1) * (A / np) + ((k + 1) * (A % np)) / np;
+    // the first sequence whose units reach past lo
+    int fs = a.S;
+    int64_t fP = 0, fT = 0;
+    long long carry = 0;
+    for (int s0 = 0; s0 < a.S && fs == a.S; s0 += 32) {
+        const int s = s0 + lane;
+        long long ts = 0;
+        if (s < a.S) {
+            SeqInfo si;
+            seq_info(a, s, whole, si);
+            for (int t = 0; t < si.ni; ++t) ts += item_cost(si, t);
+        }
+        long long e = ts * HP;                        // inclusive scan of the sequences' cost
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long u = __shfl_up_sync(0xffffffffu, e, o);
+            if (lane >= o) e += u;
+        }
+        e += carry;
+        const unsigned hit = __ballot_sync(0xffffffffu, s < a.S && 2 * e > lo);
+        if (hit) {
+            const int f = __ffs(hit) - 1;
+            fs = s0 + f;
+            fT = __shfl_sync(0xffffffffu, ts, f);
+            fP = __shfl_sync(0xffffffffu, e, f) - fT * HP;
+        }
+        carry = __shfl_sync(0xffffffffu, e, 31);
+    }
+    if (lane == 0) {
+        int hp0 = 0;
+        if (fs < a.S && fT > 0 && lo > 2 * fP) {
+            const int64_t h = (lo - 2 * fP) / (2 * fT);
+            hp0 = (int)(h < HP - 1 ? h : HP - 1);
+        }
+        out->s = fs;
+        out->hp = hp0;
+        out->P = fP + (int64_t)hp0 * fT;
+        out->lo = lo;
+        out->hi = hi;
+    }
 }
 
 template <typename T, int D, bool FUSED>
@@ -517,8 +656,7 @@ __global__ void __launch_bounds__(threads_for(FUSED), 1)
         reinterpret_cast<volatile int*>(gbase + C::BAR_OFF + 8 * kBarCount + 4);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int64_t n_items = (int64_t)a.q_items * a.S * a.H;
-    const int64_t w0 = blockIdx.x, dw = gridDim.x;
+    Sched* sched = reinterpret_cast<Sched*>(gbase + C::BAR_OFF + 8 * kBarCount + 8);
 
     if (tid == 0) {
         for (int i = 0; i < kBarCount; ++i)
@@ -533,6 +671,7 @@ __global__ void __launch_bounds__(threads_for(FUSED), 1)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
+    if (warp == 2) plan(a, FUSED, sched, lane);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -558,9 +697,10 @@ __global__ void __launch_bounds__(threads_for(FUSED), 1)
             int64_t g = 0;
             int items = 0;
             bool ok = true;
-            for (int64_t w = w0; ok && w < n_items; w += dw) {
-                Item it;
-                if (!item_at(a, w, false, it, FUSED)) continue;
+            Walker wk;
+            wk.init(*sched);
+            Item it;
+            while (ok && wk.next(a, *sched, FUSED, it)) {
                 if (kq) {
                     // both query tiles, once the previous item's S products are done
                     if (items > 0 && !mbar_wait(bar(kBarQEmpty), (items - 1) & 1, abort_flag)) {
@@ -637,9 +777,10 @@ __global__ void __launch_bounds__(threads_for(FUSED), 1)
         int64_t g = 0;
         unsigned char* kc = static_cast<unsigned char*>(a.k_cache);
         unsigned char* vc = static_cast<unsigned char*>(a.v_cache);
-        for (int64_t w = w0; ok && w < n_items; w += dw) {
-            Item it;
-            if (!item_at(a, w, false, it, FUSED)) continue;
+        Walker wk;
+        wk.init(*sched);
+        Item it;
+        while (ok && wk.next(a, *sched, FUSED, it)) {
             const int32_t* row_tab = a.block_tables + (int64_t)it.s * a.max_blocks;
             for (int j = 0; j < it.n_kv; ++j, ++g) {
                 const int st = (int)(g % NST);
@@ -746,15 +887,9 @@ __global__ void __launch_bounds__(threads_for(FUSED), 1)
             // The next item is looked up while the current one runs: its
             // lengths are global loads whose latency would otherwise fall
             // between two items, when nothing is queued on the tensor pipe.
-            int64_t wn = w0;
-            auto next_item = [&](Item& nit) -> bool {
-                for (; wn < n_items; wn += dw)
-                    if (item_at(a, wn, true, nit, FUSED)) {
-                        wn += dw;
-                        return true;
-                    }
-                return false;
-            };
+            Walker wk;
+            wk.init(*sched);
+            auto next_item = [&](Item& nit) -> bool { return wk.next(a, *sched, FUSED, nit); };
             Item nit;
             bool have = next_item(nit);
             while (ok && have) {
@@ -857,9 +992,10 @@ __global__ void __launch_bounds__(threads_for(FUSED), 1)
         int64_t gx = 0;                              // this group's tiles so far
         int64_t g = 0;                               // key tiles so far (V stage)
         int items = 0;
-        for (int64_t w = w0; ok && w < n_items; w += dw) {
-            Item it;
-            if (!item_at(a, w, false, it, FUSED)) continue;
+        Walker wk;
+        wk.init(*sched);
+        Item it;
+        while (ok && wk.next(a, *sched, FUSED, it)) {
             const int nx = x ? it.n[1] : it.n[0];
             const int pos0 = x ? it.pos0[1] : it.pos0[0];
             const int rows = x ? it.rows[1] : it.rows[0];
@@ -1115,9 +1251,8 @@ cudaError_t launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const C
     cudaError_t e = cudaFuncSetAttribute(paged_prefill_tc<T, D, FUSED>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    // Clusters of two CTAs, so that CTAs 2k and 2k + 1, which take
-    // neighbouring items (as a rule the same sequence and query tiles and
-    // adjacent heads, so the same cache blocks), run on the two SMs of one TPC.  How the CTAs
+    // Clusters of two CTAs, so that CTAs 2k and 2k + 1, which take the same
+    // items of adjacent heads, run on the two SMs of one TPC.  How the CTAs
     // are paired matters on GB300: placed at random (as a programmatic
     // dependent of a reshape_and_cache, whose CTAs let it launch as they
     // start), most CTAs ran 1.3-1.5x longer on the same items; the default
@@ -1127,14 +1262,16 @@ cudaError_t launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const C
     // either: that still cost 13 us after a reshape_and_cache.
     cudaLaunchConfig_t cfg = {};
     // persistent: one CTA per SM (shared memory and tensor memory allow no
-    // more), each walking the work items grid-stride, longest first
+    // more), each pair walking its run of the units
     int dev = 0;
     e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    const int64_t items = (int64_t)a.q_items * a.S * a.H;
+    // an even number of CTAs (pairs), no more than two per unit of work
+    const int64_t units = (int64_t)a.q_items * a.S * ((a.H + 1) / 2);
     const int sms = pkv::sm_count(dev);
     if (sms < 1) return cudaErrorInvalidDevice;
-    cfg.gridDim = dim3((unsigned)(items < sms ? items : sms));
+    const int64_t pairs = sms / 2 > 1 ? sms / 2 : 1;
+    cfg.gridDim = dim3((unsigned)(2 * (units < pairs ? units : pairs)));
     cfg.blockDim = dim3(threads_for(FUSED));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
@@ -1189,6 +1326,16 @@ pkv_status prefill_common(const char* fn, void* out, const void* q, const void* 
     if (num_blocks * num_heads * block_size >= (1LL << 31))
         return pkv::fail(PKV_ERR_INVALID, "%s: pool too large for 32-bit row coordinates", fn);
     if (dtype != PKV_F16 && dtype != PKV_BF16) return pkv::fail(PKV_ERR_INVALID, "%s: dtype", fn);
+    {
+        // the work schedule sums item costs in 64 bits: a bound far above any
+        // call whose tensors fit in memory
+        const double units = (double)((num_heads + 1) / 2) * num_seqs *
+                             (double)(((int64_t)max_query_len + kRows - 1) / kRows);
+        const double unit_cost =
+            kPairCost * ((double)max_blocks_per_seq * block_size / kBN + 1.0) + kItemCost;
+        if (units * unit_cost >= 0x1p60)
+            return pkv::fail(PKV_ERR_INVALID, "%s: too much work for one call", fn);
+    }
     if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f)
         return pkv::fail(PKV_ERR_INVALID, "%s: scale is not finite", fn);
     if (num_seqs == 0 || max_query_len == 0 || num_query_tokens == 0) return PKV_OK;

@@ -291,3 +291,40 @@ def test_prefill_long_context_continued(pkv, dtype):
     rescales, and the last partial block."""
     rs = np.random.default_rng(980 + (dtype == "bf16"))
     run_case(pkv, rs, [6000, 90], [300, 90], 2, 128, 16, dtype)
+
+
+def test_prefill_bad_lengths_flagged_and_skipped(pkv):
+    """A sequence with more new tokens than context is flagged and skipped (its
+    rows stay unwritten); a sequence with more new tokens than max_query_len
+    is flagged, its rows past the last 256-row item the call plans stay
+    unwritten and the others are computed; the sequences beside them are
+    computed.  Three heads: the second CTA of a pair has no head in the last
+    head pair."""
+    import torch
+    from paged_kv_cache_05_gb300 import pagedkv as P
+    rs = np.random.default_rng(960)
+    H, D, B, dt = 3, 128, 16, "f16"
+    ctx = [300, 90, 500, 600, 40]
+    qlen = [300, 120, 200, 600, 1]                  # sequence 1: 120 new tokens, context 90
+    case = random_case(rs, len(ctx), H, D, B, [max(c, n) for c, n in zip(ctx, qlen)], dt)
+    qs = np.concatenate([[0], np.cumsum(qlen)]).astype(np.int32)
+    T = int(qs[-1])
+    q = words((T, H, D), dt, rs)
+    out = torch.full((T, H, D), float("nan"), dtype=torch.float16, device="cuda")
+    max_query_len = 300                              # two items: sequence 3 keeps rows 0..511
+    pkv.paged_attention_prefill(out, to_dev(q, dt), to_dev(case["kc"], dt),
+                                to_dev(case["vc"], dt), torch.from_numpy(case["bt"]).cuda(),
+                                torch.from_numpy(np.array(ctx, np.int32)).cuda(),
+                                torch.from_numpy(qs).cuda(), 0.088, max_query_len)
+    assert pkv.get_device_error() == P.DEVERR_BAD_CONTEXT
+    got = out.cpu()
+    assert torch.isnan(got[qs[1]:qs[2]]).all()
+    assert torch.isnan(got[qs[3] + 512:qs[4]]).all()
+    for s, rows in [(0, qlen[0]), (2, qlen[2]), (3, 512), (4, qlen[4])]:
+        # rows 0 .. rows-1 of sequence s, as a sequence of its own cut at
+        # context ctx - qlen + rows (causal rows attend up to their own)
+        cut = ctx[s] - qlen[s] + rows
+        ref = oracle.paged_attention_prefill(q[qs[s]:qs[s] + rows], case["kc"], case["vc"],
+                                             case["bt"][s:s + 1], np.array([cut], np.int32),
+                                             np.array([0, rows], np.int32), 0.088, ORC_DTYPE[dt])
+        attn_check(got[qs[s]:qs[s] + rows], ref, "sequence %d" % s)
