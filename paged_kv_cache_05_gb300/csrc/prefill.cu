@@ -10,20 +10,26 @@
 //   out[i][h] = sum_{t <= p} softmax_t(scale * q[i][h] . K[t][h]) V[t][h].
 //
 // Design.  Persistent CTAs, one per SM, in pairs (clusters of two, one TPC);
-// an item is 256 query rows of one (sequence, head): two query tiles A and B
-// of 128 rows, one row per tensor-memory lane, that share every K/V tile of
-// 128 keys.  Each pair takes a contiguous run, of equal estimated cost, of
-// the units (sequence, head pair, item; items from the last down), the two
-// CTAs the same item of adjacent heads.  Eleven warps:
-//   warps 0, 10 TMA producers: the two query tiles of each item and the K
-//               tiles (warp 0), the V tiles (warp 10), block by block through
-//               the block table (2-D tiled copies with the 128-byte swizzle),
-//               each in a ring of 2-4 stages;
+// an item is 256 query rows of one (sequence, head): two query tiles of 128
+// rows, one row per tensor-memory lane, that share every K/V tile of 128
+// keys.  Each pair takes a contiguous run, of equal estimated cost, of the
+// units (sequence, head pair, item; items from the last down), the two CTAs
+// the same item of adjacent heads.  The item's tiles go to two slots X = 0, 1
+// (a softmax group, its query buffer and tensor-memory columns each), the
+// later 128 rows, which see one more (diagonal) key tile, to slot 1 in even
+// items and slot 0 in odd ones, and at each key tile the slot with more key
+// tiles is served first: the group that ends an item first leads the next.
+// Eleven warps:
+//   warps 0, 10 TMA producers: the query tiles of each item (the first-served
+//               slot's before the item's first K tile) and the K tiles (warp
+//               0), the V tiles (warp 10), block by block through the block
+//               table (2-D tiled copies with the 128-byte swizzle), each in a
+//               ring of 2-4 stages;
 //   warp 1      owns the tensor memory and issues the MMAs from one thread:
-//               S_X = Q_X K^T (X = A, B; 128 x 128 fp32 in tensor memory) and
+//               S_X = Q_X K^T (128 x 128 fp32 in tensor memory) and
 //               O_X += P_X V with P_X read from tensor memory, where the
 //               softmax wrote it over S_X;
-//   warps 2..5  softmax of tile A, warps 6..9 of tile B, one row per thread:
+//   warps 2..5  softmax of slot 0, warps 6..9 of slot 1, one row per thread:
 //               read S from tensor memory, causal mask (diagonal tiles only),
 //               online softmax in log2 units, write P (16-bit, packed in
 //               pairs) back over S, rescale O when the running max grows.
@@ -55,7 +61,7 @@
 namespace {
 
 constexpr int kBM = 128;            // query rows per tile (MMA M, tensor-memory lanes)
-constexpr int kRows = 2 * kBM;      // query rows per work item (tiles A and B)
+constexpr int kRows = 2 * kBM;      // query rows per work item (two query tiles)
 constexpr int kBN = 128;            // keys per K/V tile (MMA N of S, K of P V)
 constexpr int kWarps = 11;          // K producer, MMA issuer, 2 x 4 softmax warps, V producer
 constexpr int kThreads = kWarps * 32;
@@ -286,30 +292,6 @@ __device__ __forceinline__ void tmem_wait64(uint32_t (&r)[64]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]), "+r"(r[32]), "+r"(r[33]), "+r"(r[34]), "+r"(r[35]), "+r"(r[36]), "+r"(r[37]), "+r"(r[38]), "+r"(r[39]), "+r"(r[40]), "+r"(r[41]), "+r"(r[42]), "+r"(r[43]), "+r"(r[44]), "+r"(r[45]), "+r"(r[46]), "+r"(r[47]), "+r"(r[48]), "+r"(r[49]), "+r"(r[50]), "+r"(r[51]), "+r"(r[52]), "+r"(r[53]), "+r"(r[54]), "+r"(r[55]), "+r"(r[56]), "+r"(r[57]), "+r"(r[58]), "+r"(r[59]), "+r"(r[60]), "+r"(r[61]), "+r"(r[62]), "+r"(r[63]) : : "memory");
 }
 
-// 64 consecutive columns of this warp's lanes, load and wait in one statement.
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-        "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
-        "%28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, "
-        "%45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, "
-        "%62, %63}, [%64];\n\t"
-        "tcgen05.wait::ld.sync.aligned;"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-          "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]),
-          "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]),
-          "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]),
-          "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]),
-          "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]),
-          "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
-        : "r"(taddr)
-        : "memory");
-}
-
 // Store 16 columns of this warp's lanes and wait for the store to complete.
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
     asm volatile(
@@ -435,26 +417,28 @@ struct PrefillArgs {
 
 // barrier slots (8 bytes each) in the barrier region
 enum : int {
-    kBarQFull = 0,
-    kBarQEmpty = 1,
-    kBarKFull = 2,    // + stage (up to 4)
-    kBarKEmpty = 6,   // + stage
-    kBarVFull = 10,   // + stage
-    kBarVEmpty = 14,  // + stage
-    kBarSFull = 18,   // + group: S_X computed (and every earlier product)
-    kBarPFull = 20,   // + group: P_X written, O_X rescaled
-    kBarPvDone = 22,  // + group: an item's last O_X += P_X V completed
-    kBarMmaDone = 24,
-    kBarKStored = 25, // + stage: the cache writer is done with a K stage (FUSED)
-    kBarVStored = 29, // + stage: ... with a V stage
-    kBarCount = 33
+    kBarQFull = 0,    // + slot: its query tile of the item loaded
+    kBarQEmpty = 2,   // + slot: its last S of the item done
+    kBarKFull = 4,    // + stage (up to 4)
+    kBarKEmpty = 8,   // + stage
+    kBarVFull = 12,   // + stage
+    kBarVEmpty = 16,  // + stage
+    kBarSFull = 20,   // + group: S_X computed (and every earlier product)
+    kBarPFull = 22,   // + group: P_X written, O_X rescaled
+    kBarPvDone = 24,  // + group: an item's last O_X += P_X V completed
+    kBarMmaDone = 26,
+    kBarKStored = 27, // + stage: the cache writer is done with a K stage (FUSED)
+    kBarVStored = 31, // + stage: ... with a V stage
+    kBarCount = 35
 };
 
-// One work item: 256 query rows (tiles A and B) of one (sequence, head).
+// One work item: 256 query rows (two query tiles) of one (sequence, head).
 struct Item {
     int s, h, q0, qlen, ctx, q_begin;
-    int rows[2], pos0[2], n[2];      // per tile: rows, first position, key tiles
+    int sw;                          // slot x holds rows (x ^ sw) * 128 .. + 127 of the item
+    int rows[2], pos0[2], n[2];      // per slot: rows, first position, key tiles
     int n_kv;                        // key tiles loaded: the larger of n[0], n[1]
+    int f;                           // the slot served first at each key tile
 };
 
 // Lengths of one sequence and its number of items (0 for a sequence whose
@@ -475,16 +459,23 @@ __device__ __forceinline__ bool seq_info(const PrefillArgs& a, int s, bool whole
     return true;
 }
 
-// Item t of a sequence: per query tile its rows, first position and key tiles.
+// Item t of a sequence: per slot (query group) its tile's rows, first
+// position and key tiles.  Odd items put the later 128 rows (the tile with the
+// extra, diagonal key tile) in slot 0, even ones in slot 1, and the slot with
+// more key tiles is served first: the group that finishes an item first (the
+// one with fewer key tiles) takes the longer tile of the next item and leads
+// it, while the other still works through its diagonal tile and output rows.
 __device__ __forceinline__ void item_tiles(const SeqInfo& si, int t, Item& it) {
     it.q_begin = t * kRows;
+    it.sw = t & 1;
     for (int x = 0; x < 2; ++x) {
-        const int b = it.q_begin + x * kBM;
+        const int b = it.q_begin + (x ^ it.sw) * kBM;
         it.rows[x] = si.qlen - b < kBM ? (si.qlen - b > 0 ? si.qlen - b : 0) : kBM;
         it.pos0[x] = si.ctx - si.qlen + b;            // position of the tile's first query
         it.n[x] = it.rows[x] > 0 ? (it.pos0[x] + it.rows[x] - 1) / kBN + 1 : 0;
     }
     it.n_kv = it.n[1] > it.n[0] ? it.n[1] : it.n[0];
+    it.f = it.n[1] > it.n[0] ? 1 : 0;
 }
 
 // Estimated cost of an item, in tenths of a 128 x 128 tile product issued
@@ -695,27 +686,36 @@ __global__ void __launch_bounds__(threads_for(FUSED), 1)
             const int full0 = kq ? kBarKFull : kBarVFull, empty0 = kq ? kBarKEmpty : kBarVEmpty;
             const int stored0 = kq ? kBarKStored : kBarVStored;
             int64_t g = 0;
-            int items = 0;
+            int qn[2] = {0, 0};               // query tiles loaded, per slot
             bool ok = true;
             Walker wk;
             wk.init(*sched);
             Item it;
             while (ok && wk.next(a, *sched, FUSED, it)) {
-                if (kq) {
-                    // both query tiles, once the previous item's S products are done
-                    if (items > 0 && !mbar_wait(bar(kBarQEmpty), (items - 1) & 1, abort_flag)) {
+                // slot x's query tile of the item, once the slot's last S of the
+                // previous item is done: the first-served slot's before the
+                // item's first K tile, the other's after it
+                auto load_q = [&](int x) -> bool {
+                    const int n = x ? qn[1] : qn[0];
+                    if (n > 0 && !mbar_wait(bar(kBarQEmpty + x), (uint32_t)((n - 1) & 1), abort_flag))
+                        return false;
+                    mbar_expect_tx(bar(kBarQFull + x), (uint32_t)C::Q_BYTES);
+                    for (int sl = 0; sl < C::SLABS; ++sl)
+                        tma_3d(sQ + x * C::Q_BYTES + sl * C::SLAB_Q, &tm_q, sl * 64, it.h,
+                               it.q0 + it.q_begin + (x ^ it.sw) * kBM, bar(kBarQFull + x));
+                    if (x) ++qn[1]; else ++qn[0];
+                    return true;
+                };
+                if (kq && !load_q(it.f)) {
+                    ok = false;
+                    break;
+                }
+                const int32_t* row_tab = a.block_tables + (int64_t)it.s * a.max_blocks;
+                for (int j = 0; j < it.n_kv; ++j, ++g) {
+                    if (kq && j == 1 && !load_q(1 - it.f)) {
                         ok = false;
                         break;
                     }
-                    mbar_expect_tx(bar(kBarQFull), (uint32_t)(2 * C::Q_BYTES));
-                    for (int x = 0; x < 2; ++x)
-                        for (int sl = 0; sl < C::SLABS; ++sl)
-                            tma_3d(sQ + x * C::Q_BYTES + sl * C::SLAB_Q, &tm_q, sl * 64, it.h,
-                                   it.q0 + it.q_begin + x * kBM, bar(kBarQFull));
-                }
-                ++items;
-                const int32_t* row_tab = a.block_tables + (int64_t)it.s * a.max_blocks;
-                for (int j = 0; j < it.n_kv; ++j, ++g) {
                     const int st = (int)(g % NST);
                     if (g >= NST &&
                         !mbar_wait(bar(empty0 + st), (uint32_t)((g / NST - 1) & 1), abort_flag)) {
@@ -755,12 +755,14 @@ __global__ void __launch_bounds__(threads_for(FUSED), 1)
                                    y, bar(full0 + st));
                     }
                 }
+                if (ok && kq && it.n_kv == 1 && !load_q(1 - it.f)) ok = false;
             }
             if (!ok) fail();
             // let the latest copy into every stage (and the last query tiles)
             // land before the CTA can exit, whatever the other roles did (on a
             // normal run these have long landed)
-            if (kq && items > 0) mbar_wait(bar(kBarQFull), (items - 1) & 1, nullptr);
+            for (int x = 0; kq && x < 2; ++x)
+                if (qn[x] > 0) mbar_wait(bar(kBarQFull + x), (uint32_t)((qn[x] - 1) & 1), nullptr);
             for (int64_t t = g - NST < 0 ? 0 : g - NST; t < g; ++t)
                 mbar_wait(bar(full0 + (int)(t % NST)), (uint32_t)((t / NST) & 1), nullptr);
         }
@@ -866,7 +868,6 @@ __global__ void __launch_bounds__(threads_for(FUSED), 1)
             // below 256 KiB)
             const uint64_t dQ = sdesc(sQ, 16, 1024), dK = sdesc(sK, 16, 1024);
             const uint64_t dV = sdesc(sV, C::SLAB_KV, 1024);
-            int64_t gkf = 0;                 // K tiles waited for so far
             int64_t gpx[2] = {0, 0};         // P V products issued per group
             int items = 0;
             // S_X = Q_X K^T for the key tile in stage st into S_X's columns
@@ -894,25 +895,31 @@ __global__ void __launch_bounds__(threads_for(FUSED), 1)
             bool have = next_item(nit);
             while (ok && have) {
                 const Item it = nit;
-                // the last group whose S reads a key tile (B, unless B has no rows)
-                const int xl = it.n[1] > 0 ? 1 : 0;
-                if (!mbar_wait(bar(kBarQFull), (uint32_t)(items & 1), abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                // S of key tile 0
+                const int s2 = 1 - it.f;             // the slot served second
+                const int n2 = s2 ? it.n[1] : it.n[0];   // its key tiles
+                // S of key tile 0, the slot served first first; a slot's query
+                // tile is released after its last S (here when it has one key
+                // tile or none)
                 {
                     const int st = (int)(g % NST);
                     if (!mbar_wait(bar(kBarKFull + st), (uint32_t)((g / NST) & 1), abort_flag)) {
                         ok = false;
                         break;
                     }
-                    ++gkf;
                     tc_fence_after();
-                    for (int x = 0; x < 2; ++x)
-                        if (it.n[x] > 0) s_mma(x, st);
+                    for (int xi = 0; ok && xi < 2; ++xi) {
+                        const int x = xi ? s2 : it.f;
+                        const int nx = x ? it.n[1] : it.n[0];
+                        if (!mbar_wait(bar(kBarQFull + x), (uint32_t)(items & 1), abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        if (nx > 0) s_mma(x, st);
+                        if (nx <= 1) umma_commit(bar(kBarQEmpty + x));
+                    }
+                    if (!ok) break;
                     umma_commit(bar(kBarKEmpty + st));
-                    if (it.n_kv == 1) umma_commit(bar(kBarQEmpty));
                 }
                 have = next_item(nit);
                 for (int j = 0; ok && j < it.n_kv; ++j, ++g) {
@@ -924,10 +931,13 @@ __global__ void __launch_bounds__(threads_for(FUSED), 1)
                     const uint64_t dv = dV + (uint64_t)((st * C::KV_BYTES) >> 4);
                     const int stn = (int)((g + 1) % NST);
                     bool k_next = false;             // next key tile's K waited for
-                    for (int x = 0; x < 2; ++x) {
-                        if (j >= it.n[x]) continue;
+                    for (int xi = 0; xi < 2; ++xi) {
+                        const int x = xi ? s2 : it.f;
+                        const int nx = x ? it.n[1] : it.n[0];
+                        if (j >= nx) continue;
+                        const uint32_t par = (uint32_t)((x ? gpx[1] : gpx[0]) & 1);
                         // O_X += P_X(j) V_j, P_X from tensor memory
-                        if (!mbar_wait<false>(bar(kBarPFull + x), (uint32_t)(gpx[x] & 1), abort_flag)) {
+                        if (!mbar_wait<false>(bar(kBarPFull + x), par, abort_flag)) {
                             ok = false;
                             break;
                         }
@@ -942,28 +952,26 @@ __global__ void __launch_bounds__(threads_for(FUSED), 1)
                             if constexpr (kSplit)
                                 umma_ts(tmem + kColO + x * D, pa + pc + 16, vd, ID_PV, 1u);
                         }
-                        ++gpx[x];
-                        if (j == it.n[x] - 1) umma_commit(bar(kBarPvDone + x));
-                        // V_j's stage is free once its last P V (B's, or A's
-                        // where B has no tile j) completes, before the next S
-                        if (x == 1 || j >= it.n[1]) umma_commit(bar(kBarVEmpty + st));
+                        if (x) ++gpx[1]; else ++gpx[0];
+                        if (j == nx - 1) umma_commit(bar(kBarPvDone + x));
+                        // V_j's stage is free once its last P V (the second
+                        // slot's, or the first's where the second has no tile
+                        // j) completes, before the next S
+                        if (x == s2 || j >= n2) umma_commit(bar(kBarVEmpty + st));
                         // then S_X of the next key tile over P_X (in issue order)
-                        if (j + 1 < it.n[x]) {
+                        if (j + 1 < nx) {
                             if (!k_next) {
                                 if (!mbar_wait(bar(kBarKFull + stn), (uint32_t)(((g + 1) / NST) & 1),
                                                abort_flag)) {
                                     ok = false;
                                     break;
                                 }
-                                ++gkf;
                                 k_next = true;
                                 tc_fence_after();
                             }
                             s_mma(x, stn);
-                            if (x == xl || j + 1 >= it.n[1]) {
-                                umma_commit(bar(kBarKEmpty + stn));
-                                if (j + 1 == it.n_kv - 1) umma_commit(bar(kBarQEmpty));
-                            }
+                            if (j + 2 == nx) umma_commit(bar(kBarQEmpty + x));
+                            if (x == s2 || j + 1 >= n2) umma_commit(bar(kBarKEmpty + stn));
                         }
                     }
                     if (!ok) break;
@@ -977,9 +985,9 @@ __global__ void __launch_bounds__(threads_for(FUSED), 1)
         }
     } else {
         // ======================================================= softmax
-        // Warps 2..5: tile A, warps 6..9: tile B; one row per thread (warp w
+        // Warps 2..5: slot 0, warps 6..9: slot 1; one row per thread (warp w
         // reaches the lanes 32 (w % 4) .. + 31 of tensor memory).
-        const int x = (warp - 2) >> 2;               // group: tile A (0) or B (1)
+        const int x = (warp - 2) >> 2;               // the group's slot
         const int q4 = warp & 3;                     // this warp's lane quarter
         const int row = q4 * 32 + lane;              // row of the tile = TMEM lane
         const int gtid = (warp - 2 - 4 * x) * 32 + lane;   // 0..127 within the group
@@ -1000,10 +1008,10 @@ __global__ void __launch_bounds__(threads_for(FUSED), 1)
             const int pos0 = x ? it.pos0[1] : it.pos0[0];
             const int rows = x ? it.rows[1] : it.rows[0];
             // the group that zeroes V rows past the context (only the item's
-            // last key tile has any): the first group whose rows reach that
-            // tile, since its P V is issued before the other's
-            const bool a_last = it.n[0] == it.n_kv;
-            const bool zeroer = x == 0 ? a_last : !a_last;
+            // last key tile has any): the first slot served whose rows reach
+            // that tile, since its P V is issued before the other's
+            const bool f_last = (it.f ? it.n[1] : it.n[0]) == it.n_kv;
+            const bool zeroer = x == it.f ? f_last : !f_last;
             const int qpos = pos0 + row;             // causal limit of the row
             float m = -INFINITY, l = 0.f;
             for (int j = 0; j < nx; ++j, ++gx) {
@@ -1177,7 +1185,7 @@ __global__ void __launch_bounds__(threads_for(FUSED), 1)
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
             T* orow = static_cast<T*>(a.out) +
-                      ((int64_t)(it.q0 + it.q_begin + x * kBM + row) * a.H + it.h) * D;
+                      ((int64_t)(it.q0 + it.q_begin + (x ^ it.sw) * kBM + row) * a.H + it.h) * D;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t o[32];
