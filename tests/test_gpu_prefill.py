@@ -328,3 +328,12 @@ def test_prefill_bad_lengths_flagged_and_skipped(pkv):
                                              case["bt"][s:s + 1], np.array([cut], np.int32),
                                              np.array([0, rows], np.int32), 0.088, ORC_DTYPE[dt])
         attn_check(got[qs[s]:qs[s] + rows], ref, "sequence %d" % s)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_prefill_single_head(pkv, dtype):
+    """One head: the units pair heads 0 and 1, so the second CTA of every pair
+    has no head and the first computes every item; whole and continued prompts
+    of one to five 256-row items."""
+    rs = np.random.default_rng(961 + (dtype == "bf16"))
+    run_case(pkv, rs, [1200, 700, 300, 90], [1200, 513, 300, 17], 1, 128, 16, dtype)
