@@ -295,7 +295,12 @@ pkv_status pkv_paged_attention_decode_noalloc(void* out, const void* q, const vo
  * skipped and PKV_DEVERR_BAD_CONTEXT set).  max_query_len (host) bounds every
  * qlen; a larger one sets PKV_DEVERR_BAD_CONTEXT and its extra rows are not
  * written.  num_blocks * num_heads * block_size must stay below 2^31 (the
- * tiled copies address cache rows with 32-bit coordinates).
+ * tiled copies address cache rows with 32-bit coordinates).  The work is dealt
+ * to the CTAs by 64-bit sums of estimated item costs: sizes whose bound on
+ * those sums (ceil(num_heads / 2) * num_seqs * ceil(max_query_len / 256)
+ * items, each at most 20 * (max_blocks_per_seq * block_size / 128 + 1) + 24)
+ * reaches 2^60 are refused with PKV_ERR_INVALID (far beyond any call whose
+ * tensors fit in memory).
  * Fifth-generation tensor cores (tcgen05, accumulators in tensor memory, TMA
  * tiled copies through the block table), fp32 accumulation, one launch, no
  * workspace.
