@@ -363,3 +363,34 @@ def test_decode_wait_limit_setter(pkv):
     finally:
         P.set_decode_wait_limit(first)
     assert P.set_decode_wait_limit(first) == first
+
+
+def test_prefill_rejects_bad_arguments_before_touching_a_gpu(pkv):
+    """The prompt-phase calls check their sizes on the host and launch nothing
+    when a check fails, including sizes whose work-schedule cost sums could
+    overflow 64 bits."""
+    L = pkv.lib()
+    fake = 1 << 20   # never dereferenced: validation fails first
+    names = ["out", "q", "k", "v", "bt", "cl", "qs", "scale", "S", "H", "D", "B", "maxb", "nb",
+             "maxq", "T", "dtype", "stream"]
+    base = [fake, fake, fake, fake, fake, fake, fake, 0.125, 4, 8, 128, 16, 8, 64, 100, 400, 0,
+            None]
+
+    def call(**kw):
+        args = list(base)
+        for k, v in kw.items():
+            args[names.index(k)] = v
+        return L.pkv_paged_attention_prefill(*args)
+
+    assert call(D=96) == 1
+    assert call(B=4) == 1
+    assert call(maxq=-1) == 1
+    assert call(dtype=3) == 1
+    assert call(scale=float("nan")) == 1
+    assert call(maxb=1 << 28) == 1 and "overflows" in pkv.pagedkv.last_error()
+    assert call(nb=1 << 20, H=4096) == 1 and "32-bit" in pkv.pagedkv.last_error()
+    # about 10^24 estimated cost: refused before anything is looked up on a device
+    assert call(S=65535, H=65535, maxb=1 << 26, nb=1, maxq=1 << 30, T=1 << 30) == 1
+    assert "too much work" in pkv.pagedkv.last_error()
+    assert call(q=None) == 1 and "NULL" in pkv.pagedkv.last_error()
+    assert call(S=0) == 0                   # empty batch: nothing to do
