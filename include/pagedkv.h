@@ -152,7 +152,9 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* k_ca
  *   k_new, v_new  [num_seqs][num_heads][head_dim], device, 16-byte aligned.
  *   k_cache, v_cache  written at the newest token's slot of every sequence
  *                 with context_lens[s] >= 1 (nothing else is written).
- * Outputs and cache contents are bit-identical to the two-call path.  A slot
+ * Cache contents are bit-identical to the two-call path, and so are outputs
+ * with a fixed split (partition_size > 0; with the balanced split they agree
+ * within rounding, as two calls of pkv_paged_attention_decode do).  A slot
  * whose table entry is out of [0, num_blocks) is not written
  * (PKV_DEVERR_BAD_BLOCK).  Every other argument and rule is that of
  * pkv_paged_attention_decode (same workspace size); two launches on `stream`.
